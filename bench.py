@@ -1,0 +1,352 @@
+#!/usr/bin/env python
+"""Throughput of one forward+backward step of bounded-decay chunked linear
+attention through libbdla.so (C ABI), on synthetic inputs shaped like the
+64K context stage (packed, 8 documents, H=32, dk=dv=128, bf16).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead (the only reference there
+is: the pages ship no code).
+
+Launch for N GPUs: python -m torch.distributed.run --nproc-per-node N
+--master-addr 127.0.0.1 bench.py --gpus N.  Every rank runs its own replica
+of the workload (units are independent; no data-path collective): weak
+scaling, value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s fwd+bwd (T=64K,H=32,d=128 bf16); % of HBM/tensor-pipe roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="varlen64k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def algorithmic_bytes(w, n_seq):
+    """Bytes the method must move at minimum (fwd, bwd, per kernel)."""
+    th = w.B * w.T * w.H
+    units = n_seq * w.H
+    st = w.dk * w.dv * 4
+    fwd = th * (2 * w.dk * 2 + 2 * w.dv + 4 + 2 * w.dv) + units * st * (2 if w.h0_std else 1)
+    bwd = th * (2 * w.dk * 2 + 2 * w.dv * 2 + 4 + 4 * w.dk * 2 + 4 * w.dv + 4) + \
+        (units * st if w.h0_std else 0)
+    decay = th * 8
+    return {"fwd": fwd, "bwd": bwd, "decay": decay}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(inp, w, target_s: float):
+    """Times the fp64 oracle (as it stands) on a bounded sample of the
+    workload: the first document, truncated, on as many heads as the oracle
+    has threads.  Returns (tokens/s equivalent, cores, description)."""
+    import numpy as np
+
+    import oracle
+    threads = oracle.threads_used()
+    cu = inp["cu_seqlens"]
+    d0 = int(cu[1]) if cu is not None else w.T
+    nh = max(1, min(w.H, threads))
+
+    def run(T):
+        sl = lambda t: t[0, :T, :nh].double().numpy()
+        q, k, v, dO = (sl(inp[x]) for x in ("q", "k", "v", "dO"))
+        a = inp["a"][0, :T, :nh].double().numpy()
+        h0 = inp["h0"][:1, :nh].double().numpy() if inp.get("h0") is not None else None
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, a, w.b, w.mode, h0=h0)
+        oracle.bwd(q, k, v, a, dO, w.b, w.mode, h0=h0)
+        return time.perf_counter() - t0
+
+    T = min(d0, 256)
+    dt = run(T)
+    T = int(min(d0, max(T, T * target_s / max(dt, 1e-3))))
+    dt = run(T)
+    tok_s = T * nh / w.H / dt
+    desc = (f"first document truncated to {T} tokens x {nh} of {w.H} heads, fwd+bwd, "
+            f"{dt:.1f} s; tokens/s counts a token as all {w.H} heads")
+    return tok_s, threads, desc
+
+
+# ---------------------------------------------------------------- arms
+def reference_arm(args, w, inp):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    per_step = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(inp, w, per_step / 4)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, desc = oracle_sample(inp, w, per_step)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": w.name, "tokens": w.B * w.T, "H": w.H, "dk": w.dk, "dv": w.dv},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads_used(),
+                            "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def ours_arm(args, w, inp):
+    import torch
+    import torch.distributed as dist
+
+    import chunked_linear_attention_bounded_gb300 as bdla
+    from chunked_linear_attention_bounded_gb300 import bdla as B
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    bdla.lib()
+    g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    n_seq = (g["cu_seqlens"].numel() - 1) if g["cu_seqlens"] is not None else w.B
+    ws_f = B.Workspace(B.workspace_bytes(B.OP_FWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode), dev)
+    ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode), dev)
+    o = torch.empty(g["v"].shape, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((n_seq, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["v"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["a"].shape, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream()
+
+    def step(src):
+        bdla.fwd(src["q"], src["k"], src["v"], src["a"], w.b, h0=src["h0"],
+                 cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_f, out=o, hT_out=hT)
+        bdla.bwd(src["q"], src["k"], src["v"], src["a"], src["dO"], w.b, h0=src["h0"],
+                 cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_b, outs=outs)
+
+    kernels = {"decay": B.KERNEL_DECAY, "fwd": B.KERNEL_FWD, "bwd": B.KERNEL_BWD,
+               "states": B.KERNEL_STATES}
+    launches_per_step = 5   # fwd: decay + fwd;  bwd: decay + states + bwd
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step(g)
+    torch.cuda.synchronize()
+    for code in (ws_f.read_status(), ws_b.read_status()):
+        if code:
+            raise RuntimeError(f"device status {code} after warm-up")
+
+    K = args.steps
+    kev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)] for n in kernels}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(K):
+            for n, kid in kernels.items():
+                B.set_kernel_events(kid, *kev[n][i])
+            step(g)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    for kid in kernels.values():
+        B.set_kernel_events(kid, None, None)
+    ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    kernel_ms = {n: sum(a.elapsed_time(b) for a, b in kev[n]) / K for n in kernels}
+
+    # end to end through the public API with host buffers
+    host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, hT, *outs)]
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in inp.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for k_, v_ in host_in.items():
+            if v_ is not None:
+                dev_in[k_].copy_(v_, non_blocking=True)
+        step(dev_in)
+        for hst, src in zip(host_out, (o, hT, *outs)):
+            hst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    for code in (ws_f.read_status(), ws_b.read_status()):
+        if code:
+            raise RuntimeError(f"device status {code} after the timed steps")
+
+    tokens = w.B * w.T
+    value = world * tokens / (ms / 1000.0)
+    e2e_value = world * tokens / (e2e_ms / 1000.0)
+    hbm, hbm_src = peaks()
+    ab = algorithmic_bytes(w, n_seq)
+    dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
+    achieved = ab[dom] / (kernel_ms[dom] / 1000.0) / 1e9
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v_, cores, desc = oracle_sample(inp, w, args.cpu_seconds)
+            cpu = {"value": v_, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+               "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": w.name, "tokens": tokens, "docs": n_seq if inp["cu_seqlens"] is not None else w.B,
+                          "H": w.H, "dk": w.dk, "dv": w.dv, "decay": "bounded b*sigmoid(a), b=-5" if w.mode == 0 else "-softplus(a)",
+                          "l2": "inputs larger than L2 (q,k,v,dO bf16: %.2f GB)" % (4 * tokens * w.H * w.dk * 2 / 1e9),
+                          "parallelism": f"replicas x{world}"},
+               "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
+                            "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
+                            "traffic": None,
+                            "algorithmic_bytes_per_launch": ab[dom]},
+               "kernel_ms": kernel_ms,
+               "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h},
+               "gpu_launches": launches_per_step * K,
+               "clocks": clk.summary(),
+               "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS, make_inputs
+    import dataclasses
+    rank, world, _ = dist_env()
+    w = WORKLOADS[args.workload]
+    if w.fwd_only:
+        w = dataclasses.replace(w, fwd_only=False)
+    if world > 1 and args.impl == "ours":
+        w = dataclasses.replace(w, seed=w.seed + 100 * rank)
+    if args.impl == "reference" and rank != 0:
+        return
+    inp = make_inputs(w, with_grad=True)
+    if args.impl == "reference":
+        reference_arm(args, w, inp)
+    else:
+        ours_arm(args, w, inp)
+
+
+if __name__ == "__main__":
+    main()

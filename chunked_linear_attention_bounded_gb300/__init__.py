@@ -1,0 +1,11 @@
+"""Bounded-decay chunked linear attention for GB300 (sm_103a).
+
+The compute lives in libbdla.so (C ABI declared in include/bdla.h); this
+package holds the CUDA sources (csrc/), their build script, a thin ctypes
+binding and the seeded synthetic input generator.
+"""
+from .bdla import (BOUNDED, CHUNK, SOFTPLUS, BdlaError, Workspace, bwd, decay, fwd,  # noqa: F401
+                   lib, n_slots, workspace_bytes)
+
+__all__ = ["BOUNDED", "SOFTPLUS", "CHUNK", "BdlaError", "Workspace", "fwd", "bwd", "decay", "lib",
+           "n_slots", "workspace_bytes"]

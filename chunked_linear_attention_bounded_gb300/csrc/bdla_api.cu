@@ -1,0 +1,308 @@
+// C ABI of libbdla.so: argument validation, workspace carving and launches.
+// Every step of the computation runs in the kernels of this library; this
+// file only checks arguments and enqueues work on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include "bdla_internal.h"
+
+using namespace bdla;
+
+namespace bdla {
+KernelEvents g_kernel_events[BDLA_KERNEL_COUNT];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+    size_t gamma = 0;    // offset of Gamma [tokens, H] fp32
+    size_t states = 0;   // offset of the per-tile states (backward), 0 if unused
+    size_t total = 0;
+};
+
+int64_t total_tokens(const bdla_dims &d) { return (int64_t)d.B * d.T; }
+
+// Backward needs the state before every 16-token tile; it uses caller
+// checkpoints when their stride is exactly 16.
+bool bwd_needs_states(int ckpt_stride) { return ckpt_stride != kChunk; }
+
+Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
+{
+    Layout L;
+    size_t off = round_up(kStatusBytes);
+    const int64_t tokens = total_tokens(d);
+    L.gamma = off;
+    off += round_up((size_t)tokens * d.H * sizeof(float));
+    if (op == BDLA_OP_BWD && bwd_needs_states(ckpt_stride)) {
+        const int64_t slots = (tokens + kChunk - 1) / kChunk + n_docs;
+        L.states = off;
+        off += round_up((size_t)d.H * slots * d.dk * d.dv * sizeof(float));
+    }
+    L.total = off;
+    return L;
+}
+
+bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs)
+{
+    if (d.T < 0 || d.H < 1 || d.B < 1)
+        return BDLA_ERR_SHAPE;
+    if (varlen && (d.B != 1 || n_docs < 1))
+        return BDLA_ERR_SHAPE;
+    if (d.dk != 64 && d.dk != 128)
+        return BDLA_ERR_UNSUPPORTED;
+    if (d.dv != 64 && d.dv != 128 && d.dv != 256)
+        return BDLA_ERR_UNSUPPORTED;
+    return BDLA_OK;
+}
+
+bdla_status check_decay(float b, int chunk, int mode)
+{
+    if (chunk != kChunk)
+        return BDLA_ERR_UNSUPPORTED;
+    if (mode != BDLA_DECAY_BOUNDED_SIGMOID && mode != BDLA_DECAY_NEG_SOFTPLUS)
+        return BDLA_ERR_UNSUPPORTED;
+    if (mode == BDLA_DECAY_BOUNDED_SIGMOID) {
+        if (!isfinite(b) || b > 0.0f)
+            return BDLA_ERR_RANGE;
+        // the bound must keep e^{-Gamma} = e^{chunk |b|} representable
+        if ((double)chunk * fabs((double)b) > 80.0)
+            return BDLA_ERR_RANGE;
+    }
+    return BDLA_OK;
+}
+
+bdla_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (ws == nullptr || ws_bytes < need || !aligned16(ws))
+        return BDLA_ERR_WORKSPACE;
+    return BDLA_OK;
+}
+
+Problem make_problem(const bdla_dims &d, const int32_t *cu, int n_docs, float b, int mode,
+                     void *ws, void *stream)
+{
+    Problem p;
+    p.cu = cu;
+    p.n_docs = cu ? n_docs : d.B;
+    p.T = cu ? d.T : d.T;
+    p.tokens = total_tokens(d);
+    p.H = d.H;
+    p.dk = d.dk;
+    p.dv = d.dv;
+    p.b = b;
+    p.mode = mode;
+    p.st = reinterpret_cast<DeviceStatus *>(ws);
+    p.stream = reinterpret_cast<cudaStream_t>(stream);
+    return p;
+}
+
+#define BDLA_TRY(expr)                                                                             \
+    do {                                                                                           \
+        bdla_status s_ = (expr);                                                                   \
+        if (s_ != BDLA_OK)                                                                         \
+            return s_;                                                                             \
+    } while (0)
+
+#define BDLA_CUDA(expr)                                                                            \
+    do {                                                                                           \
+        if ((expr) != cudaSuccess)                                                                 \
+            return BDLA_ERR_CUDA;                                                                  \
+    } while (0)
+
+bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a, float b,
+                     int chunk, const int32_t *cu, int n_docs, bool varlen, const float *h0,
+                     void *o, bdla_dtype o_dtype, float *hT, float *ckpt, int ckpt_stride,
+                     bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_dims(d, varlen, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    const bool any_tokens = total_tokens(d) > 0;
+    if ((any_tokens && (!q || !k || !v || !a || !o)) || (varlen && !cu))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
+        !aligned16(hT) || !aligned16(ckpt) || !aligned16(a))
+        return BDLA_ERR_ALIGN;
+    if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
+        return BDLA_ERR_UNSUPPORTED;
+    if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
+        return BDLA_ERR_SHAPE;
+    const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, ckpt_stride);
+    BDLA_TRY(check_ws(ws, ws_bytes, L.total));
+    Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
+    float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
+    mark_start(BDLA_KERNEL_DECAY, p.stream);
+    BDLA_CUDA(launch_decay(p, a, gamma));
+    mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    mark_start(BDLA_KERNEL_FWD, p.stream);
+    BDLA_CUDA(launch_fwd_tile(p, static_cast<const __nv_bfloat16 *>(q),
+                              static_cast<const __nv_bfloat16 *>(k),
+                              static_cast<const __nv_bfloat16 *>(v), gamma, h0, o,
+                              o_dtype == BDLA_F32, hT, ckpt, ckpt_stride));
+    mark_stop(BDLA_KERNEL_FWD, p.stream);
+    return BDLA_OK;
+}
+
+bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a, float b,
+                     int chunk, const int32_t *cu, int n_docs, bool varlen, const float *h0,
+                     const void *dO, const float *dhT, const float *ckpt, int ckpt_stride,
+                     float *dq, float *dk, float *dv, float *da, float *dh0, bdla_dims d,
+                     bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_dims(d, varlen, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    const bool any_tokens = total_tokens(d) > 0;
+    if ((any_tokens && (!q || !k || !v || !a || !dO || !dq || !dk || !dv || !da)) ||
+        (varlen && !cu))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || !aligned16(da) || !aligned16(a) ||
+        !aligned16(h0) || !aligned16(dhT) || !aligned16(ckpt) || !aligned16(dh0))
+        return BDLA_ERR_ALIGN;
+    if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
+        return BDLA_ERR_SHAPE;
+    const int stride = ckpt ? ckpt_stride : 0;
+    const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride);
+    BDLA_TRY(check_ws(ws, ws_bytes, L.total));
+    Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
+    float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    mark_start(BDLA_KERNEL_DECAY, p.stream);
+    BDLA_CUDA(launch_decay(p, a, gamma));
+    mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    const float *states = ckpt;
+    if (bwd_needs_states(stride)) {
+        float *st = reinterpret_cast<float *>(static_cast<char *>(ws) + L.states);
+        mark_start(BDLA_KERNEL_STATES, p.stream);
+        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, st, kChunk));
+        mark_stop(BDLA_KERNEL_STATES, p.stream);
+        states = st;
+    }
+    mark_start(BDLA_KERNEL_BWD, p.stream);
+    BDLA_CUDA(launch_bwd_tile(p, qb, kb, vb, a, gamma, static_cast<const __nv_bfloat16 *>(dO),
+                              dhT, states, dq, dk, dv, da, dh0));
+    mark_stop(BDLA_KERNEL_BWD, p.stream);
+    return BDLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mode, int ckpt_stride)
+{
+    (void)mode;
+    const bool varlen = n_docs > 0;
+    if (check_dims(d, varlen, n_docs) != BDLA_OK)
+        return 0;
+    return layout(op, d, varlen ? n_docs : d.B, ckpt_stride).total;
+}
+
+bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seqlens, int n_docs,
+                       float *gamma, bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
+                       void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    if (d.T < 0 || d.H < 1 || d.B < 1 || (varlen && (d.B != 1 || n_docs < 1)))
+        return BDLA_ERR_SHAPE;
+    BDLA_TRY(check_decay(b, chunk, mode));
+    if (!a || !gamma)
+        return BDLA_ERR_NULL;
+    BDLA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+    bdla_dims dd = d;
+    dd.dk = 64;
+    dd.dv = 64;
+    Problem p = make_problem(dd, cu_seqlens, n_docs, b, mode, ws, stream);
+    BDLA_CUDA(launch_decay(p, a, gamma));
+    return BDLA_OK;
+}
+
+bdla_status bdla_fwd(const void *q, const void *k, const void *v, const float *a, float b,
+                     int chunk, const float *h0, void *o, bdla_dtype o_dtype, float *hT,
+                     float *ckpt, int ckpt_stride, bdla_dims d, bdla_decay_mode mode, void *ws,
+                     size_t ws_bytes, void *stream)
+{
+    return fwd_impl(q, k, v, a, b, chunk, nullptr, 0, false, h0, o, o_dtype, hT, ckpt,
+                    ckpt_stride, d, mode, ws, ws_bytes, stream);
+}
+
+bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const float *a, float b,
+                            int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
+                            void *o, bdla_dtype o_dtype, float *hT, float *ckpt, int ckpt_stride,
+                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+{
+    return fwd_impl(q, k, v, a, b, chunk, cu_seqlens, n_docs, true, h0, o, o_dtype, hT, ckpt,
+                    ckpt_stride, d, mode, ws, ws_bytes, stream);
+}
+
+bdla_status bdla_bwd(const void *q, const void *k, const void *v, const float *a, float b,
+                     int chunk, const float *h0, const void *dO, const float *dhT,
+                     const float *ckpt, int ckpt_stride, float *dq, float *dk, float *dv,
+                     float *da, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
+                     size_t ws_bytes, void *stream)
+{
+    return bwd_impl(q, k, v, a, b, chunk, nullptr, 0, false, h0, dO, dhT, ckpt, ckpt_stride, dq,
+                    dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
+}
+
+bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const float *a, float b,
+                            int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
+                            const void *dO, const float *dhT, const float *ckpt, int ckpt_stride,
+                            float *dq, float *dk, float *dv, float *da, float *dh0, bdla_dims d,
+                            bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+{
+    return bwd_impl(q, k, v, a, b, chunk, cu_seqlens, n_docs, true, h0, dO, dhT, ckpt,
+                    ckpt_stride, dq, dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
+}
+
+bdla_status bdla_read_status(void *ws, void *stream)
+{
+    if (ws == nullptr)
+        return BDLA_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    unsigned int code = 0;
+    if (cudaMemcpy(&code, ws, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    if (code != 0 && cudaMemset(ws, 0, kStatusBytes) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    return static_cast<bdla_status>(code);
+}
+
+const char *bdla_status_string(bdla_status s)
+{
+    switch (s) {
+    case BDLA_OK: return "ok";
+    case BDLA_ERR_NULL: return "a required pointer is NULL";
+    case BDLA_ERR_SHAPE: return "a size is negative or inconsistent";
+    case BDLA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case BDLA_ERR_RANGE: return "decay bound out of range (b > 0, not finite, or chunk*|b| > 80)";
+    case BDLA_ERR_UNSUPPORTED: return "unsupported chunk, head width or decay mode";
+    case BDLA_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
+    case BDLA_ERR_CUDA: return "a CUDA runtime call failed";
+    case BDLA_ERR_TIMEOUT: return "device: a bounded wait expired";
+    case BDLA_ERR_DEVICE: return "device: malformed cu_seqlens or another device-side check";
+    }
+    return "unknown status";
+}
+
+bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event)
+{
+    if (kernel < 0 || kernel >= BDLA_KERNEL_COUNT)
+        return BDLA_ERR_SHAPE;
+    g_kernel_events[kernel].start = reinterpret_cast<cudaEvent_t>(start_event);
+    g_kernel_events[kernel].stop = reinterpret_cast<cudaEvent_t>(stop_event);
+    return BDLA_OK;
+}
+
+int bdla_version(void) { return 100; }
+
+}  // extern "C"

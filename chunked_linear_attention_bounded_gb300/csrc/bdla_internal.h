@@ -1,0 +1,62 @@
+// Host-side launcher interface between the C ABI (bdla_api.cu) and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bdla_common.cuh"
+
+namespace bdla {
+
+struct Problem {
+    const int32_t *cu;   // device cu_seqlens or nullptr (fixed-length)
+    int n_docs;          // documents (B for fixed-length calls)
+    int T;               // per-document length (fixed) or total tokens (varlen)
+    int64_t tokens;      // total tokens in the tensors
+    int H, dk, dv;
+    float b;
+    int mode;            // bdla_decay
+    DeviceStatus *st;
+    cudaStream_t stream;
+};
+
+// Slots of a checkpoint array with the given stride.
+inline int64_t ckpt_slots(const Problem &p, int stride)
+{
+    return (p.tokens + stride - 1) / stride + p.n_docs;
+}
+
+// Events recorded around a kernel's launches (measurement hook, see
+// bdla_set_kernel_events); null when unset.
+struct KernelEvents {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+extern KernelEvents g_kernel_events[BDLA_KERNEL_COUNT];
+
+inline void mark_start(int kernel, cudaStream_t s)
+{
+    if (g_kernel_events[kernel].start)
+        cudaEventRecord(g_kernel_events[kernel].start, s);
+}
+inline void mark_stop(int kernel, cudaStream_t s)
+{
+    if (g_kernel_events[kernel].stop)
+        cudaEventRecord(g_kernel_events[kernel].stop, s);
+}
+
+cudaError_t launch_decay(const Problem &p, const float *a, float *gamma);
+
+// Tile-serial forward.  o may be nullptr (states-only pass that fills ckpt).
+cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                            const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
+                            int o_f32, float *hT, float *ckpt, int ckpt_stride);
+
+// Tile-serial backward; `states` holds the state before every 16-token tile
+// (checkpoint layout with stride 16).
+cudaError_t launch_bwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                            const __nv_bfloat16 *v, const float *a, const float *gamma,
+                            const __nv_bfloat16 *dO, const float *dhT, const float *states,
+                            float *dq, float *dk, float *dv, float *da, float *dh0);
+
+}  // namespace bdla

@@ -1,0 +1,178 @@
+/*
+ * bdla.h — C ABI of the bounded-decay chunked linear attention library
+ * (libbdla.so, CUDA, sm_103a).
+ *
+ * The operation.  Gated linear attention with one scalar decay per (token,
+ * head), evaluated in 16-token tiles ("Engineering Long-Context Training for
+ * Trillion-Parameter MoE Models: Three Key Breakthroughs", sec. 3.1: matmuls
+ * inside a tile, a recurrent state passed between tiles).  For every document
+ * n and head h, with doc-local tokens t = 1..L:
+ *     lambda_t = log g_t = b * sigmoid(a_t)        BDLA_DECAY_BOUNDED_SIGMOID
+ *     lambda_t = -softplus(a_t)                    BDLA_DECAY_NEG_SOFTPLUS
+ *     S_t = exp(lambda_t) S_{t-1} + k_t v_t^T,  S_0 = h0,  o_t = S_t^T q_t,
+ *     hT = S_L.
+ * The bounded form (same page, sec. 3.2; "Scaling Trillion-Parameter MoE and
+ * Long-Context LLMs", sec. II) keeps the cumulative log-decay Gamma inside a
+ * 16-token tile in [16 b, 0] = [-80, 0] for b = -5, so exp(+-Gamma) is finite
+ * in bf16/fp32 and every tile, diagonal included, goes through the same
+ * tensor-core GEMMs.  The -softplus form is the unbounded ablation: its
+ * diagonal tiles take an explicit element-wise position-pair path.
+ * No 1/sqrt(dk) scaling is applied (scale q beforehand).  b is a constant:
+ * no gradient flows to it.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    feature dimension innermost.  The library never allocates, frees or
+ *    synchronises on these calls; its scratch comes from the caller's `ws`.
+ *  - q, k, v, dO, o and the workspace must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream); every call is
+ *    asynchronous and stream-ordered.
+ *  - Host-detectable errors return a status before any launch.  Errors found
+ *    on the device (a bounded wait that expired, malformed cu_seqlens) are
+ *    recorded in a status word inside `ws`; read it with bdla_read_status.
+ *
+ * Shapes (bdla_dims): fixed-length calls take [B, T, H, d] tensors; the
+ * _varlen calls take packed documents [1, T, H, d] with B = 1, T = total
+ * tokens and device int32 cu_seqlens[n_docs + 1] (cu[0] = 0, non-decreasing,
+ * cu[n_docs] = T).  Tiles restart at each document start; the last tile of a
+ * document may be shorter than 16.  For fixed-length calls the documents are
+ * the B rows (n_docs = B).
+ *   q, k      bf16  [B, T, H, dk]          dk in {64, 128}
+ *   v, dO     bf16  [B, T, H, dv]          dv in {64, 128, 256}
+ *   a, da     fp32  [B, T, H]              decay logits and their gradient
+ *   o         bf16 or fp32 [B, T, H, dv]
+ *   dq, dk    fp32  [B, T, H, dk];  dv fp32 [B, T, H, dv]
+ *   h0, hT, dh0, dhT   fp32 [n_docs, H, dk, dv]   (NULL = zero / not wanted)
+ *   ckpt      fp32  [H, n_slots, dk, dv], n_slots = ceil(B*T / stride) + n_docs;
+ *             slot floor(cu[n] / stride) + n + c holds the state of document n
+ *             before its doc-local token c*stride (slot c = 0 holds h0).
+ */
+#ifndef BDLA_H
+#define BDLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BDLA_OK = 0,
+    BDLA_ERR_NULL = 1,         /* a required pointer is NULL */
+    BDLA_ERR_SHAPE = 2,        /* a size is negative or inconsistent */
+    BDLA_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+    BDLA_ERR_RANGE = 4,        /* b > 0, b not finite, or chunk*|b| > 80 (bounded) */
+    BDLA_ERR_UNSUPPORTED = 5,  /* chunk != 16, dk/dv outside the supported set */
+    BDLA_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or too small */
+    BDLA_ERR_CUDA = 7,         /* a CUDA runtime call (launch, attribute) failed */
+    BDLA_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up */
+    BDLA_ERR_DEVICE = 9        /* device: malformed cu_seqlens or another device check */
+} bdla_status;
+
+typedef enum {
+    BDLA_DECAY_BOUNDED_SIGMOID = 0,  /* lambda = b * sigmoid(a), b in [-80/chunk, 0] */
+    BDLA_DECAY_NEG_SOFTPLUS = 1      /* lambda = -softplus(a); ablation, b ignored */
+} bdla_decay_mode;
+
+typedef enum { BDLA_BF16 = 0, BDLA_F32 = 1 } bdla_dtype;
+
+typedef struct {
+    int B;   /* documents (fixed-length calls) or 1 (varlen calls) */
+    int T;   /* tokens per document (fixed) or total packed tokens (varlen) */
+    int H;   /* heads */
+    int dk;  /* key / query width */
+    int dv;  /* value width */
+} bdla_dims;
+
+enum { BDLA_OP_FWD = 0, BDLA_OP_BWD = 1, BDLA_OP_DECAY = 2 };
+
+/*
+ * Bytes of device workspace an op needs.  `op` is BDLA_OP_*, `n_docs` the
+ * document count of a varlen call (0 for fixed-length calls), `ckpt_stride`
+ * the stride of the checkpoints the backward will be handed (0 if none).
+ * Returns 0 on invalid dims.  The first 256 bytes of every workspace are the
+ * device status word: zero them once after allocating the workspace
+ * (bdla_read_status clears them again).
+ */
+size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mode, int ckpt_stride);
+
+/*
+ * Decay kernel (the tile-local part of the method, sec. 3.1-3.2 of the first
+ * page): gamma[t, h] = sum of lambda over the doc-local 16-token tile of t,
+ * from the tile start through t (inclusive).  a, gamma: fp32 [B, T, H].
+ * cu_seqlens may be NULL for fixed-length inputs (then n_docs is ignored).
+ */
+bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seqlens,
+                       int n_docs, float *gamma, bdla_dims d, bdla_decay_mode mode,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Forward pass.  Writes o (dtype o_dtype) and, when non-NULL, hT and the
+ * state checkpoints ckpt every ckpt_stride tokens (ckpt_stride a multiple of
+ * 16; ignored when ckpt is NULL).
+ */
+bdla_status bdla_fwd(const void *q, const void *k, const void *v, const float *a,
+                     float b, int chunk, const float *h0,
+                     void *o, bdla_dtype o_dtype, float *hT,
+                     float *ckpt, int ckpt_stride,
+                     bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
+
+bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const float *a,
+                            float b, int chunk, const int32_t *cu_seqlens, int n_docs,
+                            const float *h0, void *o, bdla_dtype o_dtype, float *hT,
+                            float *ckpt, int ckpt_stride,
+                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/*
+ * Backward pass of the loss L with upstream gradients dO = dL/do and
+ * dhT = dL/dhT (NULL = 0).  Writes dq, dk, dv, da (dL/da through the decay
+ * parameterisation) and, when non-NULL, dh0.  ckpt (with its ckpt_stride) may
+ * hold the forward's state checkpoints; NULL makes the backward recompute the
+ * states it needs into the workspace.
+ */
+bdla_status bdla_bwd(const void *q, const void *k, const void *v, const float *a,
+                     float b, int chunk, const float *h0, const void *dO, const float *dhT,
+                     const float *ckpt, int ckpt_stride,
+                     float *dq, float *dk, float *dv, float *da, float *dh0,
+                     bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
+
+bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const float *a,
+                            float b, int chunk, const int32_t *cu_seqlens, int n_docs,
+                            const float *h0, const void *dO, const float *dhT,
+                            const float *ckpt, int ckpt_stride,
+                            float *dq, float *dk, float *dv, float *da, float *dh0,
+                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/*
+ * Synchronises `stream`, returns the device status word recorded in `ws` by
+ * earlier calls (BDLA_OK if none) and clears it.  BDLA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+bdla_status bdla_read_status(void *ws, void *stream);
+
+/*
+ * Measurement hook.  Until called again with NULL events, every later call
+ * that launches kernel `kernel` (BDLA_KERNEL_*) records `start_event` just
+ * before and `stop_event` just after that launch, on the call's stream, so
+ * the caller can time the kernel alone (cudaEventElapsedTime).  Both events
+ * are cudaEvent_t created by the caller.  Not thread-safe; meant for
+ * benchmarks.  Returns BDLA_ERR_SHAPE for an unknown kernel id.
+ */
+enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KERNEL_STATES = 3,
+       BDLA_KERNEL_COUNT = 4 };
+bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
+
+/* Static English description of a status code. */
+const char *bdla_status_string(bdla_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bdla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BDLA_H */

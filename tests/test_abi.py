@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/bdla.h declares, sizes its workspace, and rejects bad arguments on
+the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_linear_attention_bounded_gb300 as pkg
+from chunked_linear_attention_bounded_gb300 import bdla
+from chunked_linear_attention_bounded_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return bdla.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "bdla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(bdla_\w+)\s*\(", src))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert declared == set(bdla.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    for code in range(10):
+        assert bdla.status_string(code) not in ("", "unknown status")
+    assert bdla.status_string(123) == "unknown status"
+    assert L.bdla_version() >= 100
+
+
+def test_workspace_bytes(L):
+    fwd = bdla.workspace_bytes(bdla.OP_FWD, (1, 65536, 32, 128), 128, n_docs=8)
+    assert fwd >= 256 + 65536 * 32 * 4
+    bwd = bdla.workspace_bytes(bdla.OP_BWD, (1, 65536, 32, 128), 128, n_docs=8)
+    bwd16 = bdla.workspace_bytes(bdla.OP_BWD, (1, 65536, 32, 128), 128, n_docs=8, ckpt_stride=16)
+    assert bwd >= bwd16 >= fwd
+    assert bdla.workspace_bytes(bdla.OP_FWD, (1, 16, 2, 96), 64) == 0      # dk 96 unsupported
+    assert bdla.workspace_bytes(bdla.OP_FWD, (1, 16, 2, 64), 32) == 0      # dv 32 unsupported
+
+
+# Non-NULL, aligned, never dereferenced: every call below is rejected by a host
+# check before any launch (none of them may reach a kernel).
+FAKE = ctypes.c_void_p(1 << 20)
+
+
+def _fwd(L, b=-5.0, chunk=16, dims=(1, 64, 2, 64, 64), mode=0, q=FAKE, ws=FAKE, ws_bytes=1 << 40,
+         ckpt=None, stride=0, o_dtype=0):
+    return L.bdla_fwd(q, FAKE, FAKE, FAKE, b, chunk, None, FAKE, o_dtype, None, ckpt, stride,
+                      bdla.Dims(*dims), mode, ws, ws_bytes, None)
+
+
+def test_host_validation_before_launch(L):
+    assert _fwd(L, chunk=32) == 5                     # chunk != 16
+    assert _fwd(L, b=0.5) == 4                        # b > 0
+    assert _fwd(L, b=float("nan")) == 4
+    assert _fwd(L, b=-5.5) == 4                       # 16 * 5.5 > 80
+    assert _fwd(L, b=-9.0, mode=1, ws_bytes=16) == 6  # ablation ignores b; stops at the ws check
+    assert _fwd(L, mode=7) == 5
+    assert _fwd(L, dims=(1, 64, 2, 96, 64)) == 5
+    assert _fwd(L, dims=(1, -1, 2, 64, 64)) == 2
+    assert _fwd(L, dims=(0, 64, 2, 64, 64)) == 2
+    assert _fwd(L, q=None) == 1
+    assert _fwd(L, q=ctypes.c_void_p((1 << 20) + 8)) == 3
+    assert _fwd(L, ws=None) == 6
+    assert _fwd(L, ws_bytes=16) == 6
+    assert _fwd(L, ckpt=FAKE, stride=24) == 2
+    assert _fwd(L, o_dtype=5) == 5
+    st = L.bdla_bwd(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, None, None, None, 0, FAKE, FAKE, FAKE,
+                    FAKE, None, bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
+    assert st == 1                                    # dO missing
+    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 2, None, FAKE, 0, None, None, 0,
+                           bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
+    assert st == 1                                    # cu_seqlens missing
+    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, FAKE, 2, None, FAKE, 0, None, None, 0,
+                           bdla.Dims(2, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
+    assert st == 2                                    # varlen needs B == 1
+
+
+def test_package_exports():
+    for name in ("fwd", "bwd", "decay", "Workspace", "BdlaError"):
+        assert hasattr(pkg, name)

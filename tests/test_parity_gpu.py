@@ -1,0 +1,161 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded bytes.  Bar per tensor: relative L2 <= 5e-3 and max-abs
+<= 2e-2 * max|ref| (o, hT, dq, dk, dv, da, dh0)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_linear_attention_bounded_gb300 import bdla
+from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS, Workload, make_inputs, small_variant
+
+from _parity import (assert_close, compare_all, cu_of, flat64, heads64, run_gpu, run_oracle,
+                     to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(name, T, H=2, n_docs=None, **kw):
+    w = small_variant(WORKLOADS[name], T=T, H=H, n_docs=n_docs)
+    return dataclasses.replace(w, **kw) if kw else w
+
+
+@pytest.mark.parametrize("mode", [bdla.BOUNDED, bdla.SOFTPLUS])
+def test_decay_kernel_tile_cumsum(mode):
+    w = _small("varlen64k", T=777, H=3, n_docs=4, mode=mode, a_std=3.0)
+    inp = make_inputs(w, with_grad=False)
+    g = to_device(inp)
+    gamma = bdla.decay(g["a"], w.b, cu_seqlens=g["cu_seqlens"], mode=mode).cpu().double().numpy()[0]
+    lam = oracle.log_decay(inp["a"].double().numpy()[0], w.b, mode)
+    ref = np.zeros_like(lam)
+    cu = inp["cu_seqlens"].numpy()
+    for n in range(len(cu) - 1):
+        for c0 in range(cu[n], cu[n + 1], 16):
+            c1 = min(c0 + 16, cu[n + 1])
+            ref[c0:c1] = np.cumsum(lam[c0:c1], axis=0)
+    np.testing.assert_allclose(gamma, ref, rtol=2e-5, atol=2e-5)
+    if mode == bdla.BOUNDED:
+        assert gamma.min() >= 16 * w.b - 1e-3 and gamma.max() <= 0.0
+
+
+CASES = [
+    # name, T, H, n_docs, dk, dv
+    ("c8k", 300, 2, None, 128, 128),
+    ("varlen64k", 700, 2, 3, 128, 128),
+    ("c256k", 290, 2, None, 128, 256),
+    ("pr1", 333, 2, None, 64, 64),
+    ("c8k", 200, 3, None, 64, 128),
+    ("c8k", 150, 2, None, 128, 64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-T{c[1]}-dk{c[4]}-dv{c[5]}")
+@pytest.mark.parametrize("mode", [bdla.BOUNDED, bdla.SOFTPLUS])
+def test_fwd_bwd_small(case, mode):
+    name, T, H, nd, dk, dv = case
+    kw = dict(dk=dk, dv=dv, mode=mode, fwd_only=False)
+    if mode == bdla.SOFTPLUS:
+        kw.update(a_mean=2.0, a_std=2.0)
+    w = _small(name, T, H, nd, **kw)
+    inp = make_inputs(w, with_grad=True)
+    n_seq = (inp["cu_seqlens"].numel() - 1) if inp["cu_seqlens"] is not None else w.B
+    dhT = torch.randn((n_seq, H, dk, dv), generator=torch.Generator().manual_seed(5)) * 0.1
+    gpu = run_gpu(to_device(inp), w.b, mode, dhT=dhT.cuda())
+    ref = run_oracle(inp, w.b, mode, dhT=dhT)
+    compare_all(gpu, ref)
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 33, 128, 129])
+def test_edge_lengths(T):
+    w = _small("c8k", T, H=2, dk=64, dv=64, h0_std=0.3)
+    w = dataclasses.replace(w, B=2)
+    inp = make_inputs(w, with_grad=True)
+    gpu = run_gpu(to_device(inp), w.b, w.mode, o_dtype=torch.float32)
+    ref = run_oracle(inp, w.b, w.mode)
+    compare_all(gpu, ref)
+
+
+def test_fp32_output_matches_tightly():
+    w = WORKLOADS["pr1"]
+    inp = make_inputs(w)
+    gpu = run_gpu(to_device(inp), w.b, w.mode, with_grad=False, o_dtype=torch.float32)
+    ref = run_oracle(inp, w.b, w.mode, with_grad=False)
+    errs = compare_all(gpu, ref)
+    assert errs["o"] < 5e-3
+
+
+def test_varlen_with_empty_documents():
+    w = _small("varlen64k", 200, H=2, n_docs=3)
+    inp = make_inputs(w, with_grad=True)
+    inp["cu_seqlens"] = torch.tensor([0, 0, 37, 37, 150, 200, 200], dtype=torch.int32)
+    inp["h0"] = torch.randn((6, 2, 128, 128), generator=torch.Generator().manual_seed(3)) * 0.1
+    gpu = run_gpu(to_device(inp), w.b, w.mode)
+    ref = run_oracle(inp, w.b, w.mode)
+    compare_all(gpu, ref)
+
+
+def test_zero_tokens_passes_state_through():
+    h0 = torch.randn((2, 2, 64, 64), device="cuda")
+    z = lambda *s, dt=torch.bfloat16: torch.zeros(s, dtype=dt, device="cuda")
+    o, hT, _ = bdla.fwd(z(2, 0, 2, 64), z(2, 0, 2, 64), z(2, 0, 2, 64), z(2, 0, 2, dt=torch.float32),
+                        h0=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(hT, h0)
+
+
+def test_checkpoints_are_prefix_states_and_feed_the_backward():
+    w = _small("c256k", 200, H=2, dk=64, dv=128, h0_std=0.2)
+    inp = make_inputs(w, with_grad=True)
+    g = to_device(inp)
+    gpu = run_gpu(g, w.b, w.mode, ckpt_stride=16, bwd_ckpt=True)
+    ck = gpu["ckpt"].cpu().double().numpy()          # [H, slots, dk, dv]
+    q, k, v, a = (flat64(inp[x]) for x in ("q", "k", "v", "a"))
+    h0 = heads64(inp["h0"], None)
+    for c in range(0, 200 // 16 + 1):
+        t = c * 16
+        if t >= 200:
+            break
+        _, st = oracle.fwd(q[:t], k[:t], v[:t], a[:t], w.b, w.mode, h0=h0, cu_seqlens=[0, t])
+        assert_close(f"ckpt[{c}]", ck[:, c], st[0])
+    recompute = run_gpu(g, w.b, w.mode)
+    for n in ("dq", "dk", "dv", "da", "dh0"):
+        assert_close(n, gpu[n].cpu().numpy(), recompute[n].cpu().numpy(), rel=1e-5, max_abs=1e-5)
+
+
+@pytest.mark.parametrize("cu", [[0, 100, 50, 300], [0, 100, 200], [0, 500]])
+def test_bad_cu_seqlens_set_device_status(cu):
+    w = _small("varlen64k", 300, H=2, n_docs=2)
+    inp = make_inputs(w, with_grad=False)
+    g = to_device(inp)
+    g["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ws = bdla.Workspace(1 << 20, "cuda")
+    bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=g["cu_seqlens"], ws=ws)
+    assert ws.read_status() == 9
+    assert ws.read_status() == 0          # cleared after reading
+    # the context is still usable
+    o, _, _ = bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=g["cu_seqlens"][:1].new_tensor([0, 300]), ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+
+
+# Full-size workloads: the GPU runs the whole input, the oracle checks a
+# sample of heads (every document of those heads, every token).
+FULL = [("pr1", None), ("c8k", [0, 9]), ("varlen64k", [0, 17, 31]), ("c256k", [5]), ("c1m", [3]),
+        ("c1m_ablation", [6])]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,heads", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workload(name, heads):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    g = to_device(inp)
+    with_grad = not w.fwd_only
+    gpu = run_gpu(g, w.b, w.mode, with_grad=with_grad,
+                  o_dtype=torch.float32 if w.o_f32 else torch.bfloat16,
+                  ckpt_stride=w.ckpt_stride, bwd_ckpt=bool(w.ckpt_stride))
+    del g
+    ref = run_oracle(inp, w.b, w.mode, heads=heads, with_grad=with_grad)
+    compare_all(gpu, ref, heads=heads)
