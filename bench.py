@@ -240,6 +240,10 @@ def ours_arm(args, w, inp):
     K = args.steps
     kev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)] for n in kernels}
+    for pairs in kev.values():      # torch creates the CUDA event on first record
+        for a_, b_ in pairs:
+            a_.record(stream)
+            b_.record(stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
