@@ -165,10 +165,11 @@ def _ws_for(op, q, v, n_docs, mode, ckpt_stride, ws: Optional[Workspace]) -> Wor
 
 def decay(a: torch.Tensor, b: float = -5.0, cu_seqlens: Optional[torch.Tensor] = None,
           mode: int = BOUNDED, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
-    """Tile-local inclusive cumsum Gamma of the log-decay, fp32 [B, T, H]."""
+    """Tile-local inclusive cumsum Gamma of the log-decay, fp32 [H, B*T]
+    (head-major)."""
     _check(a, "a", torch.float32, 3)
     B, T, H = a.shape
-    gamma = torch.empty_like(a)
+    gamma = torch.empty((H, B * T), dtype=torch.float32, device=a.device)
     n_docs = 0
     if cu_seqlens is not None:
         _check(cu_seqlens, "cu_seqlens", torch.int32, 1)

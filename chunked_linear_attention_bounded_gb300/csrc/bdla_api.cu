@@ -21,7 +21,7 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-    size_t gamma = 0;    // offset of Gamma [tokens, H] fp32
+    size_t gamma = 0;    // offset of Gamma [H, tokens] fp32
     size_t states = 0;   // offset of the per-tile states (backward), 0 if unused
     size_t total = 0;
 };
@@ -137,14 +137,21 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
     float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma));
+    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     mark_start(BDLA_KERNEL_FWD, p.stream);
-    BDLA_CUDA(launch_fwd_tile(p, static_cast<const __nv_bfloat16 *>(q),
-                              static_cast<const __nv_bfloat16 *>(k),
-                              static_cast<const __nv_bfloat16 *>(v), gamma, h0, o,
-                              o_dtype == BDLA_F32, hT, ckpt, ckpt_stride));
+    BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT, ckpt,
+                               ckpt_stride));
     mark_stop(BDLA_KERNEL_FWD, p.stream);
+    if (ckpt && ckpt_stride % 128 != 0) {
+        // checkpoints inside the 128-token blocks: tile-serial state pass
+        mark_start(BDLA_KERNEL_STATES, p.stream);
+        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, ckpt, ckpt_stride));
+        mark_stop(BDLA_KERNEL_STATES, p.stream);
+    }
     return BDLA_OK;
 }
 
@@ -175,7 +182,7 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma));
+    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
     const float *states = ckpt;
     if (bwd_needs_states(stride)) {
@@ -220,7 +227,7 @@ bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seq
     dd.dk = 64;
     dd.dv = 64;
     Problem p = make_problem(dd, cu_seqlens, n_docs, b, mode, ws, stream);
-    BDLA_CUDA(launch_decay(p, a, gamma));
+    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     return BDLA_OK;
 }
 

@@ -1,0 +1,758 @@
+// Backward pass on the sm_100-family tensor cores: one CTA per (document,
+// head) walks the document's 128-token blocks in reverse, carrying the state
+// adjoint E (gradient w.r.t. the state at the block end from all later tokens)
+// as an fp32 accumulator in tensor memory.
+//
+// Per block, with the pair weights w_ts = e^{Lam_t - Lam_s} built from the
+// same two-level tile factors as the forward ("Engineering Long-Context
+// Training for Trillion-Parameter MoE Models", sec. 3.2-3.3: with the bounded
+// decay the diagonal 16-token tiles use the in-tile reciprocal like every
+// other tile) and w_s = e^{Lam_end - Lam_s}:
+//   P  = M o w o (Q K^T),  dA = dO V^T,  dP = M o w o dA
+//   dq = e^{Lam_t} dO S_in^T + dP K
+//   dk = (V o w_s) E^T + dP^T Q
+//   dv = (K o w_s) E + P^T dO
+//   E <- e^{Lam_end} E + (Q o e^{Lam})^T dO
+// and the decay gradient from pair sums (W = P o dA):
+//   dlam_r = sum_{u<r} X_u + sum_{t>=r} Y_t + e^{Lam_end} <S_in, E>
+//   X_u = sum_{t>u} W_tu - sum_{s<u} W_us + k_u . dk_inter_u,   Y_t = q_t . dq_inter_t
+//   da = dlam * d lambda / d a.
+// S_in (the state before the block) comes from forward checkpoints.
+//
+// Phases of one block (MMA warp <-> four epilogue warps):
+//   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
+//   EA  P (smem) and dP (registers), W sums, V -> V o w_s, E -> bf16 copy,
+//       E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
+//   Mb  C2 = P^T dO, C1 = (V o w_s) E^T
+//   Eb  k . dk_inter, dP -> smem
+//   Md  C1 += dP^T Q, C3 += dP K
+//   Ee  Q -> Q o e^{Lam}, K -> K o w_s in place
+//   Mf  C2 += (K o w_s) E, E += (Q o e^{Lam})^T dO
+//   Eg  dq = C3, dk = C1, dv = C2, da      (overlaps the next block's loads)
+#include <cudaTypedefs.h>
+
+#include "bdla_internal.h"
+#include "bdla_sm100.cuh"
+
+namespace bdla {
+
+bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tokens);
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BT = 128;
+constexpr int kBwdThreads = 192;
+constexpr uint32_t kPanel = 16384;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <int DV>
+struct BwdSmem {
+    alignas(1024) unsigned char q[2 * kPanel];
+    alignas(1024) unsigned char k[2 * kPanel];
+    alignas(1024) unsigned char v[(DV / 64) * kPanel];
+    alignas(1024) unsigned char dO[(DV / 64) * kPanel];
+    alignas(1024) unsigned char z[(DV / 64) * kPanel];   // S_in, then E: rows dk, panels dv
+    alignas(1024) unsigned char x[2 * kPanel];           // P, then dP: rows t, panels s
+    float cdiag[BT];
+    float coff[BT];
+    float colsum[4][BT];
+    float scan[2][4];
+    float gam[BT / kChunk];
+    float se[4];
+    uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
+        mf_done, acc_free, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool epi_all(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 x, float s)
+{
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = pack_bf16(bf16_lo(w[i]) * s, bf16_hi(w[i]) * s);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Sum over the warp of 32 per-lane values; lane l ends with the total of value l.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&vals)[32], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? vals[i] : vals[i + off];
+            const float keep = upper ? vals[i + off] : vals[i];
+            vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return vals[0];
+}
+
+// Exclusive prefix sum over the 128 epilogue rows (row = 32 * q4 + lane).
+__device__ __forceinline__ float block_exclusive_scan(float x, float *warp_tot, int q4, int lane, float &total)
+{
+    float incl = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += y;
+    }
+    if (lane == 31)
+        warp_tot[q4] = incl;
+    epi_sync();
+    float before = 0.0f;
+    total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        before += (w < q4) ? warp_tot[w] : 0.0f;
+        total += warp_tot[w];
+    }
+    return before + incl - x;
+}
+
+// Row r (of dk rows) of the state before block j from the checkpoint array.
+__device__ __forceinline__ void load_state_row(const void *states, int st_bf16, int stride,
+                                               int64_t n_slots, const DocSpan &d, int n, int h, int j,
+                                               int dk, int dv, int j0, int r, float (&out)[32], int c)
+{
+    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / stride, stride);
+    const size_t off = (((size_t)h * n_slots + slot) * dk + r) * dv + j0 + c * 32;
+    if (st_bf16) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(states) + off);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const uint4 u = src[k4];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                out[8 * k4 + 2 * i] = bf16_lo(w[i]);
+                out[8 * k4 + 2 * i + 1] = bf16_hi(w[i]);
+            }
+        }
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(states) + off);
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 u = src[k4];
+            out[4 * k4] = u.x;
+            out[4 * k4 + 1] = u.y;
+            out[4 * k4 + 2] = u.z;
+            out[4 * k4 + 3] = u.w;
+        }
+    }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                 const float *__restrict__ gamma, const float *__restrict__ dfac,
+                 const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
+                 const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
+                 const float *__restrict__ dhT, float *__restrict__ dq, float *__restrict__ dkk,
+                 float *__restrict__ dvv, float *__restrict__ da, float *__restrict__ dh0,
+                 DeviceStatus *st)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, n = blockIdx.y;
+    const int j0 = 0;
+    const DocSpan d = doc_span(cu, n, T);
+    if (!doc_valid(d, tokens))
+        return;
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+        if (tid == 0)
+            set_status(st, BDLA_ERR_DEVICE, 0xB11u);
+        return;
+    }
+    const int nblk = (int)((d.len + BT - 1) / BT);
+    const int kpan = dk / 64;
+    const size_t sstride = (size_t)dk * dv;
+    const int64_t unit = (int64_t)n * H + h;
+
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.full_in, 1);
+        mbar_init(&sm.free_in, 1);
+        mbar_init(&sm.z_ready, 128);
+        mbar_init(&sm.m1_done, 1);
+        mbar_init(&sm.ea_done, 128);
+        mbar_init(&sm.mb_done, 1);
+        mbar_init(&sm.eb_done, 128);
+        mbar_init(&sm.md_done, 1);
+        mbar_init(&sm.ee_done, 128);
+        mbar_init(&sm.mf_done, 1);
+        mbar_init(&sm.acc_free, 128);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (kpan == 1) {   // dk = 64: the second dk panel of Q and K stays zero
+        for (int e = tid; e < (int)(kPanel / 16); e += kBwdThreads) {
+            reinterpret_cast<uint4 *>(sm.q + kPanel)[e] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.k + kPanel)[e] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const uint32_t t_e = tmem, t_c1 = tmem + 128, t_c2 = tmem + 256, t_c3 = tmem + 384;
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tdo);
+            const uint32_t bytes = (uint32_t)kpan * 2u * kPanel + 2u * (uint32_t)(DV / 64) * kPanel;
+            int last = -1;
+            bool ok = true;
+            for (int jj = 0; jj < nblk; ++jj) {
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const int j = nblk - 1 - jj;
+                const int t0 = (int)(d.start + (int64_t)j * BT);
+                if (jj > 0 && !mbar_wait(&sm.free_in, (jj - 1) & 1, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full_in, bytes);
+                for (int p = 0; p < kpan; ++p) {
+                    tma_load_3d(sm.q + p * kPanel, &tq, &sm.full_in, p * 64, h, t0);
+                    tma_load_3d(sm.k + p * kPanel, &tk, &sm.full_in, p * 64, h, t0);
+                }
+                for (int p = 0; p < DV / 64; ++p) {
+                    tma_load_3d(sm.v + p * kPanel, &tv, &sm.full_in, j0 + p * 64, h, t0);
+                    tma_load_3d(sm.dO + p * kPanel, &tdo, &sm.full_in, j0 + p * 64, h, t0);
+                }
+                last = jj;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(st, BDLA_ERR_TIMEOUT, 11u);
+                if (last >= 0)
+                    mbar_wait(&sm.full_in, last & 1, kWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t sq = smem_u32(sm.q), sk = smem_u32(sm.k), sv = smem_u32(sm.v);
+            const uint32_t sdo = smem_u32(sm.dO), sz = smem_u32(sm.z), sx = smem_u32(sm.x);
+            const uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);   // C1 = Q K^T, C2 = dO V^T
+            const uint32_t id_dqs = idesc_bf16_f32(128, dk, false, false);   // C3 = dO S_in^T
+            const uint32_t id_pdo = idesc_bf16_f32(128, DV, true, true);     // C2 = P^T dO
+            const uint32_t id_ve = idesc_bf16_f32(128, dk, false, false);    // C1 = V E^T
+            const uint32_t id_dpq = idesc_bf16_f32(128, dk, true, true);     // C1 += dP^T Q
+            const uint32_t id_dpk = idesc_bf16_f32(128, dk, false, true);    // C3 += dP K
+            const uint32_t id_ke = idesc_bf16_f32(128, DV, false, true);     // C2 += K E
+            const uint32_t id_qdo = idesc_bf16_f32(128, DV, true, true);     // E += Q^T dO
+            auto kmaj = [](uint32_t base, int ks) {
+                return sdesc_sw128(base + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024);
+            };
+            auto mnmaj = [](uint32_t base, int ks) { return sdesc_sw128(base + ks * 2048, kPanel, 1024); };
+            bool ok = true;
+            for (int jj = 0; jj < nblk && ok; ++jj) {
+                const uint32_t par = jj & 1;
+                if (*abort_flag || !mbar_wait(&sm.full_in, par, kWaitNs) ||
+                    !mbar_wait(&sm.z_ready, par, kWaitNs) ||
+                    (jj > 0 && !mbar_wait(&sm.acc_free, (jj - 1) & 1, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < dk / 16; ++ks)
+                    umma_bf16(t_c1, kmaj(sq, ks), kmaj(sk, ks), id_ss, ks > 0);
+                for (int ks = 0; ks < DV / 16; ++ks) {
+                    umma_bf16(t_c2, kmaj(sdo, ks), kmaj(sv, ks), id_ss, ks > 0);
+                    umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
+                }
+                umma_commit(&sm.m1_done);
+                if (!mbar_wait(&sm.ea_done, par, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_c2, mnmaj(sx, ks), mnmaj(sdo, ks), id_pdo, ks > 0);
+                for (int ks = 0; ks < DV / 16; ++ks)
+                    umma_bf16(t_c1, kmaj(sv, ks), kmaj(sz, ks), id_ve, ks > 0);
+                umma_commit(&sm.mb_done);
+                if (!mbar_wait(&sm.eb_done, par, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < BT / 16; ++ks) {
+                    umma_bf16(t_c1, mnmaj(sx, ks), mnmaj(sq, ks), id_dpq, 1);
+                    umma_bf16(t_c3, kmaj(sx, ks), mnmaj(sk, ks), id_dpk, 1);
+                }
+                umma_commit(&sm.md_done);
+                if (!mbar_wait(&sm.ee_done, par, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < dk / 16; ++ks)
+                    umma_bf16(t_c2, kmaj(sk, ks), mnmaj(sz, ks), id_ke, 1);
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_e, mnmaj(sq, ks), mnmaj(sdo, ks), id_qdo, 1);
+                umma_commit(&sm.mf_done);
+                umma_commit(&sm.free_in);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(st, BDLA_ERR_TIMEOUT, 12u);
+            }
+            umma_commit(&sm.drain);
+            mbar_wait(&sm.drain, 0, kWaitNs);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        {   // E <- dhT
+            uint32_t x[32];
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[i] = __float_as_uint((dhT != nullptr && r < dk)
+                                               ? dhT[unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
+                                               : 0.0f);
+                tmem_st32(t_e + lane_off + c * 32, x);
+            }
+            tmem_st_wait();
+        }
+        // values of the block whose outputs are still pending (written in Eg)
+        int pend_j = -1;
+        float pend_row = 0.0f, pend_kd = 0.0f, pend_y = 0.0f, pend_fac = 0.0f, pend_lend = 0.0f;
+
+        auto finish_block = [&]() -> bool {
+            // Eg: outputs of block pend_j once Mf has completed
+            const int jj = nblk - 1 - pend_j;
+            if (!epi_all(mbar_wait(&sm.mf_done, jj & 1, kWaitNs)) || *abort_flag)
+                return false;
+            tc_fence_after();
+            const int64_t t = d.start + (int64_t)pend_j * BT + r;
+            const bool valid = (int64_t)pend_j * BT + r < d.len;
+            const size_t ok_off = (size_t)t * H + h;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c * 32 >= dk)
+                    break;
+                uint32_t x[32], y[32];
+                tmem_ld32(t_c3 + lane_off + c * 32, x);
+                tmem_ld32(t_c1 + lane_off + c * 32, y);
+                tmem_ld_wait();
+                if (valid) {
+                    float4 *pq = reinterpret_cast<float4 *>(dq + ok_off * dk + c * 32);
+                    float4 *pk = reinterpret_cast<float4 *>(dkk + ok_off * dk + c * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        pq[k4] = make_float4(__uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
+                                             __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
+                        pk[k4] = make_float4(__uint_as_float(y[4 * k4]), __uint_as_float(y[4 * k4 + 1]),
+                                             __uint_as_float(y[4 * k4 + 2]), __uint_as_float(y[4 * k4 + 3]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t x[32];
+                tmem_ld32(t_c2 + lane_off + c * 32, x);
+                tmem_ld_wait();
+                if (valid) {
+                    float4 *pv = reinterpret_cast<float4 *>(dvv + ok_off * dv + j0 + c * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4)
+                        pv[k4] = make_float4(__uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
+                                             __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.acc_free);
+            // decay gradient of the block
+            float col = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                col += sm.colsum[w][r];
+            const float X = col - pend_row + pend_kd;
+            float tx, ty;
+            const float px = block_exclusive_scan(X, sm.scan[0], q4, lane, tx);
+            const float py = block_exclusive_scan(pend_y, sm.scan[1], q4, lane, ty);
+            const float C = expf(pend_lend) * (sm.se[0] + sm.se[1] + sm.se[2] + sm.se[3]);
+            if (valid)
+                da[(size_t)t * H + h] = (px + (ty - py) + C) * pend_fac;
+            epi_sync();   // scan scratch and colsum are reused by the next block
+            return true;
+        };
+
+        bool ok = true;
+        for (int jj = 0; jj < nblk; ++jj) {
+            const int j = nblk - 1 - jj;
+            const uint32_t par = jj & 1;
+            const int64_t t0 = d.start + (int64_t)j * BT;
+            const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
+            const bool valid = r < Lb;
+            const int tau = r >> 4;
+            if (pend_j >= 0) {
+                ok = finish_block();
+                if (!ok)
+                    break;
+                pend_j = -1;
+            }
+            // ---- decay scalars
+            const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
+            const float fac = valid ? dfac[(int64_t)h * tokens + t0 + r] : 0.0f;
+            const int last = min(16 * tau + 15, Lb - 1);
+            const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
+            const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
+            if ((r & 15) == 0)
+                sm.gam[tau] = gam_tau;
+            epi_sync();
+            float G[BT / kChunk + 1];
+            G[0] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BT / kChunk; ++i)
+                G[i + 1] = G[i] + sm.gam[i];
+            float Gt = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BT / kChunk; ++i)
+                Gt = (i == tau) ? G[i] : Gt;
+            const float lend = G[BT / kChunk];
+            const float lam_r = Gt + g;
+            const float rt = valid ? expf(g) : 0.0f;
+            sm.cdiag[r] = valid ? expf(-g) : 0.0f;
+            sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
+            const float qsc = valid ? expf(lam_r) : 0.0f;
+            const float wsc = valid ? expf(lend - lam_r) : 0.0f;
+            float f[BT / kChunk];
+#pragma unroll
+            for (int sg = 0; sg < BT / kChunk; ++sg)
+                f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
+
+            // ---- S_in row r -> bf16 copy (z) and <S_in, E>
+            {
+                float se = 0.0f;
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    float s_in[32];
+                    if (r < dk)
+                        load_state_row(states, st_bf16, st_stride, n_slots, d, n, h, j, dk, dv, j0, r, s_in, c);
+                    else
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            s_in[i] = 0.0f;
+                    uint32_t e[32];
+                    tmem_ld32(t_e + lane_off + c * 32, e);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        se = fmaf(s_in[i], __uint_as_float(e[i]), se);
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        u[i] = pack_bf16(s_in[2 * i], s_in[2 * i + 1]);
+                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                }
+                se = warp_sum(se);
+                if (lane == 0)
+                    sm.se[q4] = se;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.z_ready);
+
+            // ---- EA
+            ok = epi_all(mbar_wait(&sm.m1_done, par, kWaitNs)) && !*abort_flag;
+            if (!ok)
+                break;
+            tc_fence_after();
+            float rowsum = 0.0f;
+            uint32_t dpk[BT / 2];   // dP row r, bf16 pairs
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) {
+                uint32_t xs[32], xa[32];
+                tmem_ld32(t_c1 + lane_off + c * 32, xs);
+                tmem_ld32(t_c2 + lane_off + c * 32, xa);
+                tmem_ld_wait();
+                float pv[32], wv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = c * 32 + i;
+                    const int sg = col >> 4;
+                    const float sc = __uint_as_float(xs[i]);
+                    const float av = __uint_as_float(xa[i]);
+                    float p, dp;
+                    if (sg < tau) {
+                        const float w = sm.coff[col] * f[sg];
+                        p = sc * w;
+                        dp = av * w;
+                    } else if (sg == tau && col <= r) {
+                        const float cd = sm.cdiag[col];
+                        p = (sc * cd) * rt;
+                        dp = (av * cd) * rt;
+                    } else {
+                        p = 0.0f;
+                        dp = 0.0f;
+                    }
+                    pv[i] = p;
+                    const float wt = (col < r) ? p * av : 0.0f;
+                    wv[i] = wt;
+                    rowsum += wt;
+                    xa[i] = __float_as_uint(dp);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    dpk[c * 16 + i] = pack_bf16(__uint_as_float(xa[2 * i]), __uint_as_float(xa[2 * i + 1]));
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    u[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                unsigned char *xp = sm.x + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                        make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                const float cs = warp_reduce_scatter32(wv, lane);
+                sm.colsum[q4][c * 32 + lane] = cs;
+            }
+            // V -> V o w_s in place
+#pragma unroll
+            for (int p = 0; p < DV / 64; ++p)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint4 *va = reinterpret_cast<uint4 *>(sm.v + p * kPanel + sw128_offset(r, c8));
+                    *va = scale_bf16x8(*va, wsc);
+                }
+            // E -> bf16 copy (z), E <- e^{Lam_end} E
+            {
+                const float el = expf(lend);
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t e[32];
+                    tmem_ld32(t_e + lane_off + c * 32, e);
+                    tmem_ld_wait();
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        u[i] = pack_bf16(__uint_as_float(e[2 * i]), __uint_as_float(e[2 * i + 1]));
+                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        e[i] = __float_as_uint(__uint_as_float(e[i]) * el);
+                    tmem_st32(t_e + lane_off + c * 32, e);
+                }
+            }
+            // C3 <- e^{Lam_t} C3 (the inter-block part of dq) and Y_t = q_t . dq_inter_t
+            float yv = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c * 32 >= dk)
+                    break;
+                uint32_t x[32];
+                tmem_ld32(t_c3 + lane_off + c * 32, x);
+                tmem_ld_wait();
+                const unsigned char *qp = sm.q + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const uint4 qq = *reinterpret_cast<const uint4 *>(qp + sw128_offset(r, (c & 1) * 4 + k4));
+                    const uint32_t w[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float a0 = __uint_as_float(x[8 * k4 + 2 * i]) * qsc;
+                        const float a1 = __uint_as_float(x[8 * k4 + 2 * i + 1]) * qsc;
+                        yv = fmaf(bf16_lo(w[i]), a0, yv);
+                        yv = fmaf(bf16_hi(w[i]), a1, yv);
+                        x[8 * k4 + 2 * i] = __float_as_uint(a0);
+                        x[8 * k4 + 2 * i + 1] = __float_as_uint(a1);
+                    }
+                }
+                tmem_st32(t_c3 + lane_off + c * 32, x);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.ea_done);
+
+            // ---- Eb: k . dk_inter, then dP -> smem
+            ok = epi_all(mbar_wait(&sm.mb_done, par, kWaitNs)) && !*abort_flag;
+            if (!ok)
+                break;
+            tc_fence_after();
+            float kd = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c * 32 >= dk)
+                    break;
+                uint32_t x[32];
+                tmem_ld32(t_c1 + lane_off + c * 32, x);
+                tmem_ld_wait();
+                const unsigned char *kp = sm.k + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const uint4 kk = *reinterpret_cast<const uint4 *>(kp + sw128_offset(r, (c & 1) * 4 + k4));
+                    const uint32_t w[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        kd = fmaf(bf16_lo(w[i]), __uint_as_float(x[8 * k4 + 2 * i]), kd);
+                        kd = fmaf(bf16_hi(w[i]), __uint_as_float(x[8 * k4 + 2 * i + 1]), kd);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) {
+                unsigned char *xp = sm.x + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                        make_uint4(dpk[c * 16 + 4 * k4], dpk[c * 16 + 4 * k4 + 1], dpk[c * 16 + 4 * k4 + 2],
+                                   dpk[c * 16 + 4 * k4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.eb_done);
+
+            // ---- Ee: Q -> Q o e^{Lam}, K -> K o w_s in place
+            ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;
+            if (!ok)
+                break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint4 *qa = reinterpret_cast<uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
+                    uint4 *ka = reinterpret_cast<uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
+                    *qa = scale_bf16x8(*qa, qsc);
+                    *ka = scale_bf16x8(*ka, wsc);
+                }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.ee_done);
+
+            pend_j = j;
+            pend_row = rowsum;
+            pend_kd = kd;
+            pend_y = yv;
+            pend_fac = fac;
+            pend_lend = lend;
+        }
+        if (ok && pend_j >= 0)
+            ok = finish_block();
+        if (ok && dh0 != nullptr && r < dk) {
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t x[32];
+                tmem_ld32(t_e + lane_off + c * 32, x);
+                tmem_ld_wait();
+                float4 *row = reinterpret_cast<float4 *>(dh0 + unit * sstride + (size_t)r * dv + j0 + c * 32);
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4)
+                    row[k4] = make_float4(__uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
+                                          __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0)
+                set_status(st, BDLA_ERR_TIMEOUT, 13u);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem, 512);
+}
+
+template <int DV>
+cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                               const CUtensorMap &mv, const CUtensorMap &mdo, const float *gamma,
+                               const float *dfac, const void *states, int st_bf16, int st_stride,
+                               const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0)
+{
+    auto kern = bwd_sm100_kernel<DV>;
+    const size_t smem = sizeof(BwdSmem<DV>);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    dim3 grid(p.H, p.n_docs);
+    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, gamma, dfac, p.cu, p.T, p.tokens, p.H,
+                                                p.dk, p.dv, states, st_bf16, st_stride,
+                                                ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0, p.st);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
+                             const float *dfac, const void *states, int st_bf16, int st_stride,
+                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0)
+{
+    if (p.n_docs <= 0 || p.tokens == 0)
+        return cudaSuccess;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!make_token_map(&mq, q, p.dk, p.H, p.tokens) || !make_token_map(&mk, k, p.dk, p.H, p.tokens) ||
+        !make_token_map(&mv, v, p.dv, p.H, p.tokens) || !make_token_map(&mdo, dO, p.dv, p.H, p.tokens))
+        return cudaErrorInvalidValue;
+    if (p.dv == 64)
+        return launch_bwd_sm100_t<64>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16, st_stride, dhT,
+                                      dq, dk, dv, da, dh0);
+    if (p.dv == 128)
+        return launch_bwd_sm100_t<128>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16, st_stride, dhT,
+                                       dq, dk, dv, da, dh0);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bdla

@@ -5,15 +5,28 @@
 // reciprocal normalises the in-chunk products; sec. 3.2: the log-decay is
 // b * sigmoid(a) (bounded) instead of -softplus(a).  Gamma restarts at every
 // doc-local 16-token tile, so with the bound it stays in [16 b, 0].
+//
+// One CTA handles 128 consecutive tokens of one document for 32 heads at a
+// time: the [128 x heads] slab of logits is read coalesced (a is token-major)
+// into shared memory, each thread sums one (tile, head) column, and Gamma is
+// written head-major ([H][tokens]) so the attention kernels read one head's
+// 128 values as a single coalesced line.  Optionally also writes
+// d lambda / d a in the same layout (used by the backward).
 #include "bdla_internal.h"
 
 namespace bdla {
 
+namespace {
+constexpr int kTok = 128;   // tokens per slab (8 tiles)
+constexpr int kHeads = 32;  // heads per pass
+}
+
 __global__ void __launch_bounds__(256)
 decay_kernel(const float *__restrict__ a, float b, int mode, const int32_t *__restrict__ cu,
              int n_docs, int T, int64_t tokens, int H, float *__restrict__ gamma,
-             DeviceStatus *st)
+             float *__restrict__ dfac, DeviceStatus *st)
 {
+    __shared__ float sa[kTok][kHeads + 1];
     const int n = blockIdx.y;
     const DocSpan d = doc_span(cu, n, T);
     if (cu != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -27,34 +40,58 @@ decay_kernel(const float *__restrict__ a, float b, int mode, const int32_t *__re
     }
     if (!doc_valid(d, tokens))
         return;
-    const int64_t ntiles = (d.len + kChunk - 1) / kChunk;
-    const int64_t work = ntiles * H;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < work;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int h = (int)(idx % H);
-        const int64_t c = idx / H;
-        const int64_t t0 = d.start + c * kChunk;
-        const int m = (int)(d.len - c * kChunk < kChunk ? d.len - c * kChunk : kChunk);
-        float acc = 0.0f;
-        for (int i = 0; i < m; ++i) {
-            acc += log_decay(a[(t0 + i) * H + h], b, mode);
-            gamma[(t0 + i) * H + h] = acc;
+    const int64_t nslab = (d.len + kTok - 1) / kTok;
+    for (int64_t sl = blockIdx.x; sl < nslab; sl += gridDim.x) {
+        const int64_t t0 = d.start + sl * kTok;
+        const int len = (int)(d.len - sl * kTok < kTok ? d.len - sl * kTok : kTok);
+        for (int h0 = 0; h0 < H; h0 += kHeads) {
+            const int nh = H - h0 < kHeads ? H - h0 : kHeads;
+            __syncthreads();
+            for (int e = threadIdx.x; e < kTok * nh; e += blockDim.x) {
+                const int t = e / nh, hh = e % nh;
+                sa[t][hh] = t < len ? a[(t0 + t) * H + h0 + hh] : 0.0f;
+            }
+            __syncthreads();
+            if (dfac != nullptr) {
+                for (int e = threadIdx.x; e < kTok * nh; e += blockDim.x) {
+                    const int hh = e / kTok, t = e % kTok;
+                    if (t < len)
+                        dfac[(int64_t)(h0 + hh) * tokens + t0 + t] = log_decay_deriv(sa[t][hh], b, mode);
+                }
+                __syncthreads();
+            }
+            for (int e = threadIdx.x; e < (kTok / kChunk) * nh; e += blockDim.x) {
+                const int hh = e / (kTok / kChunk), c = e % (kTok / kChunk);
+                float acc = 0.0f;
+                for (int i = 0; i < kChunk; ++i) {
+                    const int t = c * kChunk + i;
+                    if (t < len) {
+                        acc += log_decay(sa[t][hh], b, mode);
+                        sa[t][hh] = acc;
+                    }
+                }
+            }
+            __syncthreads();
+            for (int e = threadIdx.x; e < kTok * nh; e += blockDim.x) {
+                const int hh = e / kTok, t = e % kTok;
+                if (t < len)
+                    gamma[(int64_t)(h0 + hh) * tokens + t0 + t] = sa[t][hh];
+            }
         }
     }
 }
 
-cudaError_t launch_decay(const Problem &p, const float *a, float *gamma)
+cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *dfac)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
-    const int64_t max_tiles = p.cu ? (p.tokens + kChunk - 1) / kChunk + 1 : (p.T + kChunk - 1) / kChunk;
-    int64_t gx = (max_tiles * p.H + 255) / 256;
-    if (p.cu)  // document lengths are on the device: spread each document over a fixed grid
-        gx = (gx + p.n_docs - 1) / p.n_docs + 1;
-    gx = gx < 1 ? 1 : (gx > 4096 ? 4096 : gx);
-    dim3 grid((unsigned)gx, (unsigned)p.n_docs);
+    // slabs per document: exact for fixed-length inputs; packed documents
+    // spread over a grid sized for the average length (grid-stride inside).
+    int64_t per_doc = p.cu ? (p.tokens / p.n_docs + kTok - 1) / kTok + 1 : (p.T + kTok - 1) / kTok;
+    per_doc = per_doc < 1 ? 1 : (per_doc > 65535 ? 65535 : per_doc);
+    dim3 grid((unsigned)per_doc, (unsigned)p.n_docs);
     decay_kernel<<<grid, 256, 0, p.stream>>>(a, p.b, p.mode, p.cu, p.n_docs, p.T, p.tokens, p.H,
-                                             gamma, p.st);
+                                             gamma, dfac, p.st);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,595 @@
+// Forward pass on the sm_100-family tensor cores: TMA tile loads,
+// tcgen05.mma with fp32 accumulators in tensor memory, one CTA per
+// (document, head, dv slice) walking the document in 128-token blocks.
+//
+// Method ("Engineering Long-Context Training for Trillion-Parameter MoE
+// Models", sec. 3.1-3.3; "Engineering Stability in Ultra-Long Context and
+// Trillion-Parameter Sparse Models", sec. 2.2): inside a chunk the products
+// are dense GEMMs and a state passes between chunks; the bounded log-decay
+// keeps the reciprocal of the in-tile cumulative decay finite so that the
+// diagonal tiles go through the same GEMM as every other tile.
+//
+// Per block of 128 tokens (8 decay tiles of 16) with Gamma the tile-local
+// cumulative log-decay, gamma_tau the tile totals, G_tau their exclusive
+// prefix inside the block and Lam = G + Gamma:
+//   score = Q K^T                                            (tensor cores)
+//   P_ts  = score_ts e^{-Gamma_s} e^{Gamma_t}                 same tile, s <= t
+//   P_ts  = score_ts e^{gamma_sig - Gamma_s} e^{G_tau - G_sig+1} e^{Gamma_t}   sig < tau
+//   O     = P V + (Q o e^{Lam}) S_in                          (tensor cores)
+//   S_out = e^{Lam_end} S_in + (K o e^{Lam_end - Lam})^T V    (tensor cores)
+// Every factor is <= 1 except e^{-Gamma_s} on the diagonal tile, which the
+// bound keeps <= e^{16 |b|} = e^{80}.  The unbounded ablation instead
+// computes the diagonal tile pair by pair on CUDA cores,
+//   P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}   (explicit position-pair path),
+// and keeps the GEMM result only for the off-diagonal tiles.
+//
+// Warp roles: warp 0 issues TMA loads (Q, K double-buffered, V single),
+// warp 1 allocates TMEM and issues the MMAs, warps 2-5 (one TMEM lane
+// quarter each) turn scores into P, fold the decay into Q and K in place,
+// move the state between TMEM and its bf16 shared copy, and store O.
+// Every wait is bounded; on expiry the CTA records BDLA_ERR_TIMEOUT, drains
+// its own copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "bdla_internal.h"
+#include "bdla_sm100.cuh"
+
+namespace bdla {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BT = 128;             // tokens per block
+constexpr int kFwdThreads = 192;    // 6 warps
+constexpr uint32_t kPanel = 16384;  // one 128-row x 128-byte swizzled panel
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <int DV>
+struct FwdSmem {
+    alignas(1024) unsigned char q[2][2 * kPanel];   // stages x dk panels
+    alignas(1024) unsigned char k[2][2 * kPanel];
+    alignas(1024) unsigned char v[(DV / 64) * kPanel];
+    alignas(1024) unsigned char p[2 * kPanel];      // P: rows t, panels over s
+    alignas(1024) unsigned char sb[(DV / 64) * kPanel];  // state bf16: rows dk, panels over dv
+    float cdiag[BT];     // e^{-Gamma_s}
+    float coff[BT];      // e^{gamma_sig - Gamma_s}
+    float gq[BT];        // Gamma per row (ablation diagonal path)
+    float gam[BT / kChunk];
+    uint64_t full_qk[2], empty_qk[2], score_full[2], score_free[2];
+    uint64_t full_v, empty_v, p_ready, o_full, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool epi_all(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 x, float s)
+{
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = pack_bf16(bf16_lo(w[i]) * s, bf16_hi(w[i]) * s);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b, float acc)
+{
+    const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = fmaf(bf16_lo(x[i]), bf16_lo(y[i]), acc);
+        acc = fmaf(bf16_hi(x[i]), bf16_hi(y[i]), acc);
+    }
+    return acc;
+}
+
+template <int DV, bool ABL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const float *__restrict__ gamma,
+                 const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
+                 const float *__restrict__ h0, void *__restrict__ o, int o_f32,
+                 float *__restrict__ hT, float *__restrict__ ckpt, int ckpt_stride,
+                 int64_t n_slots, DeviceStatus *st)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    FwdSmem<DV> &sm = *reinterpret_cast<FwdSmem<DV> *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = blockIdx.x * DV, h = blockIdx.y, n = blockIdx.z;
+    const DocSpan d = doc_span(cu, n, T);
+    if (!doc_valid(d, tokens))
+        return;
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+        if (tid == 0)
+            set_status(st, BDLA_ERR_DEVICE, 0xA11u);
+        return;
+    }
+    const int nblk = (int)((d.len + BT - 1) / BT);
+    const int kpan = dk / 64;
+    const size_t sstride = (size_t)dk * dv;
+    const int64_t unit = (int64_t)n * H + h;
+
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.full_qk[s], 1);
+            mbar_init(&sm.empty_qk[s], 1);
+            mbar_init(&sm.score_full[s], 1);
+            mbar_init(&sm.score_free[s], 128);
+        }
+        mbar_init(&sm.full_v, 1);
+        mbar_init(&sm.empty_v, 1);
+        mbar_init(&sm.p_ready, 128);
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (kpan == 1) {   // dk = 64: the second dk panel of Q and K stays zero
+        for (int e = tid; e < 2 * (int)(kPanel / 16); e += kFwdThreads) {
+            const int s = e / (kPanel / 16), i = e % (kPanel / 16);
+            reinterpret_cast<uint4 *>(sm.q[s] + kPanel)[i] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.k[s] + kPanel)[i] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const uint32_t t_score0 = tmem, t_o = tmem + 256, t_s = tmem + 384;
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const uint32_t qk_bytes = (uint32_t)kpan * 2u * kPanel;
+            const uint32_t v_bytes = (uint32_t)(DV / 64) * kPanel;
+            int last_qk[2] = {-1, -1}, last_v = -1;
+            bool consumed = true;
+            for (int j = 0; j < nblk; ++j) {
+                if (*abort_flag)
+                    break;
+                const int s = j & 1;
+                const int t0 = (int)(d.start + (int64_t)j * BT);
+                if (j >= 2 && !mbar_wait(&sm.empty_qk[s], ((j >> 1) - 1) & 1, kWaitNs)) {
+                    consumed = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full_qk[s], qk_bytes);
+                for (int p = 0; p < kpan; ++p) {
+                    tma_load_3d(sm.q[s] + p * kPanel, &tq, &sm.full_qk[s], p * 64, h, t0);
+                    tma_load_3d(sm.k[s] + p * kPanel, &tk, &sm.full_qk[s], p * 64, h, t0);
+                }
+                last_qk[s] = j;
+                if (j >= 1 && !mbar_wait(&sm.empty_v, (j - 1) & 1, kWaitNs)) {
+                    consumed = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full_v, v_bytes);
+                for (int p = 0; p < DV / 64; ++p)
+                    tma_load_3d(sm.v + p * kPanel, &tv, &sm.full_v, j0 + p * 64, h, t0);
+                last_v = j;
+            }
+            if (!consumed || *abort_flag) {
+                *abort_flag = 1;
+                set_status(st, BDLA_ERR_TIMEOUT, 1u);
+                // let the copies this thread started land before the CTA exits
+                for (int s = 0; s < 2; ++s)
+                    if (last_qk[s] >= 0)
+                        mbar_wait(&sm.full_qk[s], (last_qk[s] >> 1) & 1, kWaitNs);
+                if (last_v >= 0)
+                    mbar_wait(&sm.full_v, last_v & 1, kWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t id_pv = idesc_bf16_f32(128, DV, false, true);
+            const uint32_t id_kv = idesc_bf16_f32(128, DV, true, true);
+            const uint32_t sq[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+            const uint32_t sk[2] = {smem_u32(sm.k[0]), smem_u32(sm.k[1])};
+            const uint32_t sv = smem_u32(sm.v), sp = smem_u32(sm.p), ssb = smem_u32(sm.sb);
+            bool ok = true;
+            auto issue_qk = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs))
+                    return false;
+                if (j >= 2 && !mbar_wait(&sm.score_free[s], ((j >> 1) - 1) & 1, kWaitNs))
+                    return false;
+                tc_fence_after();
+                for (int ks = 0; ks < dk / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * kPanel + (ks & 3) * 32;
+                    umma_bf16(t_score0 + 128 * s, sdesc_sw128(sq[s] + off, 16, 1024),
+                              sdesc_sw128(sk[s] + off, 16, 1024), id_qk, ks > 0);
+                }
+                umma_commit(&sm.score_full[s]);
+                return true;
+            };
+            if (nblk > 0)
+                ok = issue_qk(0);
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int s = j & 1;
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (j + 1 < nblk && !(ok = issue_qk(j + 1)))
+                    break;
+                if (!mbar_wait(&sm.p_ready, j & 1, kWaitNs) || !mbar_wait(&sm.full_v, j & 1, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // O = P V
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_o, sdesc_sw128(sp + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
+                              sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
+                // O += (Q o e^{Lam}) S_in
+                for (int ks = 0; ks < dk / 16; ++ks)
+                    umma_bf16(t_o, sdesc_sw128(sq[s] + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
+                              sdesc_sw128(ssb + ks * 2048, kPanel, 1024), id_pv, 1);
+                // S += (K o e^{Lam_end - Lam})^T V
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_s, sdesc_sw128(sk[s] + ks * 2048, kPanel, 1024),
+                              sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_kv, 1);
+                umma_commit(&sm.o_full);
+                umma_commit(&sm.empty_qk[s]);
+                umma_commit(&sm.empty_v);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(st, BDLA_ERR_TIMEOUT, 2u);
+            }
+            // every MMA issued above has completed before TMEM is released
+            umma_commit(&sm.drain);
+            mbar_wait(&sm.drain, 0, kWaitNs);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;                 // row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        {   // initial state
+            uint32_t x[32];
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float val = (h0 != nullptr && r < dk)
+                                          ? h0[unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
+                                          : 0.0f;
+                    x[i] = __float_as_uint(val);
+                }
+                tmem_st32(t_s + lane_off + c * 32, x);
+            }
+            tmem_st_wait();
+        }
+
+        auto store_o = [&](int jb) {
+            const int64_t t = d.start + (int64_t)jb * BT + r;
+            const bool valid = (int64_t)jb * BT + r < d.len;
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t x[32];
+                tmem_ld32(t_o + lane_off + c * 32, x);
+                tmem_ld_wait();
+                if (!valid)
+                    continue;
+                const size_t off = ((size_t)t * H + h) * dv + j0 + c * 32;
+                if (o_f32) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(o) + off);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4)
+                        dst[k4] = make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                } else {
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(o) + off);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        dst[k4] = make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                }
+            }
+        };
+
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            const int s = j & 1;
+            const int64_t t0 = d.start + (int64_t)j * BT;
+            const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
+            const bool valid = r < Lb;
+            const int tau = r >> 4;
+            // ---- decay scalars of this block
+            const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
+            const int last = min(16 * tau + 15, Lb - 1);
+            const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
+            const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
+            if ((r & 15) == 0)
+                sm.gam[tau] = gam_tau;
+            if (ABL)
+                sm.gq[r] = g;
+            epi_sync();
+            float G[BT / kChunk + 1];
+            G[0] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BT / kChunk; ++i)
+                G[i + 1] = G[i] + sm.gam[i];
+            float Gt = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BT / kChunk; ++i)
+                Gt = (i == tau) ? G[i] : Gt;
+            const float lend = G[BT / kChunk];
+            const float lam_r = Gt + g;
+            const float rt = valid ? expf(g) : 0.0f;
+            sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
+            sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
+            const float qsc = valid ? expf(lam_r) : 0.0f;
+            const float ksc = valid ? expf(lend - lam_r) : 0.0f;
+            float f[BT / kChunk];   // per source tile: e^{G_tau - G_sig+1} e^{Gamma_t}
+#pragma unroll
+            for (int sg = 0; sg < BT / kChunk; ++sg)
+                f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
+            epi_sync();
+
+            ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+            if (!ok)
+                break;
+            tc_fence_after();
+
+            float diag[kChunk];
+            if (ABL) {   // explicit position-pair path for the diagonal tile
+                const unsigned char *qrow = sm.q[s];
+                const unsigned char *kb = sm.k[s];
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const int sc = 16 * tau + i;
+                    float acc = 0.0f;
+                    if (valid && sc <= r) {
+                        for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + p * kPanel + sw128_offset(r, c8));
+                                const uint4 kk = *reinterpret_cast<const uint4 *>(kb + p * kPanel + sw128_offset(sc, c8));
+                                acc = dot_bf16x8(qa, kk, acc);
+                            }
+                        acc *= expf(g - sm.gq[sc]);
+                    }
+                    diag[i] = acc;
+                }
+                epi_sync();   // every thread is done with the raw K rows
+            }
+            // ---- fold the decay into Q and K in place (row r)
+#pragma unroll 1
+            for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint4 *qa = reinterpret_cast<uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
+                    uint4 *ka = reinterpret_cast<uint4 *>(sm.k[s] + p * kPanel + sw128_offset(r, c8));
+                    *qa = scale_bf16x8(*qa, qsc);
+                    *ka = scale_bf16x8(*ka, ksc);
+                }
+            // ---- P = decay-weighted causal scores (bf16, K-major rows t)
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) {
+                uint32_t x[32];
+                tmem_ld32(t_score0 + 128 * s + lane_off + c * 32, x);
+                tmem_ld_wait();
+                float pv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = c * 32 + i;
+                    const int sg = col >> 4;
+                    const float sc = __uint_as_float(x[i]);
+                    float val;
+                    if (sg < tau)
+                        val = sc * sm.coff[col] * f[sg];
+                    else if (sg == tau)
+                        val = (col <= r) ? (ABL ? diag[col & 15] : (sc * sm.cdiag[col]) * rt) : 0.0f;
+                    else
+                        val = 0.0f;
+                    pv[i] = val;
+                }
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    u[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                unsigned char *pp = sm.p + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4 *>(pp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                        make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.score_free[s]);
+
+            // ---- output of the previous block
+            if (j > 0) {
+                ok = epi_all(mbar_wait(&sm.o_full, (j - 1) & 1, kWaitNs)) && !*abort_flag;
+                if (!ok)
+                    break;
+                tc_fence_after();
+                store_o(j - 1);
+            }
+            // ---- state: checkpoint, bf16 copy for the Q S GEMM, decay for the K V update
+            {
+                const float el = expf(lend);
+                const bool wck = ckpt != nullptr && r < dk && ckpt_stride % BT == 0 &&
+                                 ((int64_t)j * BT) % ckpt_stride == 0;
+                float *ckrow = wck ? ckpt + ((size_t)h * n_slots +
+                                             ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride)) *
+                                                sstride + (size_t)r * dv + j0
+                                   : nullptr;
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t x[32];
+                    tmem_ld32(t_s + lane_off + c * 32, x);
+                    tmem_ld_wait();
+                    if (wck) {
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            reinterpret_cast<uint4 *>(ckrow + c * 32)[k4] =
+                                make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    }
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                    unsigned char *sp = sm.sb + (c >> 1) * kPanel;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        *reinterpret_cast<uint4 *>(sp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        x[i] = __float_as_uint(__uint_as_float(x[i]) * el);
+                    tmem_st32(t_s + lane_off + c * 32, x);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.p_ready);
+        }
+        if (ok && nblk > 0) {
+            ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, kWaitNs)) && !*abort_flag;
+            if (ok) {
+                tc_fence_after();
+                store_o(nblk - 1);
+            }
+        }
+        if (ok && hT != nullptr && r < dk) {
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t x[32];
+                tmem_ld32(t_s + lane_off + c * 32, x);
+                tmem_ld_wait();
+                float *row = hT + unit * sstride + (size_t)r * dv + j0 + c * 32;
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4)
+                    reinterpret_cast<uint4 *>(row)[k4] =
+                        make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+            }
+        } else if (ok && hT != nullptr) {
+            // rows >= dk hold no state
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0)
+                set_status(st, BDLA_ERR_TIMEOUT, 3u);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem, 512);
+}
+
+// hT = h0 (or 0) for documents without tokens when the whole call has none.
+__global__ void copy_state_kernel(const float *__restrict__ h0, float *__restrict__ hT, size_t n)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        hT[i] = h0 ? h0[i] : 0.0f;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+// 3-D map over a token-major bf16 tensor [tokens][H][d]: box = 64 features x
+// 1 head x 128 tokens, 128-byte swizzle, zero fill past the last token.
+bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tokens)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr || ptr == nullptr || tokens <= 0)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)BT};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DV, bool ABL>
+static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                      const CUtensorMap &mv, const float *gamma, const float *h0,
+                                      void *o, int o_f32, float *hT, float *ckpt, int ckpt_stride)
+{
+    auto kern = fwd_sm100_kernel<DV, ABL>;
+    const size_t smem = sizeof(FwdSmem<DV>);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
+    dim3 grid(p.dv / DV, p.H, p.n_docs);
+    kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
+                                                p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots, p.st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
+                             int o_f32, float *hT, float *ckpt, int ckpt_stride)
+{
+    if (p.n_docs <= 0)
+        return cudaSuccess;
+    if (p.tokens == 0) {
+        if (hT == nullptr)
+            return cudaSuccess;
+        const size_t nst = (size_t)p.n_docs * p.H * p.dk * p.dv;
+        copy_state_kernel<<<(unsigned)((nst + 255) / 256 < 4096 ? (nst + 255) / 256 : 4096), 256, 0,
+                            p.stream>>>(h0, hT, nst);
+        return cudaGetLastError();
+    }
+    CUtensorMap mq, mk, mv;
+    if (!make_token_map(&mq, q, p.dk, p.H, p.tokens) || !make_token_map(&mk, k, p.dk, p.H, p.tokens) ||
+        !make_token_map(&mv, v, p.dv, p.H, p.tokens))
+        return cudaErrorInvalidValue;
+    const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
+    if (p.dv == 64)
+        return abl ? launch_fwd_sm100_t<64, true>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride)
+                   : launch_fwd_sm100_t<64, false>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride);
+    return abl ? launch_fwd_sm100_t<128, true>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride)
+               : launch_fwd_sm100_t<128, false>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride);
+}
+
+}  // namespace bdla

@@ -45,12 +45,19 @@ inline void mark_stop(int kernel, cudaStream_t s)
         cudaEventRecord(g_kernel_events[kernel].stop, s);
 }
 
-cudaError_t launch_decay(const Problem &p, const float *a, float *gamma);
+// gamma and dfac (d lambda / d a, may be nullptr) are head-major [H][tokens].
+cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *dfac);
 
 // Tile-serial forward.  o may be nullptr (states-only pass that fills ckpt).
 cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
                             int o_f32, float *hT, float *ckpt, int ckpt_stride);
+
+// Tensor-core forward (tcgen05 / TMEM / TMA): o, hT and checkpoints whose
+// stride is a multiple of 128 tokens.
+cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
+                             int o_f32, float *hT, float *ckpt, int ckpt_stride);
 
 // Tile-serial backward; `states` holds the state before every 16-token tile
 // (checkpoint layout with stride 16).

@@ -3,7 +3,8 @@
 // One CTA walks one (document, head[, dv slice]) through its 16-token tiles
 // ("Engineering Long-Context Training for Trillion-Parameter MoE Models",
 // sec. 3.1: products inside a tile, recurrent state between tiles):
-//   Gamma_t   tile-local inclusive cumsum of log-decay (decay kernel output)
+//   Gamma_t   tile-local inclusive cumsum of log-decay (decay kernel output,
+//             head-major [H][tokens])
 //   A_ts      = (q_t . k_s) e^{Gamma_t - Gamma_s},  s <= t in the tile
 //   o_t       = e^{Gamma_t} S_in^T q_t + sum_s A_ts v_s
 //   S_out     = e^{gamma} S_in + sum_s e^{gamma - Gamma_s} k_s v_s^T,
@@ -97,7 +98,7 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         }
         if (tid < kChunk) {
             const int t = tid < m ? tid : m - 1;
-            sm.g[tid] = gamma[(t0 + t) * H + h];
+            sm.g[tid] = gamma[(int64_t)h * tokens + t0 + t];
         }
         __syncthreads();
         if (tid < kChunk)
@@ -257,7 +258,7 @@ bwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         }
         if (tid < kChunk) {
             const int t = tid < m ? tid : m - 1;
-            sm.g[tid] = gamma[(t0 + t) * H + h];
+            sm.g[tid] = gamma[(int64_t)h * tokens + t0 + t];
         }
         __syncthreads();
         const float gam = sm.g[m - 1];

@@ -99,8 +99,9 @@ size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mod
 
 /*
  * Decay kernel (the tile-local part of the method, sec. 3.1-3.2 of the first
- * page): gamma[t, h] = sum of lambda over the doc-local 16-token tile of t,
- * from the tile start through t (inclusive).  a, gamma: fp32 [B, T, H].
+ * page): gamma[h, t] = sum of lambda over the doc-local 16-token tile of t,
+ * from the tile start through t (inclusive).  a: fp32 [B, T, H] (token-major);
+ * gamma: fp32 [H, B*T] (head-major, the layout the attention kernels read).
  * cu_seqlens may be NULL for fixed-length inputs (then n_docs is ignored).
  */
 bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seqlens,

@@ -27,7 +27,7 @@ def test_decay_kernel_tile_cumsum(mode):
     w = _small("varlen64k", T=777, H=3, n_docs=4, mode=mode, a_std=3.0)
     inp = make_inputs(w, with_grad=False)
     g = to_device(inp)
-    gamma = bdla.decay(g["a"], w.b, cu_seqlens=g["cu_seqlens"], mode=mode).cpu().double().numpy()[0]
+    gamma = bdla.decay(g["a"], w.b, cu_seqlens=g["cu_seqlens"], mode=mode).cpu().double().numpy().T
     lam = oracle.log_decay(inp["a"].double().numpy()[0], w.b, mode)
     ref = np.zeros_like(lam)
     cu = inp["cu_seqlens"].numpy()
