@@ -207,8 +207,11 @@ def ours_arm(args, w, inp):
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     n_seq = (g["cu_seqlens"].numel() - 1) if g["cu_seqlens"] is not None else w.B
     ws_f = B.Workspace(B.workspace_bytes(B.OP_FWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode), dev)
-    ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode), dev)
+    ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode, ckpt_stride=128), dev)
     o = torch.empty(g["v"].shape, dtype=torch.bfloat16, device=dev)
+    # the forward hands the backward bf16 states every 128 tokens
+    ck = torch.empty((w.H, B.n_slots(w.B * w.T, n_seq, 128), w.dk, w.dv), dtype=torch.bfloat16,
+                     device=dev)
     hT = torch.empty((n_seq, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
             torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
@@ -218,13 +221,15 @@ def ours_arm(args, w, inp):
 
     def step(src):
         bdla.fwd(src["q"], src["k"], src["v"], src["a"], w.b, h0=src["h0"],
-                 cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_f, out=o, hT_out=hT)
+                 cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_f, out=o, hT_out=hT,
+                 ckpt_stride=128, ckpt_out=ck)
         bdla.bwd(src["q"], src["k"], src["v"], src["a"], src["dO"], w.b, h0=src["h0"],
-                 cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_b, outs=outs)
+                 cu_seqlens=src["cu_seqlens"], ckpt=ck, ckpt_stride=128, mode=w.mode, ws=ws_b,
+                 outs=outs)
 
     kernels = {"decay": B.KERNEL_DECAY, "fwd": B.KERNEL_FWD, "bwd": B.KERNEL_BWD,
                "states": B.KERNEL_STATES}
-    launches_per_step = 5   # fwd: decay + fwd;  bwd: decay + states + bwd
+    launches_per_step = 4   # fwd: decay + fwd;  bwd: decay + bwd
 
     def barrier():
         if world > 1:

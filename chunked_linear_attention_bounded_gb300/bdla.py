@@ -59,12 +59,13 @@ def lib():
         L.bdla_workspace_bytes.argtypes = [ci, Dims, ci, ci, ci]
         L.bdla_workspace_bytes.restype = sz
         L.bdla_decay.argtypes = [vp, f32, ci, vp, ci, vp, Dims, ci, vp, sz, vp]
-        L.bdla_fwd.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, ci, vp, vp, ci, Dims, ci, vp, sz, vp]
-        L.bdla_fwd_varlen.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, vp, ci, Dims,
+        L.bdla_fwd.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, ci, vp, vp, ci, ci, Dims, ci, vp, sz,
+                               vp]
+        L.bdla_fwd_varlen.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, vp, ci, ci, Dims,
                                       ci, vp, sz, vp]
-        L.bdla_bwd.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, vp, vp, ci, vp, vp, vp, vp, vp, Dims,
+        L.bdla_bwd.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, vp, vp, ci, ci, vp, vp, vp, vp, vp, Dims,
                                ci, vp, sz, vp]
-        L.bdla_bwd_varlen.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, ci, vp, vp, vp,
+        L.bdla_bwd_varlen.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, ci, ci, vp, vp, vp,
                                       vp, vp, Dims, ci, vp, sz, vp]
         for name in ("bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd", "bdla_bwd_varlen",
                      "bdla_read_status"):
@@ -182,10 +183,21 @@ def decay(a: torch.Tensor, b: float = -5.0, cu_seqlens: Optional[torch.Tensor] =
     return gamma
 
 
+def _dtype_code(dt) -> int:
+    if dt == torch.bfloat16:
+        return 0
+    if dt == torch.float32:
+        return 1
+    raise ValueError(f"unsupported dtype {dt}")
+
+
 def fwd(q, k, v, a, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUNDED,
         o_dtype=torch.bfloat16, want_hT: bool = True, ckpt_stride: int = 0,
-        ws: Optional[Workspace] = None, out=None, hT_out=None, stream=None):
-    """Forward pass.  Returns (o, hT, ckpt); hT / ckpt are None when not asked for."""
+        ckpt_dtype=torch.float32, ws: Optional[Workspace] = None, out=None, hT_out=None,
+        ckpt_out=None, stream=None):
+    """Forward pass.  Returns (o, hT, ckpt); hT / ckpt are None when not asked
+    for.  ckpt_stride > 0 also writes the state every ckpt_stride tokens
+    ([H, n_slots, dk, dv], ckpt_dtype), which bwd() can reuse."""
     _check(q, "q", torch.bfloat16, 4)
     _check(k, "k", torch.bfloat16, 4)
     _check(v, "v", torch.bfloat16, 4)
@@ -208,13 +220,14 @@ def fwd(q, k, v, a, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUND
     hT = hT_out
     if hT is None and want_hT:
         hT = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
-    ckpt = None
-    if ckpt_stride:
-        ckpt = torch.empty((H, n_slots(B * T, n_seq, ckpt_stride), dk, dv), dtype=torch.float32,
+    ckpt = ckpt_out
+    if ckpt is None and ckpt_stride:
+        ckpt = torch.empty((H, n_slots(B * T, n_seq, ckpt_stride), dk, dv), dtype=ckpt_dtype,
                            device=dev)
     ws = _ws_for(OP_FWD, q, v, n_docs, mode, 0, ws)
     odt = 1 if o.dtype == torch.float32 else 0
-    args_tail = (_p(h0), _p(o), odt, _p(hT), _p(ckpt), int(ckpt_stride), _dims(q, v), mode,
+    ckdt = _dtype_code(ckpt.dtype) if ckpt is not None else 1
+    args_tail = (_p(h0), _p(o), odt, _p(hT), _p(ckpt), int(ckpt_stride), ckdt, _dims(q, v), mode,
                  ws.ptr, ws.nbytes, _stream_handle(stream))
     L = lib()
     if n_docs:
@@ -248,8 +261,10 @@ def bwd(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, ckp
             _check(t, n, torch.float32, 4)
             if tuple(t.shape) != (n_seq, H, dk, dv):
                 raise ValueError(f"{n} must be [n_docs, H, dk, dv]")
+    ckdt = 1
     if ckpt is not None:
-        _check(ckpt, "ckpt", torch.float32, 4)
+        _check(ckpt, "ckpt", ckpt.dtype, 4)
+        ckdt = _dtype_code(ckpt.dtype)
         if not ckpt_stride:
             raise ValueError("ckpt needs its ckpt_stride")
     dev = q.device
@@ -262,8 +277,9 @@ def bwd(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, ckp
         dq, dkk, dvv, da = outs
     dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     stride = int(ckpt_stride) if ckpt is not None else 0
-    ws = _ws_for(OP_BWD, q, v, n_docs, mode, stride, ws)
-    args_tail = (_p(h0), _p(dO), _p(dhT), _p(ckpt), stride, _p(dq), _p(dkk), _p(dvv), _p(da),
+    ws_stride = stride if (ckdt == 1 or dv <= 128) else 0
+    ws = _ws_for(OP_BWD, q, v, n_docs, mode, ws_stride, ws)
+    args_tail = (_p(h0), _p(dO), _p(dhT), _p(ckpt), stride, ckdt, _p(dq), _p(dkk), _p(dvv), _p(da),
                  _p(dh0), _dims(q, v), mode, ws.ptr, ws.nbytes, _stream_handle(stream))
     L = lib()
     if n_docs:

@@ -21,28 +21,49 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-    size_t gamma = 0;    // offset of Gamma [H, tokens] fp32
-    size_t states = 0;   // offset of the per-tile states (backward), 0 if unused
+    size_t gamma = 0;    // Gamma [H, tokens] fp32
+    size_t dfac = 0;     // d lambda / d a [H, tokens] fp32 (backward)
+    size_t states = 0;   // recomputed states for the backward, 0 if unused
     size_t total = 0;
 };
 
 int64_t total_tokens(const bdla_dims &d) { return (int64_t)d.B * d.T; }
 
-// Backward needs the state before every 16-token tile; it uses caller
-// checkpoints when their stride is exactly 16.
-bool bwd_needs_states(int ckpt_stride) { return ckpt_stride != kChunk; }
+constexpr int kBlock = 128;   // tokens per block of the tensor-core kernels
 
-Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
+// The tensor-core backward (dv <= 128) reads the state before every 128-token
+// block from checkpoints whose stride divides 128; the tile backward (dv =
+// 256) needs fp32 states before every 16-token tile.
+bool bwd_ckpt_usable(const bdla_dims &d, int ckpt_stride, int ckpt_bf16)
+{
+    if (ckpt_stride <= 0)
+        return false;
+    if (d.dv <= 128)
+        return kBlock % ckpt_stride == 0;
+    return ckpt_stride == kChunk && !ckpt_bf16;
+}
+
+Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride, int ckpt_bf16)
 {
     Layout L;
     size_t off = round_up(kStatusBytes);
     const int64_t tokens = total_tokens(d);
+    const size_t per_head = round_up((size_t)tokens * sizeof(float));
     L.gamma = off;
-    off += round_up((size_t)tokens * d.H * sizeof(float));
-    if (op == BDLA_OP_BWD && bwd_needs_states(ckpt_stride)) {
-        const int64_t slots = (tokens + kChunk - 1) / kChunk + n_docs;
-        L.states = off;
-        off += round_up((size_t)d.H * slots * d.dk * d.dv * sizeof(float));
+    off += per_head * d.H;
+    if (op == BDLA_OP_BWD) {
+        L.dfac = off;
+        off += per_head * d.H;
+        if (!bwd_ckpt_usable(d, ckpt_stride, ckpt_bf16)) {
+            L.states = off;
+            if (d.dv <= 128) {
+                const int64_t slots = (tokens + kBlock - 1) / kBlock + n_docs;
+                off += round_up((size_t)d.H * slots * d.dk * d.dv * 2);
+            } else {
+                const int64_t slots = (tokens + kChunk - 1) / kChunk + n_docs;
+                off += round_up((size_t)d.H * slots * d.dk * d.dv * sizeof(float));
+            }
+        }
     }
     L.total = off;
     return L;
@@ -117,8 +138,9 @@ Problem make_problem(const bdla_dims &d, const int32_t *cu, int n_docs, float b,
 
 bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a, float b,
                      int chunk, const int32_t *cu, int n_docs, bool varlen, const float *h0,
-                     void *o, bdla_dtype o_dtype, float *hT, float *ckpt, int ckpt_stride,
-                     bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+                     void *o, bdla_dtype o_dtype, float *hT, void *ckpt, int ckpt_stride,
+                     bdla_dtype ckpt_dtype, bdla_dims d, bdla_decay_mode mode, void *ws,
+                     size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_dims(d, varlen, n_docs));
     BDLA_TRY(check_decay(b, chunk, mode));
@@ -132,24 +154,30 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
         return BDLA_ERR_UNSUPPORTED;
     if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
         return BDLA_ERR_SHAPE;
-    const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, ckpt_stride);
+    if (ckpt && ckpt_dtype != BDLA_F32 && ckpt_dtype != BDLA_BF16)
+        return BDLA_ERR_UNSUPPORTED;
+    if (ckpt && ckpt_dtype == BDLA_BF16 && ckpt_stride % kBlock != 0)
+        return BDLA_ERR_UNSUPPORTED;
+    const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, 0, 0);
     BDLA_TRY(check_ws(ws, ws_bytes, L.total));
     Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
     float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
-    mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
-    mark_stop(BDLA_KERNEL_DECAY, p.stream);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    const bool fused_ckpt = ckpt && ckpt_stride % kBlock == 0;
+    mark_start(BDLA_KERNEL_DECAY, p.stream);
+    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
+    mark_stop(BDLA_KERNEL_DECAY, p.stream);
     mark_start(BDLA_KERNEL_FWD, p.stream);
-    BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT, ckpt,
-                               ckpt_stride));
+    BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
+                               fused_ckpt ? ckpt : nullptr, ckpt_dtype == BDLA_BF16, ckpt_stride));
     mark_stop(BDLA_KERNEL_FWD, p.stream);
-    if (ckpt && ckpt_stride % 128 != 0) {
-        // checkpoints inside the 128-token blocks: tile-serial state pass
+    if (ckpt && !fused_ckpt) {
+        // checkpoints inside the 128-token blocks: tile-serial state pass (fp32)
         mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, ckpt, ckpt_stride));
+        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr,
+                                  static_cast<float *>(ckpt), ckpt_stride));
         mark_stop(BDLA_KERNEL_STATES, p.stream);
     }
     return BDLA_OK;
@@ -157,9 +185,9 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
 
 bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a, float b,
                      int chunk, const int32_t *cu, int n_docs, bool varlen, const float *h0,
-                     const void *dO, const float *dhT, const float *ckpt, int ckpt_stride,
-                     float *dq, float *dk, float *dv, float *da, float *dh0, bdla_dims d,
-                     bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+                     const void *dO, const float *dhT, const void *ckpt, int ckpt_stride,
+                     bdla_dtype ckpt_dtype, float *dq, float *dk, float *dv, float *da, float *dh0,
+                     bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_dims(d, varlen, n_docs));
     BDLA_TRY(check_decay(b, chunk, mode));
@@ -173,28 +201,53 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
         return BDLA_ERR_ALIGN;
     if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
         return BDLA_ERR_SHAPE;
+    if (ckpt && ckpt_dtype != BDLA_F32 && ckpt_dtype != BDLA_BF16)
+        return BDLA_ERR_UNSUPPORTED;
     const int stride = ckpt ? ckpt_stride : 0;
-    const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride);
+    const int ck_bf16 = ckpt && ckpt_dtype == BDLA_BF16;
+    const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride, ck_bf16);
     BDLA_TRY(check_ws(ws, ws_bytes, L.total));
     Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
-    float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
+    char *wsb = static_cast<char *>(ws);
+    float *gamma = reinterpret_cast<float *>(wsb + L.gamma);
+    float *dfac = reinterpret_cast<float *>(wsb + L.dfac);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    const auto *dob = static_cast<const __nv_bfloat16 *>(dO);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
+    BDLA_CUDA(launch_decay(p, a, gamma, dfac));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
-    const float *states = ckpt;
-    if (bwd_needs_states(stride)) {
-        float *st = reinterpret_cast<float *>(static_cast<char *>(ws) + L.states);
+    const bool use_ckpt = bwd_ckpt_usable(d, stride, ck_bf16);
+    if (d.dv <= 128) {
+        const void *states = ckpt;
+        int st_bf16 = ck_bf16, st_stride = stride;
+        if (!use_ckpt) {
+            void *stb = wsb + L.states;
+            mark_start(BDLA_KERNEL_STATES, p.stream);
+            BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock));
+            mark_stop(BDLA_KERNEL_STATES, p.stream);
+            states = stb;
+            st_bf16 = 1;
+            st_stride = kBlock;
+        }
+        mark_start(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride,
+                                   dhT, dq, dk, dv, da, dh0));
+        mark_stop(BDLA_KERNEL_BWD, p.stream);
+        return BDLA_OK;
+    }
+    // dv = 256: tile-serial backward over fp32 per-tile states
+    const float *states = static_cast<const float *>(ckpt);
+    if (!use_ckpt) {
+        float *st = reinterpret_cast<float *>(wsb + L.states);
         mark_start(BDLA_KERNEL_STATES, p.stream);
         BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, st, kChunk));
         mark_stop(BDLA_KERNEL_STATES, p.stream);
         states = st;
     }
     mark_start(BDLA_KERNEL_BWD, p.stream);
-    BDLA_CUDA(launch_bwd_tile(p, qb, kb, vb, a, gamma, static_cast<const __nv_bfloat16 *>(dO),
-                              dhT, states, dq, dk, dv, da, dh0));
+    BDLA_CUDA(launch_bwd_tile(p, qb, kb, vb, a, gamma, dob, dhT, states, dq, dk, dv, da, dh0));
     mark_stop(BDLA_KERNEL_BWD, p.stream);
     return BDLA_OK;
 }
@@ -209,7 +262,7 @@ size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mod
     const bool varlen = n_docs > 0;
     if (check_dims(d, varlen, n_docs) != BDLA_OK)
         return 0;
-    return layout(op, d, varlen ? n_docs : d.B, ckpt_stride).total;
+    return layout(op, d, varlen ? n_docs : d.B, ckpt_stride, 0).total;
 }
 
 bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seqlens, int n_docs,
@@ -233,40 +286,42 @@ bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seq
 
 bdla_status bdla_fwd(const void *q, const void *k, const void *v, const float *a, float b,
                      int chunk, const float *h0, void *o, bdla_dtype o_dtype, float *hT,
-                     float *ckpt, int ckpt_stride, bdla_dims d, bdla_decay_mode mode, void *ws,
-                     size_t ws_bytes, void *stream)
+                     void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype, bdla_dims d,
+                     bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
 {
     return fwd_impl(q, k, v, a, b, chunk, nullptr, 0, false, h0, o, o_dtype, hT, ckpt,
-                    ckpt_stride, d, mode, ws, ws_bytes, stream);
+                    ckpt_stride, ckpt_dtype, d, mode, ws, ws_bytes, stream);
 }
 
 bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const float *a, float b,
                             int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
-                            void *o, bdla_dtype o_dtype, float *hT, float *ckpt, int ckpt_stride,
-                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+                            void *o, bdla_dtype o_dtype, float *hT, void *ckpt, int ckpt_stride,
+                            bdla_dtype ckpt_dtype, bdla_dims d, bdla_decay_mode mode, void *ws,
+                            size_t ws_bytes, void *stream)
 {
     return fwd_impl(q, k, v, a, b, chunk, cu_seqlens, n_docs, true, h0, o, o_dtype, hT, ckpt,
-                    ckpt_stride, d, mode, ws, ws_bytes, stream);
+                    ckpt_stride, ckpt_dtype, d, mode, ws, ws_bytes, stream);
 }
 
 bdla_status bdla_bwd(const void *q, const void *k, const void *v, const float *a, float b,
                      int chunk, const float *h0, const void *dO, const float *dhT,
-                     const float *ckpt, int ckpt_stride, float *dq, float *dk, float *dv,
-                     float *da, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
-                     size_t ws_bytes, void *stream)
+                     const void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype, float *dq,
+                     float *dk, float *dv, float *da, float *dh0, bdla_dims d,
+                     bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
 {
-    return bwd_impl(q, k, v, a, b, chunk, nullptr, 0, false, h0, dO, dhT, ckpt, ckpt_stride, dq,
-                    dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
+    return bwd_impl(q, k, v, a, b, chunk, nullptr, 0, false, h0, dO, dhT, ckpt, ckpt_stride,
+                    ckpt_dtype, dq, dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
 }
 
 bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const float *a, float b,
                             int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
-                            const void *dO, const float *dhT, const float *ckpt, int ckpt_stride,
-                            float *dq, float *dk, float *dv, float *da, float *dh0, bdla_dims d,
-                            bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+                            const void *dO, const float *dhT, const void *ckpt, int ckpt_stride,
+                            bdla_dtype ckpt_dtype, float *dq, float *dk, float *dv, float *da,
+                            float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
+                            size_t ws_bytes, void *stream)
 {
     return bwd_impl(q, k, v, a, b, chunk, cu_seqlens, n_docs, true, h0, dO, dhT, ckpt,
-                    ckpt_stride, dq, dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
+                    ckpt_stride, ckpt_dtype, dq, dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
 }
 
 bdla_status bdla_read_status(void *ws, void *stream)

@@ -98,13 +98,15 @@ __device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b, float acc)
     return acc;
 }
 
-template <int DV, bool ABL>
+// STATES: only the state chain runs (no Q, no scores, no output); it writes
+// the checkpoints the backward reads.
+template <int DV, bool ABL, bool STATES>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const float *__restrict__ gamma,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
-                 float *__restrict__ hT, float *__restrict__ ckpt, int ckpt_stride,
+                 float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
                  int64_t n_slots, DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -164,7 +166,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
-            const uint32_t qk_bytes = (uint32_t)kpan * 2u * kPanel;
+            const uint32_t qk_bytes = (uint32_t)kpan * (STATES ? 1u : 2u) * kPanel;
             const uint32_t v_bytes = (uint32_t)(DV / 64) * kPanel;
             int last_qk[2] = {-1, -1}, last_v = -1;
             bool consumed = true;
@@ -179,7 +181,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 mbar_arrive_expect_tx(&sm.full_qk[s], qk_bytes);
                 for (int p = 0; p < kpan; ++p) {
-                    tma_load_3d(sm.q[s] + p * kPanel, &tq, &sm.full_qk[s], p * 64, h, t0);
+                    if (!STATES)
+                        tma_load_3d(sm.q[s] + p * kPanel, &tq, &sm.full_qk[s], p * 64, h, t0);
                     tma_load_3d(sm.k[s] + p * kPanel, &tk, &sm.full_qk[s], p * 64, h, t0);
                 }
                 last_qk[s] = j;
@@ -228,7 +231,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 umma_commit(&sm.score_full[s]);
                 return true;
             };
-            if (nblk > 0)
+            if (nblk > 0 && !STATES)
                 ok = issue_qk(0);
             for (int j = 0; ok && j < nblk; ++j) {
                 const int s = j & 1;
@@ -236,21 +239,23 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     ok = false;
                     break;
                 }
-                if (j + 1 < nblk && !(ok = issue_qk(j + 1)))
+                if (!STATES && j + 1 < nblk && !(ok = issue_qk(j + 1)))
                     break;
                 if (!mbar_wait(&sm.p_ready, j & 1, kWaitNs) || !mbar_wait(&sm.full_v, j & 1, kWaitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // O = P V
-                for (int ks = 0; ks < BT / 16; ++ks)
-                    umma_bf16(t_o, sdesc_sw128(sp + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
-                              sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
-                // O += (Q o e^{Lam}) S_in
-                for (int ks = 0; ks < dk / 16; ++ks)
-                    umma_bf16(t_o, sdesc_sw128(sq[s] + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
-                              sdesc_sw128(ssb + ks * 2048, kPanel, 1024), id_pv, 1);
+                if (!STATES) {
+                    // O = P V
+                    for (int ks = 0; ks < BT / 16; ++ks)
+                        umma_bf16(t_o, sdesc_sw128(sp + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
+                                  sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
+                    // O += (Q o e^{Lam}) S_in
+                    for (int ks = 0; ks < dk / 16; ++ks)
+                        umma_bf16(t_o, sdesc_sw128(sq[s] + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
+                                  sdesc_sw128(ssb + ks * 2048, kPanel, 1024), id_pv, 1);
+                }
                 // S += (K o e^{Lam_end - Lam})^T V
                 for (int ks = 0; ks < BT / 16; ++ks)
                     umma_bf16(t_s, sdesc_sw128(sk[s] + ks * 2048, kPanel, 1024),
@@ -356,7 +361,10 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
             epi_sync();
 
-            ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+            if (STATES)
+                ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+            else
+                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
@@ -388,14 +396,16 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int p = 0; p < kpan; ++p)
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    uint4 *qa = reinterpret_cast<uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
                     uint4 *ka = reinterpret_cast<uint4 *>(sm.k[s] + p * kPanel + sw128_offset(r, c8));
-                    *qa = scale_bf16x8(*qa, qsc);
                     *ka = scale_bf16x8(*ka, ksc);
+                    if (!STATES) {
+                        uint4 *qa = reinterpret_cast<uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
+                        *qa = scale_bf16x8(*qa, qsc);
+                    }
                 }
             // ---- P = decay-weighted causal scores (bf16, K-major rows t)
 #pragma unroll
-            for (int c = 0; c < BT / 32; ++c) {
+            for (int c = 0; c < (STATES ? 0 : BT / 32); ++c) {
                 uint32_t x[32];
                 tmem_ld32(t_score0 + 128 * s + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -425,7 +435,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
             }
             tc_fence_before();
-            mbar_arrive(&sm.score_free[s]);
+            if (!STATES)
+                mbar_arrive(&sm.score_free[s]);
 
             // ---- output of the previous block
             if (j > 0) {
@@ -433,37 +444,45 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 if (!ok)
                     break;
                 tc_fence_after();
-                store_o(j - 1);
+                if (!STATES)
+                    store_o(j - 1);
             }
             // ---- state: checkpoint, bf16 copy for the Q S GEMM, decay for the K V update
             {
                 const float el = expf(lend);
                 const bool wck = ckpt != nullptr && r < dk && ckpt_stride % BT == 0 &&
                                  ((int64_t)j * BT) % ckpt_stride == 0;
-                float *ckrow = wck ? ckpt + ((size_t)h * n_slots +
-                                             ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride)) *
-                                                sstride + (size_t)r * dv + j0
-                                   : nullptr;
+                const size_t ckoff = wck ? ((size_t)h * n_slots +
+                                            ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride)) *
+                                               sstride + (size_t)r * dv + j0
+                                         : 0;
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) {
                     uint32_t x[32];
                     tmem_ld32(t_s + lane_off + c * 32, x);
                     tmem_ld_wait();
-                    if (wck) {
-#pragma unroll
-                        for (int k4 = 0; k4 < 8; ++k4)
-                            reinterpret_cast<uint4 *>(ckrow + c * 32)[k4] =
-                                make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
-                    }
                     uint32_t u[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-                    unsigned char *sp = sm.sb + (c >> 1) * kPanel;
+                    if (wck && !ck_bf16) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(ckpt) + ckoff + c * 32);
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4)
-                        *reinterpret_cast<uint4 *>(sp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            dst[k4] = make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    } else if (wck) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(ckpt) + ckoff + c * 32);
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            dst[k4] = make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                    }
+                    if (!STATES) {
+                        unsigned char *sp = sm.sb + (c >> 1) * kPanel;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            *reinterpret_cast<uint4 *>(sp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                                make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         x[i] = __float_as_uint(__uint_as_float(x[i]) * el);
@@ -479,7 +498,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, kWaitNs)) && !*abort_flag;
             if (ok) {
                 tc_fence_after();
-                store_o(nblk - 1);
+                if (!STATES)
+                    store_o(nblk - 1);
             }
         }
         if (ok && hT != nullptr && r < dk) {
@@ -549,12 +569,13 @@ bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tok
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DV, bool ABL>
+template <int DV, bool ABL, bool STATES>
 static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                       const CUtensorMap &mv, const float *gamma, const float *h0,
-                                      void *o, int o_f32, float *hT, float *ckpt, int ckpt_stride)
+                                      void *o, int o_f32, float *hT, void *ckpt, int ck_bf16,
+                                      int ckpt_stride)
 {
-    auto kern = fwd_sm100_kernel<DV, ABL>;
+    auto kern = fwd_sm100_kernel<DV, ABL, STATES>;
     const size_t smem = sizeof(FwdSmem<DV>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
@@ -562,13 +583,14 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
     dim3 grid(p.dv / DV, p.H, p.n_docs);
     kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
-                                                p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots, p.st);
+                                                p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
+                                                n_slots, p.st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                             int o_f32, float *hT, float *ckpt, int ckpt_stride)
+                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -581,15 +603,30 @@ cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
         return cudaGetLastError();
     }
     CUtensorMap mq, mk, mv;
-    if (!make_token_map(&mq, q, p.dk, p.H, p.tokens) || !make_token_map(&mk, k, p.dk, p.H, p.tokens) ||
-        !make_token_map(&mv, v, p.dv, p.H, p.tokens))
+    const bool states_only = (o == nullptr);
+    if ((!states_only && !make_token_map(&mq, q, p.dk, p.H, p.tokens)) ||
+        !make_token_map(&mk, k, p.dk, p.H, p.tokens) || !make_token_map(&mv, v, p.dv, p.H, p.tokens))
         return cudaErrorInvalidValue;
+    if (states_only)
+        mq = mk;
     const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
-    if (p.dv == 64)
-        return abl ? launch_fwd_sm100_t<64, true>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride)
-                   : launch_fwd_sm100_t<64, false>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride);
-    return abl ? launch_fwd_sm100_t<128, true>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride)
-               : launch_fwd_sm100_t<128, false>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ckpt_stride);
+#define BDLA_FWD_GO(DV_, ABL_, ST_)                                                                 \
+    return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ck_bf16, \
+                                              ckpt_stride)
+    if (states_only) {
+        if (p.dv == 64)
+            BDLA_FWD_GO(64, false, true);
+        BDLA_FWD_GO(128, false, true);
+    }
+    if (p.dv == 64) {
+        if (abl)
+            BDLA_FWD_GO(64, true, false);
+        BDLA_FWD_GO(64, false, false);
+    }
+    if (abl)
+        BDLA_FWD_GO(128, true, false);
+    BDLA_FWD_GO(128, false, false);
+#undef BDLA_FWD_GO
 }
 
 }  // namespace bdla

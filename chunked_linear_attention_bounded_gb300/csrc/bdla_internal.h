@@ -55,9 +55,17 @@ cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv
 
 // Tensor-core forward (tcgen05 / TMEM / TMA): o, hT and checkpoints whose
 // stride is a multiple of 128 tokens.
+// o == nullptr runs the state chain only (checkpoints for the backward).
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                             int o_f32, float *hT, float *ckpt, int ckpt_stride);
+                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride);
+
+// Tensor-core backward for dv <= 128.  `states` holds the state before every
+// 128-token block: checkpoints whose stride divides 128, fp32 or bf16.
+cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
+                             const float *dfac, const void *states, int st_bf16, int st_stride,
+                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0);
 
 // Tile-serial backward; `states` holds the state before every 16-token tile
 // (checkpoint layout with stride 16).

@@ -43,9 +43,12 @@
  *   o         bf16 or fp32 [B, T, H, dv]
  *   dq, dk    fp32  [B, T, H, dk];  dv fp32 [B, T, H, dv]
  *   h0, hT, dh0, dhT   fp32 [n_docs, H, dk, dv]   (NULL = zero / not wanted)
- *   ckpt      fp32  [H, n_slots, dk, dv], n_slots = ceil(B*T / stride) + n_docs;
+ *   ckpt      fp32 or bf16 [H, n_slots, dk, dv], n_slots = ceil(B*T / stride) + n_docs;
  *             slot floor(cu[n] / stride) + n + c holds the state of document n
  *             before its doc-local token c*stride (slot c = 0 holds h0).
+ *             bf16 checkpoints need a stride that is a multiple of 128; the
+ *             backward uses checkpoints whose stride divides 128 (16, 32, 64,
+ *             128), other strides make it recompute the states it needs.
  */
 #ifndef BDLA_H
 #define BDLA_H
@@ -90,7 +93,8 @@ enum { BDLA_OP_FWD = 0, BDLA_OP_BWD = 1, BDLA_OP_DECAY = 2 };
 /*
  * Bytes of device workspace an op needs.  `op` is BDLA_OP_*, `n_docs` the
  * document count of a varlen call (0 for fixed-length calls), `ckpt_stride`
- * the stride of the checkpoints the backward will be handed (0 if none).
+ * the stride of the fp32 checkpoints the backward will be handed (0 if none;
+ * bf16 checkpoints: pass their stride only when dv <= 128).
  * Returns 0 on invalid dims.  The first 256 bytes of every workspace are the
  * device status word: zero them once after allocating the workspace
  * (bdla_read_status clears them again).
@@ -110,19 +114,19 @@ bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seq
 
 /*
  * Forward pass.  Writes o (dtype o_dtype) and, when non-NULL, hT and the
- * state checkpoints ckpt every ckpt_stride tokens (ckpt_stride a multiple of
- * 16; ignored when ckpt is NULL).
+ * state checkpoints ckpt (dtype ckpt_dtype) every ckpt_stride tokens
+ * (ckpt_stride a multiple of 16; both ignored when ckpt is NULL).
  */
 bdla_status bdla_fwd(const void *q, const void *k, const void *v, const float *a,
                      float b, int chunk, const float *h0,
                      void *o, bdla_dtype o_dtype, float *hT,
-                     float *ckpt, int ckpt_stride,
+                     void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype,
                      bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
 
 bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const float *a,
                             float b, int chunk, const int32_t *cu_seqlens, int n_docs,
                             const float *h0, void *o, bdla_dtype o_dtype, float *hT,
-                            float *ckpt, int ckpt_stride,
+                            void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype,
                             bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
                             void *stream);
 
@@ -135,14 +139,14 @@ bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const f
  */
 bdla_status bdla_bwd(const void *q, const void *k, const void *v, const float *a,
                      float b, int chunk, const float *h0, const void *dO, const float *dhT,
-                     const float *ckpt, int ckpt_stride,
+                     const void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype,
                      float *dq, float *dk, float *dv, float *da, float *dh0,
                      bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
 
 bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const float *a,
                             float b, int chunk, const int32_t *cu_seqlens, int n_docs,
                             const float *h0, const void *dO, const float *dhT,
-                            const float *ckpt, int ckpt_stride,
+                            const void *ckpt, int ckpt_stride, bdla_dtype ckpt_dtype,
                             float *dq, float *dk, float *dv, float *da, float *dh0,
                             bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
                             void *stream);

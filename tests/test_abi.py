@@ -56,8 +56,8 @@ FAKE = ctypes.c_void_p(1 << 20)
 
 
 def _fwd(L, b=-5.0, chunk=16, dims=(1, 64, 2, 64, 64), mode=0, q=FAKE, ws=FAKE, ws_bytes=1 << 40,
-         ckpt=None, stride=0, o_dtype=0):
-    return L.bdla_fwd(q, FAKE, FAKE, FAKE, b, chunk, None, FAKE, o_dtype, None, ckpt, stride,
+         ckpt=None, stride=0, o_dtype=0, ck_dtype=1):
+    return L.bdla_fwd(q, FAKE, FAKE, FAKE, b, chunk, None, FAKE, o_dtype, None, ckpt, stride, ck_dtype,
                       bdla.Dims(*dims), mode, ws, ws_bytes, None)
 
 
@@ -77,13 +77,15 @@ def test_host_validation_before_launch(L):
     assert _fwd(L, ws_bytes=16) == 6
     assert _fwd(L, ckpt=FAKE, stride=24) == 2
     assert _fwd(L, o_dtype=5) == 5
-    st = L.bdla_bwd(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, None, None, None, 0, FAKE, FAKE, FAKE,
+    assert _fwd(L, ckpt=FAKE, stride=64, ck_dtype=0) == 5    # bf16 checkpoints need stride % 128 == 0
+    assert _fwd(L, ckpt=FAKE, stride=128, ck_dtype=7) == 5
+    st = L.bdla_bwd(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, None, None, None, 0, 1, FAKE, FAKE, FAKE,
                     FAKE, None, bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
     assert st == 1                                    # dO missing
-    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 2, None, FAKE, 0, None, None, 0,
+    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 2, None, FAKE, 0, None, None, 0, 1,
                            bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
     assert st == 1                                    # cu_seqlens missing
-    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, FAKE, 2, None, FAKE, 0, None, None, 0,
+    st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, FAKE, 2, None, FAKE, 0, None, None, 0, 1,
                            bdla.Dims(2, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
     assert st == 2                                    # varlen needs B == 1
 
