@@ -24,12 +24,13 @@ OP_FWD, OP_BWD, OP_DECAY = 0, 1, 2
 
 STATUS_NAMES = {0: "BDLA_OK", 1: "BDLA_ERR_NULL", 2: "BDLA_ERR_SHAPE", 3: "BDLA_ERR_ALIGN",
                 4: "BDLA_ERR_RANGE", 5: "BDLA_ERR_UNSUPPORTED", 6: "BDLA_ERR_WORKSPACE",
-                7: "BDLA_ERR_CUDA", 8: "BDLA_ERR_TIMEOUT", 9: "BDLA_ERR_DEVICE"}
+                7: "BDLA_ERR_CUDA", 8: "BDLA_ERR_TIMEOUT", 9: "BDLA_ERR_DEVICE",
+                10: "BDLA_ERR_TOO_LARGE"}
 
 # Every symbol include/bdla.h declares.
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
            "bdla_bwd_varlen", "bdla_read_status", "bdla_status_string", "bdla_version",
-           "bdla_set_kernel_events")
+           "bdla_set_kernel_events", "bdla_fwd_noalloc")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES = 0, 1, 2, 3
 
 
@@ -76,6 +77,8 @@ def lib():
         L.bdla_version.restype = ci
         L.bdla_set_kernel_events.argtypes = [ci, vp, vp]
         L.bdla_set_kernel_events.restype = ci
+        L.bdla_fwd_noalloc.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, ci, vp, Dims, ci, vp]
+        L.bdla_fwd_noalloc.restype = ci
         del i32
         _lib = L
     return _lib

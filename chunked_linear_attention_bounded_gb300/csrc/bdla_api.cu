@@ -352,6 +352,7 @@ const char *bdla_status_string(bdla_status s)
     case BDLA_ERR_CUDA: return "a CUDA runtime call failed";
     case BDLA_ERR_TIMEOUT: return "device: a bounded wait expired";
     case BDLA_ERR_DEVICE: return "device: malformed cu_seqlens or another device-side check";
+    case BDLA_ERR_TOO_LARGE: return "problem larger than the fixed scratch of bdla_fwd_noalloc";
     }
     return "unknown status";
 }

@@ -70,7 +70,8 @@ typedef enum {
     BDLA_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or too small */
     BDLA_ERR_CUDA = 7,         /* a CUDA runtime call (launch, attribute) failed */
     BDLA_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up */
-    BDLA_ERR_DEVICE = 9        /* device: malformed cu_seqlens or another device check */
+    BDLA_ERR_DEVICE = 9,       /* device: malformed cu_seqlens or another device check */
+    BDLA_ERR_TOO_LARGE = 10    /* bdla_fwd_noalloc: problem larger than its fixed scratch */
 } bdla_status;
 
 typedef enum {
@@ -169,6 +170,28 @@ bdla_status bdla_read_status(void *ws, void *stream);
 enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KERNEL_STATES = 3,
        BDLA_KERNEL_COUNT = 4 };
 bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
+
+/*
+ * Forward pass for callers that cannot allocate device memory (no workspace
+ * argument).  The pages have no counterpart: this is an interface for
+ * callers, such as code running inside an allocator's callbacks or a runtime
+ * that only hands out fixed buffers for inputs and outputs, which must not
+ * call cudaMalloc.  Same operation and argument meaning as bdla_fwd for
+ * fixed-length batches, without checkpoints.  Its scratch (the per-token
+ * decay cumsum for at most 2^21 (token, head) pairs, i.e. B*T*H <= 2097152,
+ * and a device status word) is a fixed array inside the library that every
+ * GPU loading the library holds (about 8 MiB) until exit; larger problems
+ * return BDLA_ERR_TOO_LARGE before any launch.  It calls no cudaMalloc or
+ * cudaFree.  The first call on each device looks up the array's device
+ * address; make that first call before any stream capture.  Every call
+ * shares the one array: calls that overlap on the GPU (different streams
+ * without ordering) race and give wrong results; order them.  Device-side
+ * errors (a bounded wait that expired) are recorded in the library's own
+ * status word, which each call clears, and are not reported.
+ */
+bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void *v, const float *a,
+                             float b, int chunk, const float *h0, void *o, bdla_dtype o_dtype,
+                             float *hT, bdla_dims d, bdla_decay_mode mode, void *stream);
 
 /* Static English description of a status code. */
 const char *bdla_status_string(bdla_status s);

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(10):
+    for code in range(11):
         assert bdla.status_string(code) not in ("", "unknown status")
     assert bdla.status_string(123) == "unknown status"
     assert L.bdla_version() >= 100
