@@ -23,7 +23,8 @@ bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr
 struct Layout {
     size_t gamma = 0;    // Gamma [H, tokens] fp32
     size_t dfac = 0;     // d lambda / d a [H, tokens] fp32 (backward)
-    size_t states = 0;   // recomputed states for the backward, 0 if unused
+    size_t states = 0;   // recomputed bf16 states for the backward, 0 if unused
+    size_t part = 0;     // partial dq, dk, da of the second dv slice (dv = 256)
     size_t total = 0;
 };
 
@@ -31,19 +32,11 @@ int64_t total_tokens(const bdla_dims &d) { return (int64_t)d.B * d.T; }
 
 constexpr int kBlock = 128;   // tokens per block of the tensor-core kernels
 
-// The tensor-core backward (dv <= 128) reads the state before every 128-token
-// block from checkpoints whose stride divides 128; the tile backward (dv =
-// 256) needs fp32 states before every 16-token tile.
-bool bwd_ckpt_usable(const bdla_dims &d, int ckpt_stride, int ckpt_bf16)
-{
-    if (ckpt_stride <= 0)
-        return false;
-    if (d.dv <= 128)
-        return kBlock % ckpt_stride == 0;
-    return ckpt_stride == kChunk && !ckpt_bf16;
-}
+// The backward reads the state before every 128-token block from checkpoints
+// whose stride divides 128 (fp32 or bf16); otherwise it recomputes them.
+bool bwd_ckpt_usable(int ckpt_stride) { return ckpt_stride > 0 && kBlock % ckpt_stride == 0; }
 
-Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride, int ckpt_bf16)
+Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
 {
     Layout L;
     size_t off = round_up(kStatusBytes);
@@ -54,15 +47,15 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride, int ckpt_
     if (op == BDLA_OP_BWD) {
         L.dfac = off;
         off += per_head * d.H;
-        if (!bwd_ckpt_usable(d, ckpt_stride, ckpt_bf16)) {
+        if (!bwd_ckpt_usable(ckpt_stride)) {
             L.states = off;
-            if (d.dv <= 128) {
-                const int64_t slots = (tokens + kBlock - 1) / kBlock + n_docs;
-                off += round_up((size_t)d.H * slots * d.dk * d.dv * 2);
-            } else {
-                const int64_t slots = (tokens + kChunk - 1) / kChunk + n_docs;
-                off += round_up((size_t)d.H * slots * d.dk * d.dv * sizeof(float));
-            }
+            const int64_t slots = (tokens + kBlock - 1) / kBlock + n_docs;
+            off += round_up((size_t)d.H * slots * d.dk * d.dv * 2);
+        }
+        if (d.dv > 128) {
+            L.part = off;
+            off += round_up((size_t)(d.dv / 128 - 1) * (2 * tokens * d.H * d.dk + tokens * d.H) *
+                            sizeof(float));
         }
     }
     L.total = off;
@@ -158,7 +151,7 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
         return BDLA_ERR_UNSUPPORTED;
     if (ckpt && ckpt_dtype == BDLA_BF16 && ckpt_stride % kBlock != 0)
         return BDLA_ERR_UNSUPPORTED;
-    const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, 0, 0);
+    const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, 0);
     BDLA_TRY(check_ws(ws, ws_bytes, L.total));
     Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
     float *gamma = reinterpret_cast<float *>(static_cast<char *>(ws) + L.gamma);
@@ -205,7 +198,7 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
         return BDLA_ERR_UNSUPPORTED;
     const int stride = ckpt ? ckpt_stride : 0;
     const int ck_bf16 = ckpt && ckpt_dtype == BDLA_BF16;
-    const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride, ck_bf16);
+    const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride);
     BDLA_TRY(check_ws(ws, ws_bytes, L.total));
     Problem p = make_problem(d, varlen ? cu : nullptr, n_docs, b, mode, ws, stream);
     char *wsb = static_cast<char *>(ws);
@@ -218,36 +211,21 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     mark_start(BDLA_KERNEL_DECAY, p.stream);
     BDLA_CUDA(launch_decay(p, a, gamma, dfac));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
-    const bool use_ckpt = bwd_ckpt_usable(d, stride, ck_bf16);
-    if (d.dv <= 128) {
-        const void *states = ckpt;
-        int st_bf16 = ck_bf16, st_stride = stride;
-        if (!use_ckpt) {
-            void *stb = wsb + L.states;
-            mark_start(BDLA_KERNEL_STATES, p.stream);
-            BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock));
-            mark_stop(BDLA_KERNEL_STATES, p.stream);
-            states = stb;
-            st_bf16 = 1;
-            st_stride = kBlock;
-        }
-        mark_start(BDLA_KERNEL_BWD, p.stream);
-        BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride,
-                                   dhT, dq, dk, dv, da, dh0));
-        mark_stop(BDLA_KERNEL_BWD, p.stream);
-        return BDLA_OK;
-    }
-    // dv = 256: tile-serial backward over fp32 per-tile states
-    const float *states = static_cast<const float *>(ckpt);
-    if (!use_ckpt) {
-        float *st = reinterpret_cast<float *>(wsb + L.states);
+    const void *states = ckpt;
+    int st_bf16 = ck_bf16, st_stride = stride;
+    if (!bwd_ckpt_usable(stride)) {
+        void *stb = wsb + L.states;
         mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, st, kChunk));
+        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock));
         mark_stop(BDLA_KERNEL_STATES, p.stream);
-        states = st;
+        states = stb;
+        st_bf16 = 1;
+        st_stride = kBlock;
     }
+    float *part = L.part ? reinterpret_cast<float *>(wsb + L.part) : nullptr;
     mark_start(BDLA_KERNEL_BWD, p.stream);
-    BDLA_CUDA(launch_bwd_tile(p, qb, kb, vb, a, gamma, dob, dhT, states, dq, dk, dv, da, dh0));
+    BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride, dhT, dq,
+                               dk, dv, da, dh0, part));
     mark_stop(BDLA_KERNEL_BWD, p.stream);
     return BDLA_OK;
 }
@@ -262,7 +240,7 @@ size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mod
     const bool varlen = n_docs > 0;
     if (check_dims(d, varlen, n_docs) != BDLA_OK)
         return 0;
-    return layout(op, d, varlen ? n_docs : d.B, ckpt_stride, 0).total;
+    return layout(op, d, varlen ? n_docs : d.B, ckpt_stride).total;
 }
 
 bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seqlens, int n_docs,

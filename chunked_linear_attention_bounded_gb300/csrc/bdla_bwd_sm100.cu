@@ -61,6 +61,9 @@ struct BwdSmem {
     float scan[2][4];
     float gam[BT / kChunk];
     float se[4];
+    float gq[BT];                  // Gamma per row (ablation diagonal path)
+    float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
+    float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
     uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
         mf_done, acc_free, drain;
     uint32_t tmem_base;
@@ -90,6 +93,17 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 x, float s)
     for (int i = 0; i < 4; ++i)
         w[i] = pack_bf16(bf16_lo(w[i]) * s, bf16_hi(w[i]) * s);
     return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b, float acc)
+{
+    const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = fmaf(bf16_lo(x[i]), bf16_lo(y[i]), acc);
+        acc = fmaf(bf16_hi(x[i]), bf16_hi(y[i]), acc);
+    }
+    return acc;
 }
 
 __device__ __forceinline__ float warp_sum(float x)
@@ -171,22 +185,32 @@ __device__ __forceinline__ void load_state_row(const void *states, int st_bf16, 
     }
 }
 
-template <int DV>
+// ABL: unbounded -softplus decay; the diagonal 16-token tiles of P and dP
+// are computed pair by pair on CUDA cores (explicit position-pair path).
+// With dv split over gridDim.z slices, slice z handles value columns
+// [z*DV, (z+1)*DV): dv is exact per slice, while dq, dk and da are partial
+// sums that slice z > 0 writes at offset z*part_qk / z*part_a (added to
+// slice 0 by a separate kernel).
+template <int DV, bool ABL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const float *__restrict__ gamma, const float *__restrict__ dfac,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
-                 const float *__restrict__ dhT, float *__restrict__ dq, float *__restrict__ dkk,
-                 float *__restrict__ dvv, float *__restrict__ da, float *__restrict__ dh0,
-                 DeviceStatus *st)
+                 const float *__restrict__ dhT, float *__restrict__ dq_base, float *__restrict__ dk_base,
+                 float *__restrict__ dvv, float *__restrict__ da_base, float *__restrict__ dh0,
+                 float *__restrict__ part, int64_t part_qk, int64_t part_a, DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, n = blockIdx.y;
-    const int j0 = 0;
+    const int j0 = blockIdx.z * DV;
+    // slice 0 writes dq, dk, da; later slices write partial sums into `part`
+    float *dq = blockIdx.z == 0 ? dq_base : part + (size_t)(blockIdx.z - 1) * (2 * part_qk + part_a);
+    float *dkk = blockIdx.z == 0 ? dk_base : dq + part_qk;
+    float *da = blockIdx.z == 0 ? da_base : dq + 2 * part_qk;
     const DocSpan d = doc_span(cu, n, T);
     if (!doc_valid(d, tokens))
         return;
@@ -450,6 +474,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
             if ((r & 15) == 0)
                 sm.gam[tau] = gam_tau;
+            if (ABL)
+                sm.gq[r] = g;
             epi_sync();
             float G[BT / kChunk + 1];
             G[0] = 0.0f;
@@ -463,7 +489,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float lend = G[BT / kChunk];
             const float lam_r = Gt + g;
             const float rt = valid ? expf(g) : 0.0f;
-            sm.cdiag[r] = valid ? expf(-g) : 0.0f;
+            sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
             sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float wsc = valid ? expf(lend - lam_r) : 0.0f;
@@ -513,6 +539,38 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (!ok)
                 break;
             tc_fence_after();
+            if (ABL) {
+                // explicit position-pair path for the diagonal tile:
+                // P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}, dP_ts = (dO_t . v_s) e^{Gamma_t - Gamma_s}
+#pragma unroll 1
+                for (int i = 0; i < kChunk; ++i) {
+                    const int sc = 16 * tau + i;
+                    float pq = 0.0f, pd = 0.0f;
+                    if (valid && sc <= r) {
+                        for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
+                                const uint4 kb = *reinterpret_cast<const uint4 *>(sm.k + p * kPanel + sw128_offset(sc, c8));
+                                pq = dot_bf16x8(qa, kb, pq);
+                            }
+#pragma unroll
+                        for (int p = 0; p < DV / 64; ++p)
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 oa = *reinterpret_cast<const uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
+                                const uint4 vb = *reinterpret_cast<const uint4 *>(sm.v + p * kPanel + sw128_offset(sc, c8));
+                                pd = dot_bf16x8(oa, vb, pd);
+                            }
+                        const float e = expf(g - sm.gq[sc]);
+                        pq *= e;
+                        pd *= e;
+                    }
+                    sm.dgp[r][i] = pq;
+                    sm.dgd[r][i] = pd;
+                }
+                epi_sync();   // all raw V rows read before any row is rescaled below
+            }
             float rowsum = 0.0f;
             uint32_t dpk[BT / 2];   // dP row r, bf16 pairs
 #pragma unroll
@@ -534,9 +592,14 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         p = sc * w;
                         dp = av * w;
                     } else if (sg == tau && col <= r) {
-                        const float cd = sm.cdiag[col];
-                        p = (sc * cd) * rt;
-                        dp = (av * cd) * rt;
+                        if (ABL) {
+                            p = sm.dgp[r][col & 15];
+                            dp = sm.dgd[r][col & 15];
+                        } else {
+                            const float cd = sm.cdiag[col];
+                            p = (sc * cd) * rt;
+                            dp = (av * cd) * rt;
+                        }
                     } else {
                         p = 0.0f;
                         dp = 0.0f;
@@ -715,30 +778,68 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         tmem_dealloc(tmem, 512);
 }
 
-template <int DV>
+// dq += partial dq of the other dv slices (and dk, da).
+__global__ void add_partials_kernel(float *__restrict__ dq, float *__restrict__ dk,
+                                    float *__restrict__ da, const float *__restrict__ part,
+                                    int64_t n_qk, int64_t n_a, int n_extra)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_qk; i += stride) {
+        float aq = dq[i], ak = dk[i];
+        for (int z = 0; z < n_extra; ++z) {
+            const float *p = part + (size_t)z * (2 * n_qk + n_a);
+            aq += p[i];
+            ak += p[n_qk + i];
+        }
+        dq[i] = aq;
+        dk[i] = ak;
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_a; i += stride) {
+        float acc = da[i];
+        for (int z = 0; z < n_extra; ++z)
+            acc += part[(size_t)z * (2 * n_qk + n_a) + 2 * n_qk + i];
+        da[i] = acc;
+    }
+}
+
+template <int DV, bool ABL>
 cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                const CUtensorMap &mv, const CUtensorMap &mdo, const float *gamma,
                                const float *dfac, const void *states, int st_bf16, int st_stride,
-                               const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0)
+                               const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
+                               float *part)
 {
-    auto kern = bwd_sm100_kernel<DV>;
+    auto kern = bwd_sm100_kernel<DV, ABL>;
     const size_t smem = sizeof(BwdSmem<DV>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
-    dim3 grid(p.H, p.n_docs);
+    const int slices = p.dv / DV;
+    const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
+    dim3 grid(p.H, p.n_docs, slices);
     kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, gamma, dfac, p.cu, p.T, p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
-                                                ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0, p.st);
+                                                ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
+                                                part, n_qk, n_a, p.st);
+    if ((err = cudaGetLastError()) != cudaSuccess || slices == 1)
+        return err;
+    add_partials_kernel<<<1184, 256, 0, p.stream>>>(dq, dk, da, part, n_qk, n_a, slices - 1);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t bwd_partial_floats(const Problem &p)
+{
+    const int slices = p.dv > 128 ? p.dv / 128 : 1;
+    return (size_t)(slices - 1) * (size_t)(2 * p.tokens * p.H * p.dk + p.tokens * p.H);
+}
+
 cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
                              const float *dfac, const void *states, int st_bf16, int st_stride,
-                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0)
+                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
+                             float *part)
 {
     if (p.n_docs <= 0 || p.tokens == 0)
         return cudaSuccess;
@@ -746,13 +847,16 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
     if (!make_token_map(&mq, q, p.dk, p.H, p.tokens) || !make_token_map(&mk, k, p.dk, p.H, p.tokens) ||
         !make_token_map(&mv, v, p.dv, p.H, p.tokens) || !make_token_map(&mdo, dO, p.dv, p.H, p.tokens))
         return cudaErrorInvalidValue;
+    const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
     if (p.dv == 64)
-        return launch_bwd_sm100_t<64>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16, st_stride, dhT,
-                                      dq, dk, dv, da, dh0);
-    if (p.dv == 128)
-        return launch_bwd_sm100_t<128>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16, st_stride, dhT,
-                                       dq, dk, dv, da, dh0);
-    return cudaErrorInvalidValue;
+        return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+                                                  st_stride, dhT, dq, dk, dv, da, dh0, part)
+                   : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+                                                   st_stride, dhT, dq, dk, dv, da, dh0, part);
+    return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+                                               st_stride, dhT, dq, dk, dv, da, dh0, part)
+               : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+                                                st_stride, dhT, dq, dk, dv, da, dh0, part);
 }
 
 }  // namespace bdla

@@ -48,7 +48,8 @@ inline void mark_stop(int kernel, cudaStream_t s)
 // gamma and dfac (d lambda / d a, may be nullptr) are head-major [H][tokens].
 cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *dfac);
 
-// Tile-serial forward.  o may be nullptr (states-only pass that fills ckpt).
+// Tile-serial forward on CUDA cores.  Used with o == nullptr to write fp32
+// checkpoints whose stride is below the 128-token block.
 cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
                             int o_f32, float *hT, float *ckpt, int ckpt_stride);
@@ -60,18 +61,17 @@ cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
                              const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
                              int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride);
 
-// Tensor-core backward for dv <= 128.  `states` holds the state before every
-// 128-token block: checkpoints whose stride divides 128, fp32 or bf16.
+// Tensor-core backward.  `states` holds the state before every 128-token
+// block: checkpoints whose stride divides 128, fp32 or bf16.  For dv = 256
+// the value columns are split in two slices; `part` (bwd_partial_floats
+// floats of workspace) receives the second slice's partial dq, dk, da.
+size_t bwd_partial_floats(const Problem &p);
 cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
                              const float *dfac, const void *states, int st_bf16, int st_stride,
-                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0);
+                             const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
+                             float *part);
 
-// Tile-serial backward; `states` holds the state before every 16-token tile
-// (checkpoint layout with stride 16).
-cudaError_t launch_bwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                            const __nv_bfloat16 *v, const float *a, const float *gamma,
-                            const __nv_bfloat16 *dO, const float *dhT, const float *states,
-                            float *dq, float *dk, float *dv, float *da, float *dh0);
+
 
 }  // namespace bdla
