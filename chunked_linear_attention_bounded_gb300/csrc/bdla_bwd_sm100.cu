@@ -19,7 +19,8 @@
 //   da = dlam * d lambda / d a.
 // S_in (the state before the block) comes from forward checkpoints.
 //
-// Phases of one block (MMA warp <-> four epilogue warps):
+// Phases of one block (MMA warp <-> eight epilogue warps, two per TMEM lane
+// quarter splitting the columns):
 //   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
 //   EA  P (smem) and dP (registers), W sums, V -> V o w_s, E -> bf16 copy,
 //       E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
@@ -43,7 +44,8 @@ namespace {
 using namespace sm100;
 
 constexpr int BT = 128;
-constexpr int kBwdThreads = 192;
+constexpr int kEpiThreads = 256;                 // 8 epilogue warps, two per TMEM lane quarter
+constexpr int kBwdThreads = 64 + kEpiThreads;    // + producer warp and MMA warp
 constexpr uint32_t kPanel = 16384;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -58,9 +60,12 @@ struct BwdSmem {
     float cdiag[BT];
     float coff[BT];
     float colsum[4][BT];
+    float rowpart[2][BT];   // per column half: sum_{s<t} W_ts, k.dk_inter, q.dq_inter
+    float kdpart[2][BT];
+    float ypart[2][BT];
     float scan[2][4];
     float gam[BT / kChunk];
-    float se[4];
+    float se[8];
     float gq[BT];                  // Gamma per row (ablation diagonal path)
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
@@ -70,7 +75,11 @@ struct BwdSmem {
     int abort_flag;
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in shared memory per CTA
+static_assert(sizeof(BwdSmem<128>) <= kMaxSmem && sizeof(BwdSmem<64>) <= kMaxSmem,
+              "backward shared memory exceeds the per-CTA limit");
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ bool epi_all(bool v)
 {
@@ -78,7 +87,7 @@ __device__ __forceinline__ bool epi_all(bool v)
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)v)
@@ -231,15 +240,15 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     if (tid == 0) {
         mbar_init(&sm.full_in, 1);
         mbar_init(&sm.free_in, 1);
-        mbar_init(&sm.z_ready, 128);
+        mbar_init(&sm.z_ready, kEpiThreads);
         mbar_init(&sm.m1_done, 1);
-        mbar_init(&sm.ea_done, 128);
+        mbar_init(&sm.ea_done, kEpiThreads);
         mbar_init(&sm.mb_done, 1);
-        mbar_init(&sm.eb_done, 128);
+        mbar_init(&sm.eb_done, kEpiThreads);
         mbar_init(&sm.md_done, 1);
-        mbar_init(&sm.ee_done, 128);
+        mbar_init(&sm.ee_done, kEpiThreads);
         mbar_init(&sm.mf_done, 1);
-        mbar_init(&sm.acc_free, 128);
+        mbar_init(&sm.acc_free, kEpiThreads);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
@@ -372,13 +381,16 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
     } else {
         // ---------------------------------------------------------------- epilogue
+        // Thread = row r (TMEM lane); `half` takes the 32-column chunks with
+        // c % 2 == half (and half of each 64-wide smem row for the in-place folds).
         const int q4 = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         {   // E <- dhT
             uint32_t x[32];
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     x[i] = __float_as_uint((dhT != nullptr && r < dk)
@@ -390,7 +402,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         // values of the block whose outputs are still pending (written in Eg)
         int pend_j = -1;
-        float pend_row = 0.0f, pend_kd = 0.0f, pend_y = 0.0f, pend_fac = 0.0f, pend_lend = 0.0f;
+        float pend_fac = 0.0f, pend_lend = 0.0f;
 
         auto finish_block = [&]() -> bool {
             // Eg: outputs of block pend_j once Mf has completed
@@ -402,9 +414,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const bool valid = (int64_t)pend_j * BT + r < d.len;
             const size_t ok_off = (size_t)t * H + h;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c * 32 >= dk)
-                    break;
+            for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
                 uint32_t x[32], y[32];
                 tmem_ld32(t_c3 + lane_off + c * 32, x);
                 tmem_ld32(t_c1 + lane_off + c * 32, y);
@@ -422,7 +432,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             }
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
                 tmem_ld32(t_c2 + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -436,19 +446,24 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
-            // decay gradient of the block
+            // decay gradient of the block (both halves compute it; half 0 stores)
             float col = 0.0f;
 #pragma unroll
             for (int w = 0; w < 4; ++w)
                 col += sm.colsum[w][r];
-            const float X = col - pend_row + pend_kd;
+            const float X = col - (sm.rowpart[0][r] + sm.rowpart[1][r]) + (sm.kdpart[0][r] + sm.kdpart[1][r]);
+            const float Yv = sm.ypart[0][r] + sm.ypart[1][r];
             float tx, ty;
             const float px = block_exclusive_scan(X, sm.scan[0], q4, lane, tx);
-            const float py = block_exclusive_scan(pend_y, sm.scan[1], q4, lane, ty);
-            const float C = expf(pend_lend) * (sm.se[0] + sm.se[1] + sm.se[2] + sm.se[3]);
-            if (valid)
+            const float py = block_exclusive_scan(Yv, sm.scan[1], q4, lane, ty);
+            float se = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                se += sm.se[w];
+            const float C = expf(pend_lend) * se;
+            if (valid && half == 0)
                 da[(size_t)t * H + h] = (px + (ty - py) + C) * pend_fac;
-            epi_sync();   // scan scratch and colsum are reused by the next block
+            epi_sync();   // scan scratch and the per-block partials are reused by the next block
             return true;
         };
 
@@ -460,6 +475,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
+            // the decay scalars load overlaps the previous block's output stores
+            const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
+            const float fac = valid ? dfac[(int64_t)h * tokens + t0 + r] : 0.0f;
             if (pend_j >= 0) {
                 ok = finish_block();
                 if (!ok)
@@ -467,15 +485,17 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 pend_j = -1;
             }
             // ---- decay scalars
-            const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
-            const float fac = valid ? dfac[(int64_t)h * tokens + t0 + r] : 0.0f;
             const int last = min(16 * tau + 15, Lb - 1);
             const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
             const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
-            if ((r & 15) == 0)
-                sm.gam[tau] = gam_tau;
-            if (ABL)
-                sm.gq[r] = g;
+            if (half == 0) {
+                if ((r & 15) == 0)
+                    sm.gam[tau] = gam_tau;
+                if (ABL)
+                    sm.gq[r] = g;
+                sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
+                sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
+            }
             epi_sync();
             float G[BT / kChunk + 1];
             G[0] = 0.0f;
@@ -489,20 +509,14 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float lend = G[BT / kChunk];
             const float lam_r = Gt + g;
             const float rt = valid ? expf(g) : 0.0f;
-            sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
-            sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float wsc = valid ? expf(lend - lam_r) : 0.0f;
-            float f[BT / kChunk];
-#pragma unroll
-            for (int sg = 0; sg < BT / kChunk; ++sg)
-                f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
 
             // ---- S_in row r -> bf16 copy (z) and <S_in, E>
             {
                 float se = 0.0f;
 #pragma unroll
-                for (int c = 0; c < DV / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                     float s_in[32];
                     if (r < dk)
                         load_state_row(states, st_bf16, st_stride, n_slots, d, n, h, j, dk, dv, j0, r, s_in, c);
@@ -528,7 +542,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 se = warp_sum(se);
                 if (lane == 0)
-                    sm.se[q4] = se;
+                    sm.se[warp - 2] = se;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -543,7 +557,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 // explicit position-pair path for the diagonal tile:
                 // P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}, dP_ts = (dO_t . v_s) e^{Gamma_t - Gamma_s}
 #pragma unroll 1
-                for (int i = 0; i < kChunk; ++i) {
+                for (int i = 8 * half; i < 8 * half + 8; ++i) {
                     const int sc = 16 * tau + i;
                     float pq = 0.0f, pd = 0.0f;
                     if (valid && sc <= r) {
@@ -572,47 +586,69 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 epi_sync();   // all raw V rows read before any row is rescaled below
             }
             float rowsum = 0.0f;
-            uint32_t dpk[BT / 2];   // dP row r, bf16 pairs
+            uint32_t dpk[BT / 4];   // dP row r on this half's two chunks, bf16 pairs
+            float f[BT / kChunk];
 #pragma unroll
-            for (int c = 0; c < BT / 32; ++c) {
-                uint32_t xs[32], xa[32];
-                tmem_ld32(t_c1 + lane_off + c * 32, xs);
-                tmem_ld32(t_c2 + lane_off + c * 32, xa);
-                tmem_ld_wait();
+            for (int sg = 0; sg < BT / kChunk; ++sg)
+                f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
+                const int cc = c >> 1;   // this half's chunk index 0..1
                 float pv[32], wv[32];
+                uint32_t dpu[32];
+                if (c <= q4) {
+                    uint32_t xs[32], xa[32];
+                    tmem_ld32(t_c1 + lane_off + c * 32, xs);
+                    tmem_ld32(t_c2 + lane_off + c * 32, xa);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = c * 32 + i;
-                    const int sg = col >> 4;
-                    const float sc = __uint_as_float(xs[i]);
-                    const float av = __uint_as_float(xa[i]);
-                    float p, dp;
-                    if (sg < tau) {
-                        const float w = sm.coff[col] * f[sg];
-                        p = sc * w;
-                        dp = av * w;
-                    } else if (sg == tau && col <= r) {
-                        if (ABL) {
-                            p = sm.dgp[r][col & 15];
-                            dp = sm.dgd[r][col & 15];
-                        } else {
-                            const float cd = sm.cdiag[col];
-                            p = (sc * cd) * rt;
-                            dp = (av * cd) * rt;
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 co = *reinterpret_cast<const float4 *>(&sm.coff[c * 32 + 4 * i4]);
+                        const float4 cd = *reinterpret_cast<const float4 *>(&sm.cdiag[c * 32 + 4 * i4]);
+                        const float cov[4] = {co.x, co.y, co.z, co.w};
+                        const float cdv[4] = {cd.x, cd.y, cd.z, cd.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * i4 + e;
+                            const int col = c * 32 + i;
+                            const int sg = col >> 4;
+                            const float sc = __uint_as_float(xs[i]);
+                            const float av = __uint_as_float(xa[i]);
+                            float p, dp;
+                            if (sg < tau) {
+                                const float w = cov[e] * f[sg];
+                                p = sc * w;
+                                dp = av * w;
+                            } else if (sg == tau && col <= r) {
+                                if (ABL) {
+                                    p = sm.dgp[r][col & 15];
+                                    dp = sm.dgd[r][col & 15];
+                                } else {
+                                    p = (sc * cdv[e]) * rt;
+                                    dp = (av * cdv[e]) * rt;
+                                }
+                            } else {
+                                p = 0.0f;
+                                dp = 0.0f;
+                            }
+                            pv[i] = p;
+                            const float wt = (col < r) ? p * av : 0.0f;
+                            wv[i] = wt;
+                            rowsum += wt;
+                            dpu[i] = __float_as_uint(dp);
                         }
-                    } else {
-                        p = 0.0f;
-                        dp = 0.0f;
                     }
-                    pv[i] = p;
-                    const float wt = (col < r) ? p * av : 0.0f;
-                    wv[i] = wt;
-                    rowsum += wt;
-                    xa[i] = __float_as_uint(dp);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        pv[i] = 0.0f;
+                        wv[i] = 0.0f;
+                        dpu[i] = 0u;
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    dpk[c * 16 + i] = pack_bf16(__uint_as_float(xa[2 * i]), __uint_as_float(xa[2 * i + 1]));
+                    dpk[cc * 16 + i] = pack_bf16(__uint_as_float(dpu[2 * i]), __uint_as_float(dpu[2 * i + 1]));
                 uint32_t u[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -625,11 +661,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const float cs = warp_reduce_scatter32(wv, lane);
                 sm.colsum[q4][c * 32 + lane] = cs;
             }
+            sm.rowpart[half][r] = rowsum;
             // V -> V o w_s in place
 #pragma unroll
             for (int p = 0; p < DV / 64; ++p)
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
                     uint4 *va = reinterpret_cast<uint4 *>(sm.v + p * kPanel + sw128_offset(r, c8));
                     *va = scale_bf16x8(*va, wsc);
                 }
@@ -637,7 +674,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             {
                 const float el = expf(lend);
 #pragma unroll
-                for (int c = 0; c < DV / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                     uint32_t e[32];
                     tmem_ld32(t_e + lane_off + c * 32, e);
                     tmem_ld_wait();
@@ -659,9 +696,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // C3 <- e^{Lam_t} C3 (the inter-block part of dq) and Y_t = q_t . dq_inter_t
             float yv = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c * 32 >= dk)
-                    break;
+            for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
                 uint32_t x[32];
                 tmem_ld32(t_c3 + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -682,6 +717,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 tmem_st32(t_c3 + lane_off + c * 32, x);
             }
+            sm.ypart[half][r] = yv;
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -694,9 +730,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_after();
             float kd = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c * 32 >= dk)
-                    break;
+            for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
                 uint32_t x[32];
                 tmem_ld32(t_c1 + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -712,14 +746,16 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                 }
             }
+            sm.kdpart[half][r] = kd;
 #pragma unroll
-            for (int c = 0; c < BT / 32; ++c) {
+            for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
+                const int cc = c >> 1;
                 unsigned char *xp = sm.x + (c >> 1) * kPanel;
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4)
                     *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                        make_uint4(dpk[c * 16 + 4 * k4], dpk[c * 16 + 4 * k4 + 1], dpk[c * 16 + 4 * k4 + 2],
-                                   dpk[c * 16 + 4 * k4 + 3]);
+                        make_uint4(dpk[cc * 16 + 4 * k4], dpk[cc * 16 + 4 * k4 + 1],
+                                   dpk[cc * 16 + 4 * k4 + 2], dpk[cc * 16 + 4 * k4 + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -733,7 +769,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll 1
             for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
                     uint4 *qa = reinterpret_cast<uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
                     uint4 *ka = reinterpret_cast<uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
                     *qa = scale_bf16x8(*qa, qsc);
@@ -744,9 +780,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_arrive(&sm.ee_done);
 
             pend_j = j;
-            pend_row = rowsum;
-            pend_kd = kd;
-            pend_y = yv;
             pend_fac = fac;
             pend_lend = lend;
         }
@@ -754,7 +787,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             ok = finish_block();
         if (ok && dh0 != nullptr && r < dk) {
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
                 tmem_ld32(t_e + lane_off + c * 32, x);
                 tmem_ld_wait();

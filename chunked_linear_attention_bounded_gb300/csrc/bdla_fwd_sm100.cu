@@ -24,9 +24,10 @@
 // and keeps the GEMM result only for the off-diagonal tiles.
 //
 // Warp roles: warp 0 issues TMA loads (Q, K double-buffered, V single),
-// warp 1 allocates TMEM and issues the MMAs, warps 2-5 (one TMEM lane
-// quarter each) turn scores into P, fold the decay into Q and K in place,
-// move the state between TMEM and its bf16 shared copy, and store O.
+// warp 1 allocates TMEM and issues the MMAs, warps 2-9 (two per TMEM lane
+// quarter, splitting the columns) turn scores into P, fold the decay into Q
+// and K in place, move the state between TMEM and its bf16 shared copy, and
+// store O.
 // Every wait is bounded; on expiry the CTA records BDLA_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -41,7 +42,9 @@ namespace {
 using namespace sm100;
 
 constexpr int BT = 128;             // tokens per block
-constexpr int kFwdThreads = 192;    // 6 warps
+constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kFwdThreads = 64 + kEpiThreads;   // producer warp, MMA warp, epilogue
 constexpr uint32_t kPanel = 16384;  // one 128-row x 128-byte swizzled panel
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -62,7 +65,11 @@ struct FwdSmem {
     int abort_flag;
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in shared memory per CTA
+static_assert(sizeof(FwdSmem<128>) <= kMaxSmem && sizeof(FwdSmem<64>) <= kMaxSmem,
+              "forward shared memory exceeds the per-CTA limit");
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ bool epi_all(bool v)
 {
@@ -70,7 +77,7 @@ __device__ __forceinline__ bool epi_all(bool v)
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)v)
@@ -135,11 +142,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_init(&sm.full_qk[s], 1);
             mbar_init(&sm.empty_qk[s], 1);
             mbar_init(&sm.score_full[s], 1);
-            mbar_init(&sm.score_free[s], 128);
+            mbar_init(&sm.score_free[s], kEpiThreads);
         }
         mbar_init(&sm.full_v, 1);
         mbar_init(&sm.empty_v, 1);
-        mbar_init(&sm.p_ready, 128);
+        mbar_init(&sm.p_ready, kEpiThreads);
         mbar_init(&sm.o_full, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -274,13 +281,16 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
     } else {
         // ---------------------------------------------------------------- epilogue
+        // Thread = row r (TMEM lane); the two warps of a lane quarter split the
+        // columns: `half` takes 32-column chunks c with c % 2 == half.
         const int q4 = warp & 3;
-        const int r = 32 * q4 + lane;                 // row = TMEM lane
+        const int half = (warp - 2) >> 2;
+        const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         {   // initial state
             uint32_t x[32];
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float val = (h0 != nullptr && r < dk)
@@ -297,7 +307,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int64_t t = d.start + (int64_t)jb * BT + r;
             const bool valid = (int64_t)jb * BT + r < d.len;
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
                 tmem_ld32(t_o + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -323,21 +333,31 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         };
 
         bool ok = true;
+        // Gamma of the first block; later blocks are fetched one block ahead
+        float g_next = (nblk > 0 && r < d.len) ? gamma[(int64_t)h * tokens + d.start + r] : 0.0f;
         for (int j = 0; j < nblk; ++j) {
             const int s = j & 1;
-            const int64_t t0 = d.start + (int64_t)j * BT;
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
             // ---- decay scalars of this block
-            const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
+            const float g = g_next;
+            if (j + 1 < nblk) {
+                const int64_t tn = (int64_t)(j + 1) * BT + r;
+                g_next = tn < d.len ? gamma[(int64_t)h * tokens + d.start + tn] : 0.0f;
+            }
             const int last = min(16 * tau + 15, Lb - 1);
             const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
             const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
-            if ((r & 15) == 0)
+            epi_sync();   // both halves are done with the previous block's column factors
+            if (half == 0 && (r & 15) == 0)
                 sm.gam[tau] = gam_tau;
-            if (ABL)
-                sm.gq[r] = g;
+            if (half == 0) {
+                if (ABL)
+                    sm.gq[r] = g;
+                sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
+                sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
+            }
             epi_sync();
             float G[BT / kChunk + 1];
             G[0] = 0.0f;
@@ -351,15 +371,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float lend = G[BT / kChunk];
             const float lam_r = Gt + g;
             const float rt = valid ? expf(g) : 0.0f;
-            sm.cdiag[r] = (valid && !ABL) ? expf(-g) : 0.0f;
-            sm.coff[r] = valid ? expf(gam_tau - g) : 0.0f;
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float ksc = valid ? expf(lend - lam_r) : 0.0f;
-            float f[BT / kChunk];   // per source tile: e^{G_tau - G_sig+1} e^{Gamma_t}
-#pragma unroll
-            for (int sg = 0; sg < BT / kChunk; ++sg)
-                f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
-            epi_sync();
 
             if (STATES)
                 ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
@@ -369,33 +382,38 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 break;
             tc_fence_after();
 
-            float diag[kChunk];
-            if (ABL) {   // explicit position-pair path for the diagonal tile
-                const unsigned char *qrow = sm.q[s];
-                const unsigned char *kb = sm.k[s];
-#pragma unroll
-                for (int i = 0; i < kChunk; ++i) {
-                    const int sc = 16 * tau + i;
+            if (ABL) {
+                // explicit position-pair path for the diagonal tile: each half
+                // computes 8 of the row's 16 pairs and writes them, as one
+                // 16-byte chunk, straight into P
+                float pr[8];
+#pragma unroll 1
+                for (int i = 0; i < 8; ++i) {
+                    const int sc = 16 * tau + 8 * half + i;
                     float acc = 0.0f;
                     if (valid && sc <= r) {
                         for (int p = 0; p < kpan; ++p)
 #pragma unroll
                             for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + p * kPanel + sw128_offset(r, c8));
-                                const uint4 kk = *reinterpret_cast<const uint4 *>(kb + p * kPanel + sw128_offset(sc, c8));
+                                const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
+                                const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k[s] + p * kPanel + sw128_offset(sc, c8));
                                 acc = dot_bf16x8(qa, kk, acc);
                             }
                         acc *= expf(g - sm.gq[sc]);
                     }
-                    diag[i] = acc;
+                    pr[i] = acc;
                 }
+                const int cidx = 2 * tau + half;   // 16-byte chunk of the row (of 16)
+                *reinterpret_cast<uint4 *>(sm.p + (cidx >> 3) * kPanel + sw128_offset(r, cidx & 7)) =
+                    make_uint4(pack_bf16(pr[0], pr[1]), pack_bf16(pr[2], pr[3]), pack_bf16(pr[4], pr[5]),
+                               pack_bf16(pr[6], pr[7]));
                 epi_sync();   // every thread is done with the raw K rows
             }
-            // ---- fold the decay into Q and K in place (row r)
+            // ---- fold the decay into Q and K in place (row r, half the chunks)
 #pragma unroll 1
             for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
                     uint4 *ka = reinterpret_cast<uint4 *>(sm.k[s] + p * kPanel + sw128_offset(r, c8));
                     *ka = scale_bf16x8(*ka, ksc);
                     if (!STATES) {
@@ -404,39 +422,61 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                 }
             // ---- P = decay-weighted causal scores (bf16, K-major rows t)
+            if (!STATES) {
+                float f[BT / kChunk];   // per source tile: e^{G_tau - G_sig+1} e^{Gamma_t}
 #pragma unroll
-            for (int c = 0; c < (STATES ? 0 : BT / 32); ++c) {
-                uint32_t x[32];
-                tmem_ld32(t_score0 + 128 * s + lane_off + c * 32, x);
-                tmem_ld_wait();
-                float pv[32];
+                for (int sg = 0; sg < BT / kChunk; ++sg)
+                    f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = c * 32 + i;
-                    const int sg = col >> 4;
-                    const float sc = __uint_as_float(x[i]);
-                    float val;
-                    if (sg < tau)
-                        val = sc * sm.coff[col] * f[sg];
-                    else if (sg == tau)
-                        val = (col <= r) ? (ABL ? diag[col & 15] : (sc * sm.cdiag[col]) * rt) : 0.0f;
-                    else
-                        val = 0.0f;
-                    pv[i] = val;
+                for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
+                    uint32_t u[16];
+                    if (c <= q4) {   // chunks above the warp's rows are causally zero
+                        uint32_t x[32];
+                        tmem_ld32(t_score0 + 128 * s + lane_off + c * 32, x);
+                        tmem_ld_wait();
+                        float pv[32];
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 co = *reinterpret_cast<const float4 *>(&sm.coff[c * 32 + 4 * i4]);
+                            const float4 cd = *reinterpret_cast<const float4 *>(&sm.cdiag[c * 32 + 4 * i4]);
+                            const float cov[4] = {co.x, co.y, co.z, co.w};
+                            const float cdv[4] = {cd.x, cd.y, cd.z, cd.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 4 * i4 + e;
+                                const int col = c * 32 + i;
+                                const int sg = col >> 4;
+                                const float sc = __uint_as_float(x[i]);
+                                float val;
+                                if (sg < tau)
+                                    val = sc * cov[e] * f[sg];
+                                else if (sg == tau)
+                                    val = (!ABL && col <= r) ? (sc * cdv[e]) * rt : 0.0f;
+                                else
+                                    val = 0.0f;
+                                pv[i] = val;
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            u[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            u[i] = 0u;
+                    }
+                    unsigned char *pp = sm.p + (c >> 1) * kPanel;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        if (ABL && 2 * c + (k4 >> 1) == tau)
+                            continue;   // the diagonal tile was written by the pair path
+                        *reinterpret_cast<uint4 *>(pp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                    }
                 }
-                uint32_t u[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    u[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
-                unsigned char *pp = sm.p + (c >> 1) * kPanel;
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                    *reinterpret_cast<uint4 *>(pp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                        make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
-            }
-            tc_fence_before();
-            if (!STATES)
+                tc_fence_before();
                 mbar_arrive(&sm.score_free[s]);
+            }
 
             // ---- output of the previous block
             if (j > 0) {
@@ -457,7 +497,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                                sstride + (size_t)r * dv + j0
                                          : 0;
 #pragma unroll
-                for (int c = 0; c < DV / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                     uint32_t x[32];
                     tmem_ld32(t_s + lane_off + c * 32, x);
                     tmem_ld_wait();
@@ -504,7 +544,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         if (ok && hT != nullptr && r < dk) {
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
                 tmem_ld32(t_s + lane_off + c * 32, x);
                 tmem_ld_wait();
@@ -514,8 +554,6 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     reinterpret_cast<uint4 *>(row)[k4] =
                         make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
             }
-        } else if (ok && hT != nullptr) {
-            // rows >= dk hold no state
         }
         if (!ok) {
             *abort_flag = 1;
