@@ -76,18 +76,24 @@ def run_oracle(inp, b, mode, heads=None, dhT=None, with_grad=True):
 
 def run_gpu(g, b, mode, with_grad=True, o_dtype=torch.bfloat16, dhT=None, ckpt_stride=0,
             bwd_ckpt=False):
+    """Forward (and backward) through the C ABI; fails if a kernel recorded a
+    device-side error (e.g. a bounded wait that expired)."""
+    ws_f = bdla.Workspace(256, g["q"].device)
+    ws_b = bdla.Workspace(256, g["q"].device)
     o, hT, ckpt = bdla.fwd(g["q"], g["k"], g["v"], g["a"], b, h0=g.get("h0"),
                            cu_seqlens=g.get("cu_seqlens"), mode=mode, o_dtype=o_dtype,
-                           ckpt_stride=ckpt_stride)
+                           ckpt_stride=ckpt_stride, ws=ws_f)
     out = dict(o=o, hT=hT, ckpt=ckpt)
     if with_grad:
         dq, dk, dv, da, dh0 = bdla.bwd(g["q"], g["k"], g["v"], g["a"], g["dO"], b, h0=g.get("h0"),
                                        dhT=dhT, cu_seqlens=g.get("cu_seqlens"),
                                        ckpt=ckpt if bwd_ckpt else None,
                                        ckpt_stride=ckpt_stride if bwd_ckpt else 0, mode=mode,
-                                       want_dh0=True)
+                                       want_dh0=True, ws=ws_b)
         out.update(dq=dq, dk=dk, dv=dv, da=da, dh0=dh0)
     torch.cuda.synchronize()
+    assert ws_f.read_status() == 0, "forward recorded a device-side error"
+    assert ws_b.read_status() == 0, "backward recorded a device-side error"
     return out
 
 

@@ -130,11 +130,14 @@ def test_bf16_block_checkpoints_feed_the_backward(dv):
     w = _small("varlen64k", 900, H=2, n_docs=3, dv=dv)
     inp = make_inputs(w, with_grad=True)
     g = to_device(inp)
+    ws = bdla.Workspace(256, "cuda")
     o, hT, ck = bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
-                         ckpt_stride=128, ckpt_dtype=torch.bfloat16)
+                         ckpt_stride=128, ckpt_dtype=torch.bfloat16, ws=ws)
     dq, dk, dv_, da, dh0 = bdla.bwd(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"],
-                                    cu_seqlens=g["cu_seqlens"], ckpt=ck, ckpt_stride=128, want_dh0=True)
+                                    cu_seqlens=g["cu_seqlens"], ckpt=ck, ckpt_stride=128, want_dh0=True,
+                                    ws=ws)
     torch.cuda.synchronize()
+    assert ws.read_status() == 0
     gpu = dict(o=o, hT=hT, dq=dq, dk=dk, dv=dv_, da=da, dh0=dh0)
     compare_all(gpu, run_oracle(inp, w.b, w.mode))
 
