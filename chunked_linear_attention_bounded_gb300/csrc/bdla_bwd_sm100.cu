@@ -614,22 +614,15 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                             const int sg = col >> 4;
                             const float sc = __uint_as_float(xs[i]);
                             const float av = __uint_as_float(xa[i]);
-                            float p, dp;
-                            if (sg < tau) {
-                                const float w = cov[e] * f[sg];
-                                p = sc * w;
-                                dp = av * w;
-                            } else if (sg == tau && col <= r) {
-                                if (ABL) {
-                                    p = sm.dgp[r][col & 15];
-                                    dp = sm.dgd[r][col & 15];
-                                } else {
-                                    p = (sc * cdv[e]) * rt;
-                                    dp = (av * cdv[e]) * rt;
-                                }
-                            } else {
-                                p = 0.0f;
-                                dp = 0.0f;
+                            // branch-free: rows of one warp sit in two different tiles
+                            const bool diag = (sg == tau);
+                            const bool live = (sg < tau) || (diag && col <= r);
+                            const float w = diag ? cdv[e] * rt : cov[e] * f[sg];
+                            float p = live ? sc * w : 0.0f;
+                            float dp = live ? av * w : 0.0f;
+                            if (ABL && diag) {
+                                p = (col <= r) ? sm.dgp[r][col & 15] : 0.0f;
+                                dp = (col <= r) ? sm.dgd[r][col & 15] : 0.0f;
                             }
                             pv[i] = p;
                             const float wt = (col < r) ? p * av : 0.0f;

@@ -448,13 +448,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                 const int sg = col >> 4;
                                 const float sc = __uint_as_float(x[i]);
                                 float val;
-                                if (sg < tau)
-                                    val = sc * cov[e] * f[sg];
-                                else if (sg == tau)
-                                    val = (!ABL && col <= r) ? (sc * cdv[e]) * rt : 0.0f;
-                                else
-                                    val = 0.0f;
-                                pv[i] = val;
+                                // branch-free: rows of one warp sit in two different tiles
+                                const bool diag = (sg == tau);
+                                const bool live = (sg < tau) || (!ABL && diag && col <= r);
+                                const float w = diag ? cdv[e] * rt : cov[e] * f[sg];
+                                pv[i] = live ? sc * w : 0.0f;
                             }
                         }
 #pragma unroll
