@@ -38,6 +38,7 @@
 namespace bdla {
 
 bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tokens);
+bool make_state_map(CUtensorMap *map, const void *ptr, int dk, int dv, int64_t n_mats);
 
 namespace {
 
@@ -162,6 +163,29 @@ __device__ __forceinline__ float block_exclusive_scan(float x, float *warp_tot, 
     return before + incl - x;
 }
 
+// Coalesced store of a warp's 32 rows x 32 fp32 values (lane = row):
+// transposed through a 4 KB shared staging tile (16-byte chunks XOR-swizzled
+// by row, conflict-free) so that each group of 8 lanes writes one row's 128
+// contiguous bytes.  Rows >= n_valid are not written.
+__device__ __forceinline__ void warp_store_rows_f32(unsigned char *stage, const uint32_t (&x)[32],
+                                                    float *gbase, size_t row_stride, int n_valid,
+                                                    int lane)
+{
+    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4)
+        st4[lane * 8 + (k4 ^ (lane & 7))] = make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int row = 4 * it + (lane >> 3), c4 = lane & 7;
+        const uint4 v = st4[row * 8 + (c4 ^ (row & 7))];
+        if (row < n_valid)
+            *reinterpret_cast<uint4 *>(gbase + (size_t)row * row_stride + 4 * c4) = v;
+    }
+    __syncwarp();
+}
+
 // Row r (of dk rows) of the state before block j from the checkpoint array.
 __device__ __forceinline__ void load_state_row(const void *states, int st_bf16, int stride,
                                                int64_t n_slots, const DocSpan &d, int n, int h, int j,
@@ -204,6 +228,7 @@ template <int DV, bool ABL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                 const __grid_constant__ CUtensorMap tst, int st_tma,
                  const float *__restrict__ gamma, const float *__restrict__ dfac,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
@@ -274,7 +299,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tdo);
-            const uint32_t bytes = (uint32_t)kpan * 2u * kPanel + 2u * (uint32_t)(DV / 64) * kPanel;
+            const uint32_t bytes = (uint32_t)kpan * 2u * kPanel + (st_tma ? 3u : 2u) * (uint32_t)(DV / 64) * kPanel;
+            if (st_tma)
+                tma_prefetch_desc(&tst);
             int last = -1;
             bool ok = true;
             for (int jj = 0; jj < nblk; ++jj) {
@@ -296,6 +323,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int p = 0; p < DV / 64; ++p) {
                     tma_load_3d(sm.v + p * kPanel, &tv, &sm.full_in, j0 + p * 64, h, t0);
                     tma_load_3d(sm.dO + p * kPanel, &tdo, &sm.full_in, j0 + p * 64, h, t0);
+                }
+                if (st_tma) {   // bf16 state before the block, straight into the z tile
+                    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / st_stride, st_stride);
+                    for (int p = 0; p < DV / 64; ++p)
+                        tma_load_3d(sm.z + p * kPanel, &tst, &sm.full_in, j0 + p * 64, 0,
+                                    (int)((int64_t)h * n_slots + slot));
                 }
                 last = jj;
             }
@@ -412,37 +445,25 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_after();
             const int64_t t = d.start + (int64_t)pend_j * BT + r;
             const bool valid = (int64_t)pend_j * BT + r < d.len;
-            const size_t ok_off = (size_t)t * H + h;
+            // the warp's 32 rows start at token t_w; rows past the document end are skipped
+            const int64_t t_w = d.start + (int64_t)pend_j * BT + 32 * q4;
+            const int n_valid = (int)(d.len - ((int64_t)pend_j * BT + 32 * q4));
+            unsigned char *stage = sm.x + (warp - 2) * 4096;   // x is free until the next EA
 #pragma unroll
             for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
                 uint32_t x[32], y[32];
                 tmem_ld32(t_c3 + lane_off + c * 32, x);
                 tmem_ld32(t_c1 + lane_off + c * 32, y);
                 tmem_ld_wait();
-                if (valid) {
-                    float4 *pq = reinterpret_cast<float4 *>(dq + ok_off * dk + c * 32);
-                    float4 *pk = reinterpret_cast<float4 *>(dkk + ok_off * dk + c * 32);
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        pq[k4] = make_float4(__uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
-                                             __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
-                        pk[k4] = make_float4(__uint_as_float(y[4 * k4]), __uint_as_float(y[4 * k4 + 1]),
-                                             __uint_as_float(y[4 * k4 + 2]), __uint_as_float(y[4 * k4 + 3]));
-                    }
-                }
+                warp_store_rows_f32(stage, x, dq + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
+                warp_store_rows_f32(stage, y, dkk + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
             }
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
                 tmem_ld32(t_c2 + lane_off + c * 32, x);
                 tmem_ld_wait();
-                if (valid) {
-                    float4 *pv = reinterpret_cast<float4 *>(dvv + ok_off * dv + j0 + c * 32);
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4)
-                        pv[k4] = make_float4(__uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
-                                             __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
-                }
+                warp_store_rows_f32(stage, x, dvv + ((size_t)t_w * H + h) * dv + j0 + c * 32, (size_t)H * dv, n_valid, lane);
             }
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
@@ -513,10 +534,33 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float wsc = valid ? expf(lend - lam_r) : 0.0f;
 
             // ---- S_in row r -> bf16 copy (z) and <S_in, E>
+            if (st_tma) {
+                // the producer loaded S_in (bf16) into z with the block's inputs
+                ok = epi_all(mbar_wait(&sm.full_in, par, kWaitNs)) && !*abort_flag;
+                if (!ok)
+                    break;
+            }
             {
                 float se = 0.0f;
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                    uint32_t e[32];
+                    tmem_ld32(t_e + lane_off + c * 32, e);
+                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
+                    if (st_tma) {
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint4 zz = *reinterpret_cast<const uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4));
+                            const uint32_t w4[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                se = fmaf(bf16_lo(w4[i]), __uint_as_float(e[8 * k4 + 2 * i]), se);
+                                se = fmaf(bf16_hi(w4[i]), __uint_as_float(e[8 * k4 + 2 * i + 1]), se);
+                            }
+                        }
+                        continue;
+                    }
                     float s_in[32];
                     if (r < dk)
                         load_state_row(states, st_bf16, st_stride, n_slots, d, n, h, j, dk, dv, j0, r, s_in, c);
@@ -524,8 +568,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             s_in[i] = 0.0f;
-                    uint32_t e[32];
-                    tmem_ld32(t_e + lane_off + c * 32, e);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -534,7 +576,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         u[i] = pack_bf16(s_in[2 * i], s_in[2 * i + 1]);
-                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4)
                         *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
@@ -830,7 +871,8 @@ __global__ void add_partials_kernel(float *__restrict__ dq, float *__restrict__ 
 
 template <int DV, bool ABL>
 cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                               const CUtensorMap &mv, const CUtensorMap &mdo, const float *gamma,
+                               const CUtensorMap &mv, const CUtensorMap &mdo, const CUtensorMap &mst,
+                               int st_tma, const float *gamma,
                                const float *dfac, const void *states, int st_bf16, int st_stride,
                                const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
                                float *part)
@@ -843,7 +885,8 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
     const int slices = p.dv / DV;
     const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
     dim3 grid(p.H, p.n_docs, slices);
-    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, gamma, dfac, p.cu, p.T, p.tokens, p.H,
+    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, gamma, dfac, p.cu, p.T,
+                                                p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
                                                 ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
                                                 part, n_qk, n_a, p.st);
@@ -873,15 +916,24 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
     if (!make_token_map(&mq, q, p.dk, p.H, p.tokens) || !make_token_map(&mk, k, p.dk, p.H, p.tokens) ||
         !make_token_map(&mv, v, p.dv, p.H, p.tokens) || !make_token_map(&mdo, dO, p.dv, p.H, p.tokens))
         return cudaErrorInvalidValue;
+    // bf16 states go straight into shared memory by TMA; fp32 ones are
+    // converted by the epilogue
+    CUtensorMap mst = mq;
+    int st_tma = 0;
+    if (st_bf16) {
+        if (!make_state_map(&mst, states, p.dk, p.dv, (int64_t)p.H * ckpt_slots(p, st_stride)))
+            return cudaErrorInvalidValue;
+        st_tma = 1;
+    }
     const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
     if (p.dv == 64)
-        return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+        return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
                                                   st_stride, dhT, dq, dk, dv, da, dh0, part)
-                   : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+                   : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
                                                    st_stride, dhT, dq, dk, dv, da, dh0, part);
-    return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+    return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
                                                st_stride, dhT, dq, dk, dv, da, dh0, part)
-               : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, gamma, dfac, states, st_bf16,
+               : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
                                                 st_stride, dhT, dq, dk, dv, da, dh0, part);
 }
 

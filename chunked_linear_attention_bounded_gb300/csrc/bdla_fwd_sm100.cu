@@ -605,6 +605,23 @@ bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tok
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over bf16 state matrices [n_mats][dk][dv] (checkpoints): box = 64
+// value columns x 128 key rows x 1 matrix, 128-byte swizzle (rows past dk
+// read as zero), so a state lands in shared memory as a GEMM operand tile.
+bool make_state_map(CUtensorMap *map, const void *ptr, int dk, int dv, int64_t n_mats)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr || ptr == nullptr || n_mats <= 0)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)dv, (cuuint64_t)dk, (cuuint64_t)n_mats};
+    cuuint64_t strides[2] = {(cuuint64_t)dv * 2, (cuuint64_t)dk * dv * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)BT, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DV, bool ABL, bool STATES>
 static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                       const CUtensorMap &mv, const float *gamma, const float *h0,
