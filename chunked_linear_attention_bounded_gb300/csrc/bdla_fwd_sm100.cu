@@ -110,7 +110,8 @@ __device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b, float acc)
 template <int DV, bool ABL, bool STATES>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                 const __grid_constant__ CUtensorMap tv, const float *__restrict__ gamma,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tck,
+                 int ck_tma, const float *__restrict__ gamma,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                  float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
@@ -303,32 +304,61 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tmem_st_wait();
         }
 
+        // Output rows of block jb.  bf16: each half takes 64-column pairs; a
+        // warp stages its 32 rows x 128 bytes in sb (free between the Q S GEMM
+        // of block jb and the state copy of block jb+1) and 8 lanes write each
+        // row's contiguous 128 bytes.  fp32 (parity workload): per-row stores.
         auto store_o = [&](int jb) {
             const int64_t t = d.start + (int64_t)jb * BT + r;
             const bool valid = (int64_t)jb * BT + r < d.len;
+            if (o_f32) {
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
-                uint32_t x[32];
-                tmem_ld32(t_o + lane_off + c * 32, x);
-                tmem_ld_wait();
-                if (!valid)
-                    continue;
-                const size_t off = ((size_t)t * H + h) * dv + j0 + c * 32;
-                if (o_f32) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(o) + off);
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                    uint32_t x[32];
+                    tmem_ld32(t_o + lane_off + c * 32, x);
+                    tmem_ld_wait();
+                    if (!valid)
+                        continue;
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(o) +
+                                                           ((size_t)t * H + h) * dv + j0 + c * 32);
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4)
                         dst[k4] = make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
-                } else {
-                    uint32_t u[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(o) + off);
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4)
-                        dst[k4] = make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
                 }
+                return;
+            }
+            const int64_t t_w = d.start + (int64_t)jb * BT + 32 * q4;
+            const int n_valid = (int)(d.len - ((int64_t)jb * BT + 32 * q4));
+            uint4 *st4 = reinterpret_cast<uint4 *>(sm.sb + (q4 + 4 * half) * 4096);
+#pragma unroll
+            for (int c2 = 0; c2 < DV / 64; ++c2) if ((c2 & 1) == half) {
+                uint32_t xa[32], xb[32];
+                tmem_ld32(t_o + lane_off + (2 * c2) * 32, xa);
+                tmem_ld32(t_o + lane_off + (2 * c2 + 1) * 32, xb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    st4[lane * 8 + (k4 ^ (lane & 7))] =
+                        make_uint4(pack_bf16(__uint_as_float(xa[8 * k4]), __uint_as_float(xa[8 * k4 + 1])),
+                                   pack_bf16(__uint_as_float(xa[8 * k4 + 2]), __uint_as_float(xa[8 * k4 + 3])),
+                                   pack_bf16(__uint_as_float(xa[8 * k4 + 4]), __uint_as_float(xa[8 * k4 + 5])),
+                                   pack_bf16(__uint_as_float(xa[8 * k4 + 6]), __uint_as_float(xa[8 * k4 + 7])));
+                    st4[lane * 8 + ((4 + k4) ^ (lane & 7))] =
+                        make_uint4(pack_bf16(__uint_as_float(xb[8 * k4]), __uint_as_float(xb[8 * k4 + 1])),
+                                   pack_bf16(__uint_as_float(xb[8 * k4 + 2]), __uint_as_float(xb[8 * k4 + 3])),
+                                   pack_bf16(__uint_as_float(xb[8 * k4 + 4]), __uint_as_float(xb[8 * k4 + 5])),
+                                   pack_bf16(__uint_as_float(xb[8 * k4 + 6]), __uint_as_float(xb[8 * k4 + 7])));
+                }
+                __syncwarp();
+                __nv_bfloat16 *gbase = reinterpret_cast<__nv_bfloat16 *>(o) + ((size_t)t_w * H + h) * dv + j0 + c2 * 64;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = 4 * it + (lane >> 3), c8 = lane & 7;
+                    const uint4 v = st4[row * 8 + (c8 ^ (row & 7))];
+                    if (row < n_valid)
+                        *reinterpret_cast<uint4 *>(gbase + (size_t)row * H * dv + 8 * c8) = v;
+                }
+                __syncwarp();
             }
         };
 
@@ -478,18 +508,23 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
             // ---- output of the previous block
             if (j > 0) {
+                if (ck_tma && warp == 2 && lane == 0)
+                    tma_store_wait_read();   // previous checkpoint store is done with sb
                 ok = epi_all(mbar_wait(&sm.o_full, (j - 1) & 1, kWaitNs)) && !*abort_flag;
                 if (!ok)
                     break;
                 tc_fence_after();
-                if (!STATES)
+                if (!STATES) {
                     store_o(j - 1);
+                    epi_sync();   // every warp's staging in sb is done before the state copy
+                }
             }
             // ---- state: checkpoint, bf16 copy for the Q S GEMM, decay for the K V update
             {
                 const float el = expf(lend);
-                const bool wck = ckpt != nullptr && r < dk && ckpt_stride % BT == 0 &&
-                                 ((int64_t)j * BT) % ckpt_stride == 0;
+                const bool ck_block = ckpt != nullptr && ckpt_stride % BT == 0 &&
+                                      ((int64_t)j * BT) % ckpt_stride == 0;
+                const bool wck = ck_block && !ck_tma && r < dk;   // fp32 checkpoints: per-row stores
                 const size_t ckoff = wck ? ((size_t)h * n_slots +
                                             ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride)) *
                                                sstride + (size_t)r * dv + j0
@@ -514,7 +549,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         for (int k4 = 0; k4 < 4; ++k4)
                             dst[k4] = make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
                     }
-                    if (!STATES) {
+                    if (!STATES || (ck_block && ck_tma)) {
                         unsigned char *sp = sm.sb + (c >> 1) * kPanel;
 #pragma unroll
                         for (int k4 = 0; k4 < 4; ++k4)
@@ -527,11 +562,24 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tmem_st32(t_s + lane_off + c * 32, x);
                 }
                 tmem_st_wait();
+                if (ck_block && ck_tma) {
+                    // bf16 checkpoint: one TMA store of the swizzled state tile
+                    fence_proxy_async_smem();
+                    epi_sync();
+                    if (warp == 2 && lane == 0) {
+                        const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride);
+                        for (int p = 0; p < DV / 64; ++p)
+                            tma_store_3d(&tck, sm.sb + p * kPanel, j0 + p * 64, 0, (int)((int64_t)h * n_slots + slot));
+                        tma_store_commit();
+                    }
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.p_ready);
         }
+        if (ck_tma && warp == 2 && lane == 0)
+            tma_store_wait_read();
         if (ok && nblk > 0) {
             ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, kWaitNs)) && !*abort_flag;
             if (ok) {
@@ -624,7 +672,8 @@ bool make_state_map(CUtensorMap *map, const void *ptr, int dk, int dv, int64_t n
 
 template <int DV, bool ABL, bool STATES>
 static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                      const CUtensorMap &mv, const float *gamma, const float *h0,
+                                      const CUtensorMap &mv, const CUtensorMap &mck, int ck_tma,
+                                      const float *gamma, const float *h0,
                                       void *o, int o_f32, float *hT, void *ckpt, int ck_bf16,
                                       int ckpt_stride)
 {
@@ -635,7 +684,7 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
         return err;
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
     dim3 grid(p.dv / DV, p.H, p.n_docs);
-    kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
+    kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
                                                 p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
                                                 n_slots, p.st);
     return cudaGetLastError();
@@ -663,9 +712,17 @@ cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
     if (states_only)
         mq = mk;
     const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
+    // bf16 checkpoints at block starts leave by TMA store from the state tile
+    CUtensorMap mck = mk;
+    int ck_tma = 0;
+    if (ckpt != nullptr && ck_bf16 && ckpt_stride % BT == 0) {
+        if (!make_state_map(&mck, ckpt, p.dk, p.dv, (int64_t)p.H * ckpt_slots(p, ckpt_stride)))
+            return cudaErrorInvalidValue;
+        ck_tma = 1;
+    }
 #define BDLA_FWD_GO(DV_, ABL_, ST_)                                                                 \
-    return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, gamma, h0, o, o_f32, hT, ckpt, ck_bf16, \
-                                              ckpt_stride)
+    return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, mck, ck_tma, gamma, h0, o, o_f32, hT,  \
+                                              ckpt, ck_bf16, ckpt_stride)
     if (states_only) {
         if (p.dv == 64)
             BDLA_FWD_GO(64, false, true);
