@@ -41,6 +41,33 @@ bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tok
 bool make_state_map(CUtensorMap *map, const void *ptr, int dk, int dv, int64_t n_mats);
 
 namespace {
+// 3-D map over a token-major fp32 gradient [tokens][H][d] for TMA stores:
+// box = 32 features (128 bytes) x 1 head x 128 tokens, 128-byte swizzle.
+bool make_grad_map(CUtensorMap *map, void *ptr, int d, int H, int64_t tokens)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    if (ptr == nullptr || tokens <= 0)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+namespace {
 
 using namespace sm100;
 
@@ -56,6 +83,7 @@ struct BwdSmem {
     alignas(1024) unsigned char k[2 * kPanel];
     alignas(1024) unsigned char v[(DV / 64) * kPanel];
     alignas(1024) unsigned char dO[(DV / 64) * kPanel];
+    // z and x are adjacent: together they stage fp32 output panels for TMA stores
     alignas(1024) unsigned char z[(DV / 64) * kPanel];   // S_in, then E: rows dk, panels dv
     alignas(1024) unsigned char x[2 * kPanel];           // P, then dP: rows t, panels s
     float cdiag[BT];
@@ -71,7 +99,7 @@ struct BwdSmem {
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
     uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
-        mf_done, acc_free, drain;
+        mf_done, acc_free, drain, full_z, z_free;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -229,6 +257,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const __grid_constant__ CUtensorMap tst, int st_tma,
+                 const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+                 const __grid_constant__ CUtensorMap tdv, int out_tma,
                  const float *__restrict__ gamma, const float *__restrict__ dfac,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
@@ -275,6 +305,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.mf_done, 1);
         mbar_init(&sm.acc_free, kEpiThreads);
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.full_z, 1);
+        mbar_init(&sm.z_free, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
     }
@@ -299,7 +331,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tdo);
-            const uint32_t bytes = (uint32_t)kpan * 2u * kPanel + (st_tma ? 3u : 2u) * (uint32_t)(DV / 64) * kPanel;
+            const uint32_t bytes = (uint32_t)kpan * 2u * kPanel + 2u * (uint32_t)(DV / 64) * kPanel;
+            const uint32_t zbytes = (uint32_t)(DV / 64) * kPanel;
+            int last_z = -1;
             if (st_tma)
                 tma_prefetch_desc(&tst);
             int last = -1;
@@ -324,19 +358,29 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tma_load_3d(sm.v + p * kPanel, &tv, &sm.full_in, j0 + p * 64, h, t0);
                     tma_load_3d(sm.dO + p * kPanel, &tdo, &sm.full_in, j0 + p * 64, h, t0);
                 }
-                if (st_tma) {   // bf16 state before the block, straight into the z tile
-                    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / st_stride, st_stride);
-                    for (int p = 0; p < DV / 64; ++p)
-                        tma_load_3d(sm.z + p * kPanel, &tst, &sm.full_in, j0 + p * 64, 0,
-                                    (int)((int64_t)h * n_slots + slot));
-                }
                 last = jj;
+                if (st_tma) {
+                    // bf16 state before the block, straight into the z tile, once the
+                    // previous block's output staging has left z
+                    if (jj > 0 && !mbar_wait(&sm.z_free, (jj - 1) & 1, kWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / st_stride, st_stride);
+                    mbar_arrive_expect_tx(&sm.full_z, zbytes);
+                    for (int p = 0; p < DV / 64; ++p)
+                        tma_load_3d(sm.z + p * kPanel, &tst, &sm.full_z, j0 + p * 64, 0,
+                                    (int)((int64_t)h * n_slots + slot));
+                    last_z = jj;
+                }
             }
             if (!ok) {
                 *abort_flag = 1;
                 set_status(st, BDLA_ERR_TIMEOUT, 11u);
                 if (last >= 0)
                     mbar_wait(&sm.full_in, last & 1, kWaitNs);
+                if (last_z >= 0)
+                    mbar_wait(&sm.full_z, last_z & 1, kWaitNs);
             }
         }
     } else if (warp == 1) {
@@ -448,23 +492,69 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // the warp's 32 rows start at token t_w; rows past the document end are skipped
             const int64_t t_w = d.start + (int64_t)pend_j * BT + 32 * q4;
             const int n_valid = (int)(d.len - ((int64_t)pend_j * BT + 32 * q4));
-            unsigned char *stage = sm.x + (warp - 2) * 4096;   // x is free until the next EA
+            const bool full_blk = d.len - (int64_t)pend_j * BT >= BT;
+            if (out_tma && full_blk && blockIdx.z == 0) {
+                // fp32 panels (32 columns) staged in z + x and written by TMA stores:
+                // item i < dk/32: dq panel i; next dk/32: dk panels; then dv panels
+                constexpr int kStagePanels = DV / 64 + 2;
+                const int n_items = 2 * (dk / 32) + DV / 32;
+                const int t0s = (int)(d.start + (int64_t)pend_j * BT);
+                for (int base = 0; base < n_items; base += kStagePanels) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
-                uint32_t x[32], y[32];
-                tmem_ld32(t_c3 + lane_off + c * 32, x);
-                tmem_ld32(t_c1 + lane_off + c * 32, y);
-                tmem_ld_wait();
-                warp_store_rows_f32(stage, x, dq + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
-                warp_store_rows_f32(stage, y, dkk + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
-            }
+                    for (int pi = 0; pi < kStagePanels; ++pi) {
+                        const int it = base + pi;
+                        if (it >= n_items || (it & 1) != half)
+                            continue;
+                        const int kind = it < dk / 32 ? 0 : (it < 2 * (dk / 32) ? 1 : 2);
+                        const int c = kind == 0 ? it : (kind == 1 ? it - dk / 32 : it - 2 * (dk / 32));
+                        const uint32_t col = (kind == 0 ? t_c3 : (kind == 1 ? t_c1 : t_c2)) + c * 32;
+                        uint32_t x[32];
+                        tmem_ld32(col + lane_off, x);
+                        tmem_ld_wait();
+                        unsigned char *sp = sm.z + pi * kPanel;
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
-                uint32_t x[32];
-                tmem_ld32(t_c2 + lane_off + c * 32, x);
-                tmem_ld_wait();
-                warp_store_rows_f32(stage, x, dvv + ((size_t)t_w * H + h) * dv + j0 + c * 32, (size_t)H * dv, n_valid, lane);
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            *reinterpret_cast<uint4 *>(sp + sw128_offset(r, k4)) =
+                                make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    epi_sync();
+                    if (warp == 2 && lane == 0) {
+                        for (int pi = 0; pi < kStagePanels && base + pi < n_items; ++pi) {
+                            const int it = base + pi;
+                            if (it < dk / 32)
+                                tma_store_3d(&tdq, sm.z + pi * kPanel, it * 32, h, t0s);
+                            else if (it < 2 * (dk / 32))
+                                tma_store_3d(&tdk, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
+                            else
+                                tma_store_3d(&tdv, sm.z + pi * kPanel, j0 + (it - 2 * (dk / 32)) * 32, h, t0s);
+                        }
+                        tma_store_commit();
+                        tma_store_wait_read();
+                    }
+                    epi_sync();   // staging panels may be reused
+                }
+            } else {
+                unsigned char *stage = sm.x + (warp - 2) * 4096;   // x is free until the next EA
+#pragma unroll
+                for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
+                    uint32_t x[32], y[32];
+                    tmem_ld32(t_c3 + lane_off + c * 32, x);
+                    tmem_ld32(t_c1 + lane_off + c * 32, y);
+                    tmem_ld_wait();
+                    warp_store_rows_f32(stage, x, dq + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
+                    warp_store_rows_f32(stage, y, dkk + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
+                }
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                    uint32_t x[32];
+                    tmem_ld32(t_c2 + lane_off + c * 32, x);
+                    tmem_ld_wait();
+                    warp_store_rows_f32(stage, x, dvv + ((size_t)t_w * H + h) * dv + j0 + c * 32, (size_t)H * dv, n_valid, lane);
+                }
             }
+            if (warp == 2 && lane == 0)
+                mbar_arrive(&sm.z_free);   // the producer may load the next state into z
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
             // decay gradient of the block (both halves compute it; half 0 stores)
@@ -535,8 +625,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
             // ---- S_in row r -> bf16 copy (z) and <S_in, E>
             if (st_tma) {
-                // the producer loaded S_in (bf16) into z with the block's inputs
-                ok = epi_all(mbar_wait(&sm.full_in, par, kWaitNs)) && !*abort_flag;
+                // the producer loaded S_in (bf16) into z
+                ok = epi_all(mbar_wait(&sm.full_z, par, kWaitNs)) && !*abort_flag;
                 if (!ok)
                     break;
             }
@@ -872,7 +962,8 @@ __global__ void add_partials_kernel(float *__restrict__ dq, float *__restrict__ 
 template <int DV, bool ABL>
 cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                const CUtensorMap &mv, const CUtensorMap &mdo, const CUtensorMap &mst,
-                               int st_tma, const float *gamma,
+                               int st_tma, const CUtensorMap &mdq, const CUtensorMap &mdk,
+                               const CUtensorMap &mdvv, int out_tma, const float *gamma,
                                const float *dfac, const void *states, int st_bf16, int st_stride,
                                const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
                                float *part)
@@ -885,7 +976,8 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
     const int slices = p.dv / DV;
     const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
     dim3 grid(p.H, p.n_docs, slices);
-    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, gamma, dfac, p.cu, p.T,
+    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma,
+                                                gamma, dfac, p.cu, p.T,
                                                 p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
                                                 ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
@@ -925,15 +1017,20 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
             return cudaErrorInvalidValue;
         st_tma = 1;
     }
+    // fp32 gradients of full blocks leave by TMA stores
+    CUtensorMap mdq = mq, mdk = mq, mdvv = mq;
+    const int out_tma = make_grad_map(&mdq, dq, p.dk, p.H, p.tokens) &&
+                        make_grad_map(&mdk, dk, p.dk, p.H, p.tokens) &&
+                        make_grad_map(&mdvv, dv, p.dv, p.H, p.tokens);
     const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
     if (p.dv == 64)
-        return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
+        return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
                                                   st_stride, dhT, dq, dk, dv, da, dh0, part)
-                   : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
+                   : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
                                                    st_stride, dhT, dq, dk, dv, da, dh0, part);
-    return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
+    return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
                                                st_stride, dhT, dq, dk, dv, da, dh0, part)
-               : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, mst, st_tma, gamma, dfac, states, st_bf16,
+               : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
                                                 st_stride, dhT, dq, dk, dv, da, dh0, part);
 }
 
