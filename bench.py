@@ -45,10 +45,19 @@ def parse():
 
 
 def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    from chunked_linear_attention_bounded_gb300.replicas import rank_env
+    e = rank_env()
+    return e.rank, e.world, e.local
+
+
+def config_of(w, world):
+    """The workload description both arms print."""
+    tokens = w.B * w.T
+    return {"workload": w.name, "tokens": tokens, "docs": w.n_docs if w.n_docs else w.B,
+            "H": w.H, "dk": w.dk, "dv": w.dv,
+            "decay": "bounded b*sigmoid(a), b=%g" % w.b if w.mode == 0 else "-softplus(a)",
+            "l2": "inputs larger than L2 (q,k,v,dO bf16: %.2f GB)" % (4 * tokens * w.H * w.dk * 2 / 1e9),
+            "parallelism": f"replicas x{world}"}
 
 
 def peaks():
@@ -131,59 +140,86 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def oracle_sample(inp, w, target_s: float):
-    """Times the fp64 oracle (as it stands) on a bounded sample of the
-    workload: the first document, truncated, on as many heads as the oracle
-    has threads.  Returns (tokens/s equivalent, cores, description)."""
+def size_oracle_sample(inp, w, target_s: float):
+    """Chooses a bounded sample of the workload for the fp64 oracle (as it
+    stands): a prefix of the packed token stream (its documents cut at the
+    prefix end) on a subset of the heads, grown until one fwd+bwd pass takes
+    about `target_s` seconds.  Returns (run, ntok, nh, seconds of the last
+    sizing pass); run() executes one fwd+bwd pass and returns its seconds."""
     import numpy as np
 
     import oracle
     threads = oracle.threads_used()
-    cu = inp["cu_seqlens"]
-    d0 = int(cu[1]) if cu is not None else w.T
-    nh = max(1, min(w.H, threads))
+    cu_full = (inp["cu_seqlens"].numpy().astype(np.int64) if inp.get("cu_seqlens") is not None
+               else np.arange(w.B + 1, dtype=np.int64) * w.T)
+    total = int(cu_full[-1])
 
-    def run(T):
-        sl = lambda t: t[0, :T, :nh].double().numpy()
+    def prepare(ntok, nh):
+        cu = np.concatenate([cu_full[cu_full < ntok], [ntok]])
+        sl = lambda t: t.reshape(-1, *t.shape[2:])[:ntok, :nh].double().numpy()
         q, k, v, dO = (sl(inp[x]) for x in ("q", "k", "v", "dO"))
-        a = inp["a"][0, :T, :nh].double().numpy()
-        h0 = inp["h0"][:1, :nh].double().numpy() if inp.get("h0") is not None else None
-        t0 = time.perf_counter()
-        oracle.fwd(q, k, v, a, w.b, w.mode, h0=h0)
-        oracle.bwd(q, k, v, a, dO, w.b, w.mode, h0=h0)
-        return time.perf_counter() - t0
+        a = inp["a"].reshape(-1, w.H)[:ntok, :nh].double().numpy()
+        h0 = None
+        if inp.get("h0") is not None:
+            h0 = inp["h0"][:len(cu) - 1, :nh].double().numpy()
 
-    T = min(d0, 256)
-    dt = run(T)
-    T = int(min(d0, max(T, T * target_s / max(dt, 1e-3))))
-    dt = run(T)
-    tok_s = T * nh / w.H / dt
-    desc = (f"first document truncated to {T} tokens x {nh} of {w.H} heads, fwd+bwd, "
-            f"{dt:.1f} s; tokens/s counts a token as all {w.H} heads")
-    return tok_s, threads, desc
+        def run():
+            t0 = time.perf_counter()
+            oracle.fwd(q, k, v, a, w.b, w.mode, h0=h0, cu_seqlens=cu)
+            oracle.bwd(q, k, v, a, dO, w.b, w.mode, h0=h0, cu_seqlens=cu)
+            return time.perf_counter() - t0
+        return run
+
+    ntok, nh = min(total, 1024), min(w.H, threads)
+    dt = prepare(ntok, nh)()
+    grow = target_s / max(dt, 1e-4)
+    # heads first (whole multiples of the thread count), then the prefix
+    nh2 = min(w.H, max(nh, int(nh * grow) // threads * threads))
+    grow *= nh / nh2
+    ntok, nh = int(min(total, max(ntok, ntok * grow))), nh2
+    run = prepare(ntok, nh)
+    dt = run()
+    if dt < 0.6 * target_s and ntok < total:      # the small first pass overstates the rate
+        ntok = int(min(total, ntok * target_s / max(dt, 1e-4)))
+        run = prepare(ntok, nh)
+        dt = run()
+    return run, ntok, nh, dt
+
+
+def sample_desc(w, ntok, nh, dt):
+    return (f"first {ntok} tokens of the packed stream x {nh} of {w.H} heads, fwd+bwd, "
+            f"{dt:.1f} s per pass; tokens/s counts a token as all {w.H} heads")
+
+
+def oracle_sample(inp, w, target_s: float):
+    """One timed oracle pass on a sample sized for `target_s` seconds.
+    Returns (tokens/s equivalent, cores, description)."""
+    import oracle
+    _, ntok, nh, dt = size_oracle_sample(inp, w, target_s)
+    return ntok * nh / w.H / dt, oracle.threads_used(), sample_desc(w, ntok, nh, dt)
 
 
 # ---------------------------------------------------------------- arms
 def reference_arm(args, w, inp):
+    """The reference arm: the fp64 oracle on the host cores, each step one
+    fwd+bwd pass over the same bounded sample of the workload."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     per_step = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    run, ntok, nh, dt = size_oracle_sample(inp, w, per_step)
     for _ in range(args.warmup):
-        oracle_sample(inp, w, per_step / 4)
-    vals = []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        v, cores, desc = oracle_sample(inp, w, per_step)
-        vals.append(v)
-    wall = time.perf_counter() - t0
-    value = statistics.median(vals)
+        run()
+    times = [run() for _ in range(args.steps)]
+    wall = sum(times)
+    value = ntok * nh / w.H * args.steps / wall
+    desc = sample_desc(w, ntok, nh, wall / args.steps)
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": w.name, "tokens": w.B * w.T, "H": w.H, "dk": w.dk, "dv": w.dv},
+           "config": config_of(w, world),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads_used(),
                             "kind": "oracle", "sample": desc},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -197,6 +233,7 @@ def ours_arm(args, w, inp):
 
     import chunked_linear_attention_bounded_gb300 as bdla
     from chunked_linear_attention_bounded_gb300 import bdla as B
+    from chunked_linear_attention_bounded_gb300 import replicas
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -232,8 +269,7 @@ def ours_arm(args, w, inp):
     launches_per_step = 4   # fwd: decay + fwd;  bwd: decay + bwd
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        replicas.barrier(world)
 
     for _ in range(max(3, args.warmup)):
         step(g)
@@ -263,11 +299,7 @@ def ours_arm(args, w, inp):
     barrier()
     for kid in kernels.values():
         B.set_kernel_events(kid, None, None)
-    ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
     kernel_ms = {n: sum(a.elapsed_time(b) for a, b in kev[n]) / K for n in kernels}
 
     # end to end through the public API with host buffers
@@ -294,18 +326,14 @@ def ours_arm(args, w, inp):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / K
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = replicas.max_over_ranks(f0.elapsed_time(f1) / K, world, dev)
     for code in (ws_f.read_status(), ws_b.read_status()):
         if code:
             raise RuntimeError(f"device status {code} after the timed steps")
 
     tokens = w.B * w.T
-    value = world * tokens / (ms / 1000.0)
-    e2e_value = world * tokens / (e2e_ms / 1000.0)
+    value = replicas.job_throughput(tokens, world, ms)
+    e2e_value = replicas.job_throughput(tokens, world, e2e_ms)
     hbm, hbm_src = peaks()
     ab = algorithmic_bytes(w, n_seq)
     dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
@@ -319,10 +347,7 @@ def ours_arm(args, w, inp):
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-               "config": {"workload": w.name, "tokens": tokens, "docs": n_seq if inp["cu_seqlens"] is not None else w.B,
-                          "H": w.H, "dk": w.dk, "dv": w.dv, "decay": "bounded b*sigmoid(a), b=-5" if w.mode == 0 else "-softplus(a)",
-                          "l2": "inputs larger than L2 (q,k,v,dO bf16: %.2f GB)" % (4 * tokens * w.H * w.dk * 2 / 1e9),
-                          "parallelism": f"replicas x{world}"},
+               "config": config_of(w, world),
                "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
                             "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
                             "traffic": None,
@@ -346,8 +371,9 @@ def main():
     w = WORKLOADS[args.workload]
     if w.fwd_only:
         w = dataclasses.replace(w, fwd_only=False)
-    if world > 1 and args.impl == "ours":
-        w = dataclasses.replace(w, seed=w.seed + 100 * rank)
+    if args.impl == "ours":
+        from chunked_linear_attention_bounded_gb300.replicas import rank_workload
+        w = rank_workload(w, rank)
     if args.impl == "reference" and rank != 0:
         return
     inp = make_inputs(w, with_grad=True)
