@@ -265,8 +265,11 @@ def ours_arm(args, w, inp):
                  outs=outs)
 
     kernels = {"decay": B.KERNEL_DECAY, "fwd": B.KERNEL_FWD, "bwd": B.KERNEL_BWD,
-               "states": B.KERNEL_STATES}
-    launches_per_step = 4   # fwd: decay + fwd;  bwd: decay + bwd
+               "states": B.KERNEL_STATES, "seg": B.KERNEL_SEG}
+    seg = B.segments_engaged(tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0)
+    # fwd: decay + fwd;  bwd: decay + bwd;  segments: summary + scan in each;
+    # dv = 256: the backward adds the second slice's partial sums
+    launches_per_step = 4 + (4 if seg else 0) + (1 if w.dv > 128 else 0)
 
     def barrier():
         replicas.barrier(world)
@@ -353,6 +356,7 @@ def ours_arm(args, w, inp):
                             "traffic": None,
                             "algorithmic_bytes_per_launch": ab[dom]},
                "kernel_ms": kernel_ms,
+               "seq_segments": seg,
                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h},
                "gpu_launches": launches_per_step * K,

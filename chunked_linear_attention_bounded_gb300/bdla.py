@@ -30,8 +30,8 @@ STATUS_NAMES = {0: "BDLA_OK", 1: "BDLA_ERR_NULL", 2: "BDLA_ERR_SHAPE", 3: "BDLA_
 # Every symbol include/bdla.h declares.
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
            "bdla_bwd_varlen", "bdla_read_status", "bdla_status_string", "bdla_version",
-           "bdla_set_kernel_events", "bdla_fwd_noalloc")
-KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES = 0, 1, 2, 3
+           "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_set_seq_split")
+KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 
 
 class BdlaError(RuntimeError):
@@ -79,6 +79,8 @@ def lib():
         L.bdla_set_kernel_events.restype = ci
         L.bdla_fwd_noalloc.argtypes = [vp, vp, vp, vp, f32, ci, vp, vp, ci, vp, Dims, ci, vp]
         L.bdla_fwd_noalloc.restype = ci
+        L.bdla_set_seq_split.argtypes = [ci]
+        L.bdla_set_seq_split.restype = ci
         del i32
         _lib = L
     return _lib
@@ -91,6 +93,29 @@ def set_kernel_events(kernel: int, start=None, stop=None):
     st = lib().bdla_set_kernel_events(int(kernel), h(start), h(stop))
     if st:
         raise BdlaError(st, "bdla_set_kernel_events")
+
+
+_seq_split = 0
+
+
+def set_seq_split(blocks: int):
+    """Sequence segments of 128-token blocks: 0 automatic, < 0 never, > 0
+    always this many blocks per segment (process-wide)."""
+    global _seq_split
+    lib().bdla_set_seq_split(int(blocks))
+    _seq_split = int(blocks)
+
+
+def segments_engaged(q_shape, dv: int, n_docs: int = 0) -> bool:
+    """Whether calls of this shape cut documents into segments under the
+    current setting (the segment buffers then appear in the workspace)."""
+    cur = _seq_split
+    with_cut = workspace_bytes(OP_FWD, q_shape, dv, n_docs)
+    set_seq_split(-1)
+    try:
+        return with_cut > workspace_bytes(OP_FWD, q_shape, dv, n_docs)
+    finally:
+        set_seq_split(cur)
 
 
 def status_string(s: int) -> str:

@@ -25,6 +25,8 @@ struct Layout {
     size_t dfac = 0;     // d lambda / d a [H, tokens] fp32 (backward)
     size_t states = 0;   // recomputed bf16 states for the backward, 0 if unused
     size_t part = 0;     // partial dq, dk, da of the second dv slice (dv = 256)
+    size_t seg = 0;      // segment summaries / initial states [slots, H, dk, dv] fp32
+    size_t lsum = 0;     // segment log-decay sums [slots, H] fp32
     size_t total = 0;
 };
 
@@ -35,6 +37,19 @@ constexpr int kBlock = 128;   // tokens per block of the tensor-core kernels
 // The backward reads the state before every 128-token block from checkpoints
 // whose stride divides 128 (fp32 or bf16); otherwise it recomputes them.
 bool bwd_ckpt_usable(int ckpt_stride) { return ckpt_stride > 0 && kBlock % ckpt_stride == 0; }
+
+// The segment plan depends on the sizes only (never on device data).
+SegPlan plan_of(const bdla_dims &d, int n_docs)
+{
+    Problem p{};
+    p.n_docs = n_docs;
+    p.T = d.T;
+    p.tokens = total_tokens(d);
+    p.H = d.H;
+    p.dk = d.dk;
+    p.dv = d.dv;
+    return plan_segments(p);
+}
 
 Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
 {
@@ -58,6 +73,13 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
                             sizeof(float));
         }
     }
+    const SegPlan sp = plan_of(d, n_docs);
+    if (sp.seg_blk > 0) {
+        L.seg = off;
+        off += round_up((size_t)sp.n_slots * d.H * d.dk * d.dv * sizeof(float));
+        L.lsum = off;
+        off += round_up((size_t)sp.n_slots * d.H * sizeof(float));
+    }
     L.total = off;
     return L;
 }
@@ -68,6 +90,8 @@ bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs)
         return BDLA_ERR_SHAPE;
     if (varlen && (d.B != 1 || n_docs < 1))
         return BDLA_ERR_SHAPE;
+    if ((varlen ? n_docs : d.B) > 65535)   // documents are a grid extent
+        return BDLA_ERR_UNSUPPORTED;
     if (d.dk != 64 && d.dk != 128)
         return BDLA_ERR_UNSUPPORTED;
     if (d.dv != 64 && d.dv != 128 && d.dv != 256)
@@ -123,6 +147,17 @@ Problem make_problem(const bdla_dims &d, const int32_t *cu, int n_docs, float b,
             return s_;                                                                             \
     } while (0)
 
+// Segment plan of a call with its buffers carved from the workspace.
+SegPlan seg_of(const bdla_dims &d, int n_docs, const Layout &L, void *ws)
+{
+    SegPlan sp = plan_of(d, n_docs);
+    if (sp.seg_blk > 0) {
+        sp.buf = reinterpret_cast<float *>(static_cast<char *>(ws) + L.seg);
+        sp.lsum = reinterpret_cast<float *>(static_cast<char *>(ws) + L.lsum);
+    }
+    return sp;
+}
+
 #define BDLA_CUDA(expr)                                                                            \
     do {                                                                                           \
         if ((expr) != cudaSuccess)                                                                 \
@@ -159,18 +194,27 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const bool fused_ckpt = ckpt && ckpt_stride % kBlock == 0;
+    const SegPlan seg = seg_of(d, p.n_docs, L, ws);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
     BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    if (seg.seg_blk > 0) {
+        // the state entering every segment
+        mark_start(BDLA_KERNEL_SEG, p.stream);
+        BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
+        BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
+        mark_stop(BDLA_KERNEL_SEG, p.stream);
+    }
     mark_start(BDLA_KERNEL_FWD, p.stream);
     BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
-                               fused_ckpt ? ckpt : nullptr, ckpt_dtype == BDLA_BF16, ckpt_stride));
+                               fused_ckpt ? ckpt : nullptr, ckpt_dtype == BDLA_BF16, ckpt_stride,
+                               seg));
     mark_stop(BDLA_KERNEL_FWD, p.stream);
     if (ckpt && !fused_ckpt) {
         // checkpoints inside the 128-token blocks: tile-serial state pass (fp32)
         mark_start(BDLA_KERNEL_STATES, p.stream);
         BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr,
-                                  static_cast<float *>(ckpt), ckpt_stride));
+                                  static_cast<float *>(ckpt), ckpt_stride, seg));
         mark_stop(BDLA_KERNEL_STATES, p.stream);
     }
     return BDLA_OK;
@@ -213,19 +257,33 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
     const void *states = ckpt;
     int st_bf16 = ck_bf16, st_stride = stride;
+    const SegPlan seg = seg_of(d, p.n_docs, L, ws);
     if (!bwd_ckpt_usable(stride)) {
         void *stb = wsb + L.states;
+        if (seg.seg_blk > 0) {
+            mark_start(BDLA_KERNEL_SEG, p.stream);
+            BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
+            BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
+            mark_stop(BDLA_KERNEL_SEG, p.stream);
+        }
         mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock));
+        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock, seg));
         mark_stop(BDLA_KERNEL_STATES, p.stream);
         states = stb;
         st_bf16 = 1;
         st_stride = kBlock;
     }
+    if (seg.seg_blk > 0) {
+        // the adjoint entering every segment from its end
+        mark_start(BDLA_KERNEL_SEG, p.stream);
+        BDLA_CUDA(launch_seg_summary(p, qb, dob, gamma, true, seg));
+        BDLA_CUDA(launch_seg_scan(p, dhT, true, seg));
+        mark_stop(BDLA_KERNEL_SEG, p.stream);
+    }
     float *part = L.part ? reinterpret_cast<float *>(wsb + L.part) : nullptr;
     mark_start(BDLA_KERNEL_BWD, p.stream);
     BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride, dhT, dq,
-                               dk, dv, da, dh0, part));
+                               dk, dv, da, dh0, part, seg));
     mark_stop(BDLA_KERNEL_BWD, p.stream);
     return BDLA_OK;
 }
@@ -344,6 +402,12 @@ bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_eve
     return BDLA_OK;
 }
 
-int bdla_version(void) { return 100; }
+bdla_status bdla_set_seq_split(int blocks)
+{
+    g_seq_split = blocks;
+    return BDLA_OK;
+}
+
+int bdla_version(void) { return 200; }
 
 }  // extern "C"

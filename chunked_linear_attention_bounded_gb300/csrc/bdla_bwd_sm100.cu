@@ -216,10 +216,10 @@ __device__ __forceinline__ void warp_store_rows_f32(unsigned char *stage, const 
 
 // Row r (of dk rows) of the state before block j from the checkpoint array.
 __device__ __forceinline__ void load_state_row(const void *states, int st_bf16, int stride,
-                                               int64_t n_slots, const DocSpan &d, int n, int h, int j,
+                                               int64_t n_slots, int64_t doc_start, int n, int h, int64_t jd,
                                                int dk, int dv, int j0, int r, float (&out)[32], int c)
 {
-    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / stride, stride);
+    const int64_t slot = ckpt_slot(doc_start, n, jd * BT / stride, stride);
     const size_t off = (((size_t)h * n_slots + slot) * dk + r) * dv + j0 + c * 32;
     if (st_bf16) {
         const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(states) + off);
@@ -264,20 +264,27 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
                  const float *__restrict__ dhT, float *__restrict__ dq_base, float *__restrict__ dk_base,
                  float *__restrict__ dvv, float *__restrict__ da_base, float *__restrict__ dh0,
-                 float *__restrict__ part, int64_t part_qk, int64_t part_a, DeviceStatus *st)
+                 float *__restrict__ part, int64_t part_qk, int64_t part_a, int n_docs, int seg_blk,
+                 const float *__restrict__ seg_init, DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x;
     const int j0 = blockIdx.z * DV;
     // slice 0 writes dq, dk, da; later slices write partial sums into `part`
     float *dq = blockIdx.z == 0 ? dq_base : part + (size_t)(blockIdx.z - 1) * (2 * part_qk + part_a);
     float *dkk = blockIdx.z == 0 ? dk_base : dq + part_qk;
     float *da = blockIdx.z == 0 ? da_base : dq + 2 * part_qk;
-    const DocSpan d = doc_span(cu, n, T);
-    if (!doc_valid(d, tokens))
+    // one document, or one segment of it (then the adjoint after its last
+    // token comes from seg_init)
+    const SegSpan span = seg_span(cu, T, tokens, n_docs, blockIdx.y, seg_blk);
+    if (!span.valid)
         return;
+    const int n = span.n;
+    DocSpan d;
+    d.start = span.start;
+    d.len = span.len;
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (tid == 0)
             set_status(st, BDLA_ERR_DEVICE, 0xB11u);
@@ -287,6 +294,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     const int kpan = dk / 64;
     const size_t sstride = (size_t)dk * dv;
     const int64_t unit = (int64_t)n * H + h;
+    const float *einit = seg_blk > 0 ? seg_init : dhT;
+    const int64_t einit_unit = seg_blk > 0 ? (int64_t)blockIdx.y * H + h : unit;
 
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -366,7 +375,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / st_stride, st_stride);
+                    const int64_t slot = ckpt_slot(span.doc_start, n, (int64_t)(span.blk_base + j) * BT / st_stride, st_stride);
                     mbar_arrive_expect_tx(&sm.full_z, zbytes);
                     for (int p = 0; p < DV / 64; ++p)
                         tma_load_3d(sm.z + p * kPanel, &tst, &sm.full_z, j0 + p * 64, 0,
@@ -470,8 +479,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    x[i] = __float_as_uint((dhT != nullptr && r < dk)
-                                               ? dhT[unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
+                    x[i] = __float_as_uint((einit != nullptr && r < dk)
+                                               ? einit[einit_unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
                                                : 0.0f);
                 tmem_st32(t_e + lane_off + c * 32, x);
             }
@@ -653,7 +662,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                     float s_in[32];
                     if (r < dk)
-                        load_state_row(states, st_bf16, st_stride, n_slots, d, n, h, j, dk, dv, j0, r, s_in, c);
+                        load_state_row(states, st_bf16, st_stride, n_slots, span.doc_start, n, h, span.blk_base + j, dk, dv, j0, r, s_in, c);
                     else
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
@@ -909,7 +918,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         if (ok && pend_j >= 0)
             ok = finish_block();
-        if (ok && dh0 != nullptr && r < dk) {
+        if (ok && dh0 != nullptr && span.s == 0 && r < dk) {
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
@@ -966,7 +975,7 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
                                const CUtensorMap &mdvv, int out_tma, const float *gamma,
                                const float *dfac, const void *states, int st_bf16, int st_stride,
                                const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
-                               float *part)
+                               float *part, const SegPlan &seg)
 {
     auto kern = bwd_sm100_kernel<DV, ABL>;
     const size_t smem = sizeof(BwdSmem<DV>);
@@ -975,13 +984,13 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
         return err;
     const int slices = p.dv / DV;
     const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
-    dim3 grid(p.H, p.n_docs, slices);
+    dim3 grid(p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs, slices);
     kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma,
                                                 gamma, dfac, p.cu, p.T,
                                                 p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
                                                 ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
-                                                part, n_qk, n_a, p.st);
+                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, p.st);
     if ((err = cudaGetLastError()) != cudaSuccess || slices == 1)
         return err;
     add_partials_kernel<<<1184, 256, 0, p.stream>>>(dq, dk, da, part, n_qk, n_a, slices - 1);
@@ -1000,7 +1009,7 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
                              const float *dfac, const void *states, int st_bf16, int st_stride,
                              const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
-                             float *part)
+                             float *part, const SegPlan &seg)
 {
     if (p.n_docs <= 0 || p.tokens == 0)
         return cudaSuccess;
@@ -1025,13 +1034,13 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
     const bool abl = p.mode == BDLA_DECAY_NEG_SOFTPLUS;
     if (p.dv == 64)
         return abl ? launch_bwd_sm100_t<64, true>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
-                                                  st_stride, dhT, dq, dk, dv, da, dh0, part)
+                                                  st_stride, dhT, dq, dk, dv, da, dh0, part, seg)
                    : launch_bwd_sm100_t<64, false>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
-                                                   st_stride, dhT, dq, dk, dv, da, dh0, part);
+                                                   st_stride, dhT, dq, dk, dv, da, dh0, part, seg);
     return abl ? launch_bwd_sm100_t<128, true>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
-                                               st_stride, dhT, dq, dk, dv, da, dh0, part)
+                                               st_stride, dhT, dq, dk, dv, da, dh0, part, seg)
                : launch_bwd_sm100_t<128, false>(p, mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma, gamma, dfac, states, st_bf16,
-                                                st_stride, dhT, dq, dk, dv, da, dh0, part);
+                                                st_stride, dhT, dq, dk, dv, da, dh0, part, seg);
 }
 
 }  // namespace bdla

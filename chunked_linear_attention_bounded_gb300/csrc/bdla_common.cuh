@@ -75,6 +75,70 @@ __device__ __forceinline__ bool doc_valid(const DocSpan &d, int64_t tokens)
     return d.start >= 0 && d.len >= 0 && d.start + d.len <= tokens;
 }
 
+// Sequence segments (sequence parallelism inside one GPU).  When the
+// (document, head) units are too few to fill the GPU, each document is cut
+// into segments of seg_blk 128-token blocks (a document without tokens still
+// has one, empty, segment) and one CTA takes one segment.  Segment s of
+// document n owns slot floor(cu[n] / L) + n + s, L = 128 seg_blk tokens;
+// slots are distinct across documents and fewer than ceil(tokens / L) +
+// n_docs.  Slots that no segment owns are gaps.  seg_blk == 0: no cut, the
+// slot is the document index.
+struct SegSpan {
+    int n;               // document
+    int s;               // segment inside the document
+    int64_t doc_start;   // first token of the document
+    int64_t start;       // first token of the segment
+    int64_t len;         // tokens in the segment
+    int blk_base;        // doc-local index of the segment's first 128-token block
+    bool last;           // the document's last segment
+    bool valid;          // false: a gap or a malformed document
+};
+
+__device__ __forceinline__ SegSpan seg_span(const int32_t *cu, int T, int64_t tokens, int n_docs,
+                                            int slot, int seg_blk)
+{
+    SegSpan g;
+    g.valid = false;
+    g.s = 0;
+    g.blk_base = 0;
+    g.last = true;
+    if (seg_blk <= 0) {
+        g.n = slot;
+        const DocSpan d = doc_span(cu, slot, T);
+        g.doc_start = g.start = d.start;
+        g.len = d.len;
+        g.valid = doc_valid(d, tokens);
+        return g;
+    }
+    const int64_t L = (int64_t)seg_blk * 128;
+    // largest n with floor(start(n) / L) + n <= slot (increasing in n for valid offsets)
+    int lo = 0, hi = n_docs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const int64_t sm = cu != nullptr ? (int64_t)cu[mid] : (int64_t)mid * T;
+        if (sm / L + mid <= slot)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const DocSpan d = doc_span(cu, lo, T);
+    if (!doc_valid(d, tokens))
+        return g;
+    const int64_t s = (int64_t)slot - (d.start / L + lo);
+    const int64_t nseg = d.len > 0 ? (d.len + L - 1) / L : 1;
+    if (s < 0 || s >= nseg)
+        return g;
+    g.n = lo;
+    g.s = (int)s;
+    g.doc_start = d.start;
+    g.start = d.start + s * L;
+    g.len = d.len - s * L < L ? d.len - s * L : L;
+    g.blk_base = (int)(s * seg_blk);
+    g.last = s == nseg - 1;
+    g.valid = true;
+    return g;
+}
+
 // Checkpoint slot of (document n, doc-local block c) for a given stride.
 __device__ __forceinline__ int64_t ckpt_slot(int64_t doc_start, int n, int64_t c, int stride)
 {

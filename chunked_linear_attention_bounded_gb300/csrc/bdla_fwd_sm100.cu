@@ -115,15 +115,21 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                  float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
-                 int64_t n_slots, DeviceStatus *st)
+                 int64_t n_slots, int n_docs, int seg_blk, const float *__restrict__ seg_init,
+                 DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     FwdSmem<DV> &sm = *reinterpret_cast<FwdSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j0 = blockIdx.x * DV, h = blockIdx.y, n = blockIdx.z;
-    const DocSpan d = doc_span(cu, n, T);
-    if (!doc_valid(d, tokens))
+    const int j0 = blockIdx.x * DV, h = blockIdx.y;
+    // one document, or one segment of it (then the initial state comes from seg_init)
+    const SegSpan span = seg_span(cu, T, tokens, n_docs, blockIdx.z, seg_blk);
+    if (!span.valid)
         return;
+    const int n = span.n;
+    DocSpan d;
+    d.start = span.start;
+    d.len = span.len;
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (tid == 0)
             set_status(st, BDLA_ERR_DEVICE, 0xA11u);
@@ -133,6 +139,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     const int kpan = dk / 64;
     const size_t sstride = (size_t)dk * dv;
     const int64_t unit = (int64_t)n * H + h;
+    const float *init = seg_blk > 0 ? seg_init : h0;
+    const int64_t init_unit = seg_blk > 0 ? (int64_t)blockIdx.z * H + h : unit;
 
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -294,8 +302,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float val = (h0 != nullptr && r < dk)
-                                          ? h0[unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
+                    const float val = (init != nullptr && r < dk)
+                                          ? init[init_unit * sstride + (size_t)r * dv + j0 + c * 32 + i]
                                           : 0.0f;
                     x[i] = __float_as_uint(val);
                 }
@@ -522,11 +530,12 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // ---- state: checkpoint, bf16 copy for the Q S GEMM, decay for the K V update
             {
                 const float el = expf(lend);
+                const int64_t jd = span.blk_base + j;   // doc-local block
                 const bool ck_block = ckpt != nullptr && ckpt_stride % BT == 0 &&
-                                      ((int64_t)j * BT) % ckpt_stride == 0;
+                                      (jd * BT) % ckpt_stride == 0;
                 const bool wck = ck_block && !ck_tma && r < dk;   // fp32 checkpoints: per-row stores
                 const size_t ckoff = wck ? ((size_t)h * n_slots +
-                                            ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride)) *
+                                            ckpt_slot(span.doc_start, n, jd * BT / ckpt_stride, ckpt_stride)) *
                                                sstride + (size_t)r * dv + j0
                                          : 0;
 #pragma unroll
@@ -567,7 +576,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     fence_proxy_async_smem();
                     epi_sync();
                     if (warp == 2 && lane == 0) {
-                        const int64_t slot = ckpt_slot(d.start, n, (int64_t)j * BT / ckpt_stride, ckpt_stride);
+                        const int64_t slot = ckpt_slot(span.doc_start, n, jd * BT / ckpt_stride, ckpt_stride);
                         for (int p = 0; p < DV / 64; ++p)
                             tma_store_3d(&tck, sm.sb + p * kPanel, j0 + p * 64, 0, (int)((int64_t)h * n_slots + slot));
                         tma_store_commit();
@@ -588,7 +597,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     store_o(nblk - 1);
             }
         }
-        if (ok && hT != nullptr && r < dk) {
+        if (ok && hT != nullptr && span.last && r < dk) {
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                 uint32_t x[32];
@@ -675,7 +684,7 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
                                       const CUtensorMap &mv, const CUtensorMap &mck, int ck_tma,
                                       const float *gamma, const float *h0,
                                       void *o, int o_f32, float *hT, void *ckpt, int ck_bf16,
-                                      int ckpt_stride)
+                                      int ckpt_stride, const SegPlan &seg)
 {
     auto kern = fwd_sm100_kernel<DV, ABL, STATES>;
     const size_t smem = sizeof(FwdSmem<DV>);
@@ -683,16 +692,17 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
     if (err != cudaSuccess)
         return err;
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
-    dim3 grid(p.dv / DV, p.H, p.n_docs);
+    dim3 grid(p.dv / DV, p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs);
     kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
                                                 p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
-                                                n_slots, p.st);
+                                                n_slots, p.n_docs, seg.seg_blk, seg.buf, p.st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride)
+                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride,
+                             const SegPlan &seg)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -722,7 +732,7 @@ cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
     }
 #define BDLA_FWD_GO(DV_, ABL_, ST_)                                                                 \
     return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, mck, ck_tma, gamma, h0, o, o_f32, hT,  \
-                                              ckpt, ck_bf16, ckpt_stride)
+                                              ckpt, ck_bf16, ckpt_stride, seg)
     if (states_only) {
         if (p.dv == 64)
             BDLA_FWD_GO(64, false, true);

@@ -27,6 +27,22 @@ inline int64_t ckpt_slots(const Problem &p, int stride)
     return (p.tokens + stride - 1) / stride + p.n_docs;
 }
 
+// Sequence segments of one call (see SegSpan): seg_blk 128-token blocks per
+// segment, 0 when every CTA walks a whole document.
+struct SegPlan {
+    int seg_blk = 0;
+    int64_t n_slots = 0;     // segment slots (the grid extent that replaces n_docs)
+    float *buf = nullptr;    // [n_slots][H][dk][dv] fp32: segment summaries, then initial states
+    float *lsum = nullptr;   // [n_slots][H] summed log-decay of each segment
+};
+
+// Chooses the segment length for a problem: a fixed length set through
+// bdla_set_seq_split, never (split < 0), or, by default, a cut into about
+// four segments per SM when the (document, head, dv slice) units are fewer
+// than the GPU's SMs.  Pointers are left null.
+SegPlan plan_segments(const Problem &p);
+extern int g_seq_split;
+
 // Events recorded around a kernel's launches (measurement hook, see
 // bdla_set_kernel_events); null when unset.
 struct KernelEvents {
@@ -52,14 +68,28 @@ cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *
 // checkpoints whose stride is below the 128-token block.
 cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                            int o_f32, float *hT, float *ckpt, int ckpt_stride);
+                            int o_f32, float *hT, float *ckpt, int ckpt_stride, const SegPlan &seg);
 
 // Tensor-core forward (tcgen05 / TMEM / TMA): o, hT and checkpoints whose
 // stride is a multiple of 128 tokens.
 // o == nullptr runs the state chain only (checkpoints for the backward).
+// With segments, seg.buf holds each segment's initial state (seg_scan).
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride);
+                             int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride,
+                             const SegPlan &seg);
+
+// Segment summaries (tensor cores).  Forward (x = k, y = v): the state a
+// segment adds from a zero start, sum_t e^{Lam_end - Lam_t} x_t y_t^T.
+// Backward (x = q, y = dO): the adjoint a segment adds going back from a zero
+// adjoint, sum_t e^{Lam_t} x_t y_t^T.  Lam is the inclusive cumulative
+// log-decay from the segment start; seg.lsum receives Lam_end.
+cudaError_t launch_seg_summary(const Problem &p, const __nv_bfloat16 *x, const __nv_bfloat16 *y,
+                               const float *gamma, bool backward, const SegPlan &seg);
+// Turns summaries into initial states in place.  Forward: S_0 = h0 (or 0),
+// S_{i+1} = e^{lsum_i} S_i + sum_i.  Backward, from the document end:
+// D_last = dhT (or 0), D_{i-1} = e^{lsum_i} D_i + sum_i.
+cudaError_t launch_seg_scan(const Problem &p, const float *init, bool backward, const SegPlan &seg);
 
 // Tensor-core backward.  `states` holds the state before every 128-token
 // block: checkpoints whose stride divides 128, fp32 or bf16.  For dv = 256
@@ -70,7 +100,7 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
                              const float *dfac, const void *states, int st_bf16, int st_stride,
                              const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
-                             float *part);
+                             float *part, const SegPlan &seg);
 
 
 

@@ -113,7 +113,7 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
     if (launch_fwd_sm100(p, static_cast<const __nv_bfloat16 *>(q),
                          static_cast<const __nv_bfloat16 *>(k),
                          static_cast<const __nv_bfloat16 *>(v), ptrs.gamma, h0, o,
-                         o_dtype == BDLA_F32, hT, nullptr, 0, 0) != cudaSuccess)
+                         o_dtype == BDLA_F32, hT, nullptr, 0, 0, SegPlan{}) != cudaSuccess)
         return BDLA_ERR_CUDA;
     return BDLA_OK;
 }

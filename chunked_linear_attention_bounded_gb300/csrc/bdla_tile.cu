@@ -39,31 +39,38 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                 const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dv,
                 const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                 float *__restrict__ hT, float *__restrict__ ckpt, int ckpt_stride,
-                int64_t n_slots)
+                int64_t n_slots, int n_docs, int seg_blk, const float *__restrict__ seg_init)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
     const int tid = threadIdx.x;
     const int j0 = blockIdx.x * kDvSlice;
     const int h = blockIdx.y;
-    const int n = blockIdx.z;
-    const DocSpan d = doc_span(cu, n, T);
-    if (!doc_valid(d, tokens))
+    // one document, or one segment of it (initial state from seg_init)
+    const SegSpan span = seg_span(cu, T, tokens, n_docs, blockIdx.z, seg_blk);
+    if (!span.valid)
         return;
+    const int n = span.n;
+    DocSpan d;
+    d.start = span.start;
+    d.len = span.len;
+    const int64_t off0 = (int64_t)span.blk_base * 128;   // doc-local offset of the segment
     const size_t sstride = (size_t)DK * dv;
     const int64_t unit = (int64_t)n * H + h;
+    const float *init = seg_blk > 0 ? seg_init : h0;
+    const int64_t init_unit = seg_blk > 0 ? (int64_t)blockIdx.z * H + h : unit;
 
     for (int e = tid; e < DK * kDvSlice; e += kThreads) {
         const int i = e / kDvSlice, j = e % kDvSlice;
-        sm.S[i][j] = h0 ? h0[unit * sstride + (size_t)i * dv + j0 + j] : 0.0f;
+        sm.S[i][j] = init ? init[init_unit * sstride + (size_t)i * dv + j0 + j] : 0.0f;
     }
     const int64_t ntiles = (d.len + kChunk - 1) / kChunk;
     for (int64_t c = 0; c < ntiles; ++c) {
         const int64_t t0 = d.start + c * kChunk;
         const int m = (int)(d.len - c * kChunk < kChunk ? d.len - c * kChunk : kChunk);
         __syncthreads();  // previous tile finished with the smem tiles and S
-        if (ckpt && ((c * kChunk) % ckpt_stride) == 0) {
-            const int64_t slot = ckpt_slot(d.start, n, c * kChunk / ckpt_stride, ckpt_stride);
+        if (ckpt && ((off0 + c * kChunk) % ckpt_stride) == 0) {
+            const int64_t slot = ckpt_slot(span.doc_start, n, (off0 + c * kChunk) / ckpt_stride, ckpt_stride);
             float *dst = ckpt + ((size_t)h * n_slots + slot) * sstride;
             for (int e = tid; e < DK * kDvSlice; e += kThreads) {
                 const int i = e / kDvSlice, j = e % kDvSlice;
@@ -139,7 +146,7 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         }
     }
     __syncthreads();
-    if (hT) {
+    if (hT && span.last) {
         for (int e = tid; e < DK * kDvSlice; e += kThreads) {
             const int i = e / kDvSlice, j = e % kDvSlice;
             hT[unit * sstride + (size_t)i * dv + j0 + j] = sm.S[i][j];
@@ -157,11 +164,11 @@ cudaError_t set_smem(K kernel, size_t bytes)
 
 cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
-                            int o_f32, float *hT, float *ckpt, int ckpt_stride)
+                            int o_f32, float *hT, float *ckpt, int ckpt_stride, const SegPlan &seg)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
-    dim3 grid(p.dv / kDvSlice, p.H, p.n_docs);
+    dim3 grid(p.dv / kDvSlice, p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs);
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
     cudaError_t err;
     if (p.dk == 64) {
@@ -169,13 +176,15 @@ cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv
         if ((err = set_smem(kern, sizeof(FwdSmem<64>))) != cudaSuccess)
             return err;
         kern<<<grid, kThreads, sizeof(FwdSmem<64>), p.stream>>>(q, k, v, gamma, p.cu, p.T, p.tokens,
-            p.H, p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots);
+            p.H, p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots, p.n_docs,
+            seg.seg_blk, seg.buf);
     } else {
         auto kern = fwd_tile_kernel<128>;
         if ((err = set_smem(kern, sizeof(FwdSmem<128>))) != cudaSuccess)
             return err;
         kern<<<grid, kThreads, sizeof(FwdSmem<128>), p.stream>>>(q, k, v, gamma, p.cu, p.T,
-            p.tokens, p.H, p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots);
+            p.tokens, p.H, p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots, p.n_docs,
+            seg.seg_blk, seg.buf);
     }
     return cudaGetLastError();
 }

@@ -168,8 +168,30 @@ bdla_status bdla_read_status(void *ws, void *stream);
  * benchmarks.  Returns BDLA_ERR_SHAPE for an unknown kernel id.
  */
 enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KERNEL_STATES = 3,
-       BDLA_KERNEL_COUNT = 4 };
+       BDLA_KERNEL_SEG = 4, BDLA_KERNEL_COUNT = 5 };
 bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
+
+/*
+ * Sequence parallelism inside one GPU.  The pages pass a state from chunk to
+ * chunk ("Engineering Long-Context Training for Trillion-Parameter MoE
+ * Models", sec. 3.1), so a (document, head) pair is a chain of 128-token
+ * blocks.  When those pairs are too few to occupy the GPU, the library cuts
+ * each document into segments of `blocks` 128-token blocks, first computes
+ * the state (forward) or adjoint state (backward) entering every segment
+ * (kernel id BDLA_KERNEL_SEG: one summary GEMM pass and one scan over the
+ * segments), then runs one CTA per segment.  The result is the same up to
+ * floating-point rounding order.
+ *   blocks == 0 (default): automatic; documents are cut, into about four
+ *                          segments per SM, only when (documents x heads x
+ *                          dv/128 slices) is below the GPU's SM count.
+ *   blocks <  0: never cut.
+ *   blocks >  0: always cut into segments of `blocks` blocks (at least as
+ *                long as needed to keep the segment count within 65535).
+ * The setting is process-wide and read when a call (or
+ * bdla_workspace_bytes) is made: the workspace size depends on it, so size
+ * the workspace after changing it.  Not thread-safe.  Always BDLA_OK.
+ */
+bdla_status bdla_set_seq_split(int blocks);
 
 /*
  * Forward pass for callers that cannot allocate device memory (no workspace
