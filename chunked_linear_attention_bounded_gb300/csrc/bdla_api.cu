@@ -27,6 +27,7 @@ struct Layout {
     size_t part = 0;     // partial dq, dk, da of the second dv slice (dv = 256)
     size_t seg = 0;      // segment summaries / initial states [slots, H, dk, dv] fp32
     size_t lsum = 0;     // segment log-decay sums [slots, H] fp32
+    size_t order = 0;    // documents by decreasing length, int32 [n_docs]
     size_t total = 0;
 };
 
@@ -79,6 +80,9 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
         off += round_up((size_t)sp.n_slots * d.H * d.dk * d.dv * sizeof(float));
         L.lsum = off;
         off += round_up((size_t)sp.n_slots * d.H * sizeof(float));
+    } else if (n_docs > 1 && n_docs <= kMaxOrderedDocs) {
+        L.order = off;
+        off += round_up((size_t)n_docs * sizeof(int32_t));
     }
     L.total = off;
     return L;
@@ -148,12 +152,15 @@ Problem make_problem(const bdla_dims &d, const int32_t *cu, int n_docs, float b,
     } while (0)
 
 // Segment plan of a call with its buffers carved from the workspace.
-SegPlan seg_of(const bdla_dims &d, int n_docs, const Layout &L, void *ws)
+// (The order array is filled by launch_doc_order for packed calls.)
+SegPlan seg_of(const bdla_dims &d, int n_docs, bool varlen, const Layout &L, void *ws)
 {
     SegPlan sp = plan_of(d, n_docs);
     if (sp.seg_blk > 0) {
         sp.buf = reinterpret_cast<float *>(static_cast<char *>(ws) + L.seg);
         sp.lsum = reinterpret_cast<float *>(static_cast<char *>(ws) + L.lsum);
+    } else if (varlen && L.order != 0) {
+        sp.order = reinterpret_cast<const int32_t *>(static_cast<char *>(ws) + L.order);
     }
     return sp;
 }
@@ -194,9 +201,11 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const bool fused_ckpt = ckpt && ckpt_stride % kBlock == 0;
-    const SegPlan seg = seg_of(d, p.n_docs, L, ws);
+    const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
     BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
+    if (seg.order)
+        BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
     if (seg.seg_blk > 0) {
         // the state entering every segment
@@ -252,12 +261,14 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const auto *dob = static_cast<const __nv_bfloat16 *>(dO);
+    const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
     BDLA_CUDA(launch_decay(p, a, gamma, dfac));
+    if (seg.order)
+        BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
     mark_stop(BDLA_KERNEL_DECAY, p.stream);
     const void *states = ckpt;
     int st_bf16 = ck_bf16, st_stride = stride;
-    const SegPlan seg = seg_of(d, p.n_docs, L, ws);
     if (!bwd_ckpt_usable(stride)) {
         void *stb = wsb + L.states;
         if (seg.seg_blk > 0) {

@@ -265,7 +265,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const float *__restrict__ dhT, float *__restrict__ dq_base, float *__restrict__ dk_base,
                  float *__restrict__ dvv, float *__restrict__ da_base, float *__restrict__ dh0,
                  float *__restrict__ part, int64_t part_qk, int64_t part_a, int n_docs, int seg_blk,
-                 const float *__restrict__ seg_init, DeviceStatus *st)
+                 const float *__restrict__ seg_init, const int32_t *__restrict__ doc_order,
+                 DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
@@ -278,7 +279,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     float *da = blockIdx.z == 0 ? da_base : dq + 2 * part_qk;
     // one document, or one segment of it (then the adjoint after its last
     // token comes from seg_init)
-    const SegSpan span = seg_span(cu, T, tokens, n_docs, blockIdx.y, seg_blk);
+    const SegSpan span = seg_span(cu, T, tokens, n_docs,
+                                   (seg_blk <= 0 && doc_order != nullptr) ? doc_order[blockIdx.y] : (int)blockIdx.y,
+                                   seg_blk);
     if (!span.valid)
         return;
     const int n = span.n;
@@ -502,7 +505,63 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int64_t t_w = d.start + (int64_t)pend_j * BT + 32 * q4;
             const int n_valid = (int)(d.len - ((int64_t)pend_j * BT + 32 * q4));
             const bool full_blk = d.len - (int64_t)pend_j * BT >= BT;
-            if (out_tma && full_blk && blockIdx.z == 0) {
+            if (DV == 128 && out_tma && full_blk && blockIdx.z == 0) {
+                // fp32 panels (32 columns) written by TMA stores, two per round
+                // (one per column half), staged alternately in z and x; a
+                // round waits only for the reads of the round before it.
+                // Items: dq panels, then dk panels, then dv panels; z is
+                // released once its last round has been read, x before the
+                // next block writes P into it.
+                const int n_items = 2 * (dk / 32) + DV / 32;
+                const int rounds = n_items / 2;
+                const int t0s = (int)(d.start + (int64_t)pend_j * BT);
+                auto item_col = [&](int it, int &coord, const CUtensorMap *&map) -> uint32_t {
+                    if (it < dk / 32) {
+                        coord = it * 32;
+                        map = &tdq;
+                        return t_c3 + it * 32;
+                    }
+                    if (it < 2 * (dk / 32)) {
+                        coord = (it - dk / 32) * 32;
+                        map = &tdk;
+                        return t_c1 + (it - dk / 32) * 32;
+                    }
+                    coord = j0 + (it - 2 * (dk / 32)) * 32;
+                    map = &tdv;
+                    return t_c2 + (it - 2 * (dk / 32)) * 32;
+                };
+                for (int k = 0; k < rounds; ++k) {
+                    unsigned char *buf = (k & 1) ? sm.x : sm.z;
+                    {
+                        int coord;
+                        const CUtensorMap *map;
+                        const uint32_t col = item_col(2 * k + half, coord, map);
+                        uint32_t x[32];
+                        tmem_ld32(col + lane_off, x);
+                        tmem_ld_wait();
+                        unsigned char *sp = buf + half * kPanel;
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            *reinterpret_cast<uint4 *>(sp + sw128_offset(r, k4)) =
+                                make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    epi_sync();
+                    if (warp == 2 && lane == 0) {
+                        for (int hh = 0; hh < 2; ++hh) {
+                            int coord;
+                            const CUtensorMap *map;
+                            item_col(2 * k + hh, coord, map);
+                            tma_store_3d(map, buf + hh * kPanel, coord, h, t0s);
+                        }
+                        tma_store_commit();
+                        tma_store_wait_read1();   // the round before this one is read
+                        if (k == rounds - 1)
+                            mbar_arrive(&sm.z_free);   // z's last round (rounds - 2) is read
+                    }
+                    epi_sync();   // that round's buffers may be staged again
+                }
+            } else if (out_tma && full_blk && blockIdx.z == 0) {
                 // fp32 panels (32 columns) staged in z + x and written by TMA stores:
                 // item i < dk/32: dq panel i; next dk/32: dk panels; then dv panels
                 constexpr int kStagePanels = DV / 64 + 2;
@@ -543,7 +602,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                     epi_sync();   // staging panels may be reused
                 }
+                if (warp == 2 && lane == 0)
+                    mbar_arrive(&sm.z_free);   // the producer may load the next state into z
             } else {
+                if (warp == 2 && lane == 0)
+                    tma_store_wait_read();   // x may still be read by earlier stores
+                epi_sync();
                 unsigned char *stage = sm.x + (warp - 2) * 4096;   // x is free until the next EA
 #pragma unroll
                 for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
@@ -561,9 +625,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tmem_ld_wait();
                     warp_store_rows_f32(stage, x, dvv + ((size_t)t_w * H + h) * dv + j0 + c * 32, (size_t)H * dv, n_valid, lane);
                 }
+                if (warp == 2 && lane == 0)
+                    mbar_arrive(&sm.z_free);   // the producer may load the next state into z
             }
-            if (warp == 2 && lane == 0)
-                mbar_arrive(&sm.z_free);   // the producer may load the next state into z
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
             // decay gradient of the block (both halves compute it; half 0 stores)
@@ -688,7 +752,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_before();
             mbar_arrive(&sm.z_ready);
 
-            // ---- EA
+            // ---- EA (P goes into x: the previous block's output stores are done reading it)
+            if (warp == 2 && lane == 0)
+                tma_store_wait_read();
             ok = epi_all(mbar_wait(&sm.m1_done, par, kWaitNs)) && !*abort_flag;
             if (!ok)
                 break;
@@ -937,6 +1003,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 set_status(st, BDLA_ERR_TIMEOUT, 13u);
         }
     }
+    if (warp == 2 && lane == 0)
+        tma_store_wait_all();   // output stores complete before the CTA's shared memory goes
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -990,7 +1058,7 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
                                                 p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
                                                 ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
-                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, p.st);
+                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st);
     if ((err = cudaGetLastError()) != cudaSuccess || slices == 1)
         return err;
     add_partials_kernel<<<1184, 256, 0, p.stream>>>(dq, dk, da, part, n_qk, n_a, slices - 1);

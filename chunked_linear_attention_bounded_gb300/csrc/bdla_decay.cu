@@ -81,6 +81,32 @@ decay_kernel(const float *__restrict__ a, float b, int mode, const int32_t *__re
     }
 }
 
+// Documents by decreasing length (ties: lower index first).  The kernels
+// that give one CTA to a whole document take documents in this order, so
+// the longest chains start first.  One CTA; each thread ranks its documents
+// against all others.
+__global__ void __launch_bounds__(1024)
+doc_order_kernel(const int32_t *__restrict__ cu, int n_docs, int32_t *__restrict__ order)
+{
+    for (int n = threadIdx.x; n < n_docs; n += blockDim.x) {
+        const int64_t ln = (int64_t)cu[n + 1] - cu[n];
+        int rank = 0;
+        for (int m = 0; m < n_docs; ++m) {
+            const int64_t lm = (int64_t)cu[m + 1] - cu[m];
+            rank += (lm > ln || (lm == ln && m < n)) ? 1 : 0;
+        }
+        order[rank] = n;
+    }
+}
+
+cudaError_t launch_doc_order(const Problem &p, int32_t *order)
+{
+    if (p.cu == nullptr || p.n_docs <= 1)
+        return cudaSuccess;
+    doc_order_kernel<<<1, 1024, 0, p.stream>>>(p.cu, p.n_docs, order);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *dfac)
 {
     if (p.n_docs <= 0)

@@ -116,14 +116,16 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                  float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
                  int64_t n_slots, int n_docs, int seg_blk, const float *__restrict__ seg_init,
-                 DeviceStatus *st)
+                 const int32_t *__restrict__ doc_order, DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     FwdSmem<DV> &sm = *reinterpret_cast<FwdSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = blockIdx.x * DV, h = blockIdx.y;
     // one document, or one segment of it (then the initial state comes from seg_init)
-    const SegSpan span = seg_span(cu, T, tokens, n_docs, blockIdx.z, seg_blk);
+    const SegSpan span = seg_span(cu, T, tokens, n_docs,
+                                   (seg_blk <= 0 && doc_order != nullptr) ? doc_order[blockIdx.z] : (int)blockIdx.z,
+                                   seg_blk);
     if (!span.valid)
         return;
     const int n = span.n;
@@ -695,7 +697,7 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
     dim3 grid(p.dv / DV, p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs);
     kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
                                                 p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
-                                                n_slots, p.n_docs, seg.seg_blk, seg.buf, p.st);
+                                                n_slots, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st);
     return cudaGetLastError();
 }
 

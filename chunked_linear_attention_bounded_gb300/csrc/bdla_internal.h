@@ -34,7 +34,15 @@ struct SegPlan {
     int64_t n_slots = 0;     // segment slots (the grid extent that replaces n_docs)
     float *buf = nullptr;    // [n_slots][H][dk][dv] fp32: segment summaries, then initial states
     float *lsum = nullptr;   // [n_slots][H] summed log-decay of each segment
+    // Without segments: documents by decreasing length (doc_order), or null
+    // for index order.
+    const int32_t *order = nullptr;
 };
+
+// Documents of packed calls with at most this many documents are taken
+// longest first.
+constexpr int kMaxOrderedDocs = 4096;
+cudaError_t launch_doc_order(const Problem &p, int32_t *order);
 
 // Chooses the segment length for a problem: a fixed length set through
 // bdla_set_seq_split, never (split < 0), or, by default, a cut into about
