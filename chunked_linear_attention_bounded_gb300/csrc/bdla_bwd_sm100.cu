@@ -416,7 +416,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int jj = 0; jj < nblk && ok; ++jj) {
                 const uint32_t par = jj & 1;
                 if (*abort_flag || !mbar_wait(&sm.full_in, par, kWaitNs) ||
-                    !mbar_wait(&sm.z_ready, par, kWaitNs) ||
+                    // S_in: straight from its TMA load, or once the epilogue converted it
+                    !mbar_wait(st_tma ? &sm.full_z : &sm.z_ready, par, kWaitNs) ||
                     (jj > 0 && !mbar_wait(&sm.acc_free, (jj - 1) & 1, kWaitNs))) {
                     ok = false;
                     break;
@@ -506,14 +507,17 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int n_valid = (int)(d.len - ((int64_t)pend_j * BT + 32 * q4));
             const bool full_blk = d.len - (int64_t)pend_j * BT >= BT;
             if (DV == 128 && out_tma && full_blk && blockIdx.z == 0) {
-                // fp32 panels (32 columns) written by TMA stores, two per round
-                // (one per column half), staged alternately in z and x; a
-                // round waits only for the reads of the round before it.
-                // Items: dq panels, then dk panels, then dv panels; z is
-                // released once its last round has been read, x before the
-                // next block writes P into it.
+                // fp32 panels (32 columns) written by TMA stores.  Items: dq
+                // panels, then dk panels, then dv panels.  The first n_a items
+                // go two per round (one per column half) staged alternately in
+                // z and x; the last four one per round (each half staging 16
+                // of its columns) alternately in x's two panels, so that z is
+                // released early for the next block's S_in.  A round waits
+                // only for the reads of the round before it; x's last round
+                // is awaited before the next block writes P into x.
                 const int n_items = 2 * (dk / 32) + DV / 32;
-                const int rounds = n_items / 2;
+                const int n_a = n_items - 4;           // 8 (dk = 128) or 4 (dk = 64)
+                const int rounds = n_a / 2 + 4;
                 const int t0s = (int)(d.start + (int64_t)pend_j * BT);
                 auto item_col = [&](int it, int &coord, const CUtensorMap *&map) -> uint32_t {
                     if (it < dk / 32) {
@@ -530,9 +534,18 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     map = &tdv;
                     return t_c2 + (it - 2 * (dk / 32)) * 32;
                 };
+                const int ka = n_a / 2;                  // two-item rounds
                 for (int k = 0; k < rounds; ++k) {
-                    unsigned char *buf = (k & 1) ? sm.x : sm.z;
-                    {
+                    const bool pair = k < ka;
+                    unsigned char *buf = pair ? ((k & 1) ? sm.x : sm.z) : sm.x + ((k - ka) & 1) * kPanel;
+                    if (k == ka) {
+                        // the first single-item round reuses x, which the last
+                        // two-item round may still be reading
+                        if (warp == 2 && lane == 0)
+                            tma_store_wait_read();
+                        epi_sync();
+                    }
+                    if (pair) {
                         int coord;
                         const CUtensorMap *map;
                         const uint32_t col = item_col(2 * k + half, coord, map);
@@ -544,20 +557,32 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         for (int k4 = 0; k4 < 8; ++k4)
                             *reinterpret_cast<uint4 *>(sp + sw128_offset(r, k4)) =
                                 make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    } else {
+                        int coord;
+                        const CUtensorMap *map;
+                        const uint32_t col = item_col(n_a + (k - ka), coord, map);
+                        uint32_t x[16];
+                        tmem_ld16(col + 16 * half + lane_off, x);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            *reinterpret_cast<uint4 *>(buf + sw128_offset(r, 4 * half + k4)) =
+                                make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
                     }
                     fence_proxy_async_smem();
                     epi_sync();
                     if (warp == 2 && lane == 0) {
-                        for (int hh = 0; hh < 2; ++hh) {
+                        const int n_st = pair ? 2 : 1;
+                        for (int hh = 0; hh < n_st; ++hh) {
                             int coord;
                             const CUtensorMap *map;
-                            item_col(2 * k + hh, coord, map);
+                            item_col(pair ? 2 * k + hh : n_a + (k - ka), coord, map);
                             tma_store_3d(map, buf + hh * kPanel, coord, h, t0s);
                         }
                         tma_store_commit();
                         tma_store_wait_read1();   // the round before this one is read
-                        if (k == rounds - 1)
-                            mbar_arrive(&sm.z_free);   // z's last round (rounds - 2) is read
+                        if (k == ka - 1)
+                            mbar_arrive(&sm.z_free);   // z's last round (ka - 2) is read
                     }
                     epi_sync();   // that round's buffers may be staged again
                 }
