@@ -22,13 +22,13 @@
 // Phases of one block (MMA warp <-> eight epilogue warps, two per TMEM lane
 // quarter splitting the columns):
 //   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
-//   EA  P (smem) and dP (registers), W sums, V -> V o w_s, E -> bf16 copy,
-//       E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
+//   EA  P (smem) and dP (registers), W sums, V -> V o w_s, E -> bf16 copy;
+//       then, while Mb runs, E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
 //   Mb  C2 = P^T dO, C1 = (V o w_s) E^T
-//   Eb  k . dk_inter, dP -> smem
+//   Eb  k . dk_inter, dP -> smem; then, while Md runs, dO -> e^{Lam} o dO
 //   Md  C1 += dP^T Q, C3 += dP K
-//   Ee  Q -> Q o e^{Lam}, K -> K o w_s in place
-//   Mf  C2 += (K o w_s) E, E += (Q o e^{Lam})^T dO
+//   Ee  K -> K o w_s in place
+//   Mf  C2 += (K o w_s) E, E += Q^T (e^{Lam} o dO)
 //   Eg  dq = C3, dk = C1, dv = C2, da      (overlaps the next block's loads)
 #include <cudaTypedefs.h>
 
@@ -894,7 +894,28 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     uint4 *va = reinterpret_cast<uint4 *>(sm.v + p * kPanel + sw128_offset(r, c8));
                     *va = scale_bf16x8(*va, wsc);
                 }
-            // E -> bf16 copy (z), E <- e^{Lam_end} E
+            // E -> bf16 copy (z)
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                uint32_t e[32];
+                tmem_ld32(t_e + lane_off + c * 32, e);
+                tmem_ld_wait();
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    u[i] = pack_bf16(__uint_as_float(e[2 * i]), __uint_as_float(e[2 * i + 1]));
+                unsigned char *zp = sm.z + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                        make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.ea_done);
+
+            // ---- while Mb runs (it touches neither E nor C3):
+            // E <- e^{Lam_end} E
             {
                 const float el = expf(lend);
 #pragma unroll
@@ -902,15 +923,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     uint32_t e[32];
                     tmem_ld32(t_e + lane_off + c * 32, e);
                     tmem_ld_wait();
-                    uint32_t u[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        u[i] = pack_bf16(__uint_as_float(e[2 * i]), __uint_as_float(e[2 * i + 1]));
-                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4)
-                        *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         e[i] = __float_as_uint(__uint_as_float(e[i]) * el);
@@ -942,10 +954,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tmem_st32(t_c3 + lane_off + c * 32, x);
             }
             sm.ypart[half][r] = yv;
-            tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sm.ea_done);
+            tmem_st_wait();   // visible to Md and Mf through the fence before eb_done
 
             // ---- Eb: k . dk_inter, then dP -> smem
             ok = epi_all(mbar_wait(&sm.mb_done, par, kWaitNs)) && !*abort_flag;
@@ -984,8 +993,16 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.eb_done);
+            // ---- while Md runs (it reads neither dO nor E): dO -> e^{Lam} o dO for Mf
+#pragma unroll
+            for (int p = 0; p < DV / 64; ++p)
+#pragma unroll
+                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
+                    uint4 *oa = reinterpret_cast<uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
+                    *oa = scale_bf16x8(*oa, qsc);
+                }
 
-            // ---- Ee: Q -> Q o e^{Lam}, K -> K o w_s in place
+            // ---- Ee: K -> K o w_s in place
             ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;
             if (!ok)
                 break;
@@ -994,9 +1011,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int p = 0; p < kpan; ++p)
 #pragma unroll
                 for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
-                    uint4 *qa = reinterpret_cast<uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
                     uint4 *ka = reinterpret_cast<uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
-                    *qa = scale_bf16x8(*qa, qsc);
                     *ka = scale_bf16x8(*ka, wsc);
                 }
             fence_proxy_async_smem();

@@ -60,7 +60,7 @@ struct FwdSmem {
     float gq[BT];        // Gamma per row (ablation diagonal path)
     float gam[BT / kChunk];
     uint64_t full_qk[2], empty_qk[2], score_full[2], score_free[2];
-    uint64_t full_v, empty_v, p_ready, o_full, drain;
+    uint64_t full_v, empty_v, p_ready, o_full, p_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -159,6 +159,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.empty_v, 1);
         mbar_init(&sm.p_ready, kEpiThreads);
         mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.p_free, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
@@ -269,6 +270,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     for (int ks = 0; ks < BT / 16; ++ks)
                         umma_bf16(t_o, sdesc_sw128(sp + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
+                    umma_commit(&sm.p_free);   // the P tile may be rewritten once this GEMM is done
                     // O += (Q o e^{Lam}) S_in
                     for (int ks = 0; ks < dk / 16; ++ks)
                         umma_bf16(t_o, sdesc_sw128(sq[s] + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
@@ -414,10 +416,15 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float ksc = valid ? expf(lend - lam_r) : 0.0f;
 
-            if (STATES)
+            if (STATES) {
                 ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
-            else
-                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+            } else {
+                // scores of this block, and the previous block's P read by its P V GEMM
+                bool got = mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs);
+                if (j > 0)
+                    got = got && mbar_wait(&sm.p_free, (j - 1) & 1, kWaitNs);
+                ok = epi_all(got) && !*abort_flag;
+            }
             if (!ok)
                 break;
             tc_fence_after();
