@@ -295,9 +295,11 @@ def ours_arm(args, w, inp):
     kernels = {"decay": B.KERNEL_DECAY, "fwd": B.KERNEL_FWD, "bwd": B.KERNEL_BWD,
                "states": B.KERNEL_STATES, "seg": B.KERNEL_SEG}
     seg = B.segments_engaged(tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0)
-    # fwd: decay + fwd;  bwd: decay + bwd;  segments: summary + scan in each;
-    # dv = 256: the backward adds the second slice's partial sums
-    launches_per_step = 4 + (4 if seg else 0) + (1 if w.dv > 128 else 0)
+    # fwd: decay + fwd;  bwd: decay + bwd;  packed documents without segments:
+    # the document order in each;  segments: summary + scan in each;  dv = 256:
+    # the backward adds the second slice's partial sums
+    ordered = g["cu_seqlens"] is not None and not seg and 1 < n_seq <= 4096
+    launches_per_step = 4 + (2 if ordered else 0) + (4 if seg else 0) + (1 if w.dv > 128 else 0)
 
     def barrier():
         replicas.barrier(world)
