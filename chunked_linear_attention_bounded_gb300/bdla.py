@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "BDLA_OK", 1: "BDLA_ERR_NULL", 2: "BDLA_ERR_SHAPE", 3: "BDLA_
 # Every symbol include/bdla.h declares.
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
            "bdla_bwd_varlen", "bdla_read_status", "bdla_status_string", "bdla_version",
-           "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_set_seq_split")
+           "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_set_seq_split", "bdla_decode")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 
 
@@ -81,6 +81,8 @@ def lib():
         L.bdla_fwd_noalloc.restype = ci
         L.bdla_set_seq_split.argtypes = [ci]
         L.bdla_set_seq_split.restype = ci
+        L.bdla_decode.argtypes = [vp, vp, vp, vp, f32, vp, vp, ci, Dims, ci, vp]
+        L.bdla_decode.restype = ci
         del i32
         _lib = L
     return _lib
@@ -209,6 +211,28 @@ def decay(a: torch.Tensor, b: float = -5.0, cu_seqlens: Optional[torch.Tensor] =
     if st:
         raise BdlaError(st, "bdla_decay")
     return gamma
+
+
+def decode(q, k, v, a, state, b: float = -5.0, mode: int = BOUNDED, o_dtype=torch.bfloat16,
+           out=None, stream=None) -> torch.Tensor:
+    """One recurrent step per sequence: q, k [B, H, dk], v [B, H, dv] bf16,
+    a [B, H] fp32; `state` fp32 [B, H, dk, dv] is updated in place
+    (S <- e^{lambda} S + k v^T).  Returns o = S^T q [B, H, dv]."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3)
+    _check(a, "a", torch.float32, 2)
+    _check(state, "state", torch.float32, 4)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if tuple(state.shape) != (B, H, dk, dv) or tuple(a.shape) != (B, H):
+        raise BdlaError(2, "decode shapes")
+    o = out if out is not None else torch.empty((B, H, dv), dtype=o_dtype, device=q.device)
+    st = lib().bdla_decode(_p(q), _p(k), _p(v), _p(a), b, _p(state), _p(o), _dtype_code(o.dtype),
+                           Dims(B, 1, H, dk, dv), mode, _stream_handle(stream))
+    if st:
+        raise BdlaError(st, "bdla_decode")
+    return o
 
 
 def _dtype_code(dt) -> int:

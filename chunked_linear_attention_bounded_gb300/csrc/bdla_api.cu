@@ -413,6 +413,28 @@ bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_eve
     return BDLA_OK;
 }
 
+bdla_status bdla_decode(const void *q, const void *k, const void *v, const float *a, float b,
+                        float *state, void *o, bdla_dtype o_dtype, bdla_dims d,
+                        bdla_decay_mode mode, void *stream)
+{
+    if (d.T != 1)
+        return BDLA_ERR_SHAPE;
+    BDLA_TRY(check_dims(d, false, 0));
+    BDLA_TRY(check_decay(b, kChunk, mode));
+    if (!q || !k || !v || !a || !state || !o)
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o) ||
+        !aligned16(a))
+        return BDLA_ERR_ALIGN;
+    if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
+        return BDLA_ERR_UNSUPPORTED;
+    BDLA_CUDA(launch_decode(d.B, d.H, d.dk, d.dv, static_cast<const __nv_bfloat16 *>(q),
+                            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
+                            a, b, mode, state, o, o_dtype == BDLA_F32,
+                            reinterpret_cast<cudaStream_t>(stream)));
+    return BDLA_OK;
+}
+
 bdla_status bdla_set_seq_split(int blocks)
 {
     g_seq_split = blocks;

@@ -69,6 +69,13 @@ inline void mark_stop(int kernel, cudaStream_t s)
         cudaEventRecord(g_kernel_events[kernel].stop, s);
 }
 
+// One recurrent step per sequence: state <- e^{lambda} state + k v^T in place,
+// o = state^T q.  q, k bf16 [B, H, dk]; v bf16 [B, H, dv]; a fp32 [B, H];
+// state fp32 [B, H, dk, dv]; o bf16 or fp32 [B, H, dv].
+cudaError_t launch_decode(int B, int H, int dk, int dv, const __nv_bfloat16 *q,
+                          const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *a, float b,
+                          int mode, float *state, void *o, int o_f32, cudaStream_t stream);
+
 // gamma and dfac (d lambda / d a, may be nullptr) are head-major [H][tokens].
 cudaError_t launch_decay(const Problem &p, const float *a, float *gamma, float *dfac);
 

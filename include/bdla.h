@@ -172,6 +172,25 @@ enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KER
 bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
 
 /*
+ * One recurrent (decode) step per sequence: the same recurrence for a single
+ * new token against a resident state, e.g. after a chunked prefill whose hT
+ * is the state (sec. 3.1 of the first page: the state passed between chunks;
+ * its sec. 3.3: inference over long contexts).  For each sequence n and
+ * head h:
+ *     lambda = log_decay(a[n, h]),  state <- exp(lambda) state + k v^T,
+ *     o = state^T q        (o reads the updated state, as o_t reads S_t)
+ *   q, k   bf16 [B, H, dk];  v bf16 [B, H, dv];  a fp32 [B, H]
+ *   state  fp32 [B, H, dk, dv], updated in place (the hT / h0 layout)
+ *   o      bf16 or fp32 [B, H, dv]
+ * d.T must be 1 (BDLA_ERR_SHAPE otherwise).  Same b / mode rules as
+ * bdla_fwd.  No workspace, no device-side errors.  Bound by HBM: it reads and
+ * writes the state once.
+ */
+bdla_status bdla_decode(const void *q, const void *k, const void *v, const float *a, float b,
+                        float *state, void *o, bdla_dtype o_dtype, bdla_dims d,
+                        bdla_decay_mode mode, void *stream);
+
+/*
  * Sequence parallelism inside one GPU.  The pages pass a state from chunk to
  * chunk ("Engineering Long-Context Training for Trillion-Parameter MoE
  * Models", sec. 3.1), so a (document, head) pair is a chain of 128-token

@@ -84,6 +84,20 @@ def test_segment_buffers_size_the_workspace(L):
         bdla.set_seq_split(0)
 
 
+def test_decode_host_validation(L):
+    """bdla_decode refuses bad arguments before any launch (fake pointers are
+    never dereferenced)."""
+    fake = ctypes.c_void_p(1 << 20)
+    call = lambda dims, b=-5.0, mode=0, ptr=fake, odt=0: L.bdla_decode(
+        ptr, fake, fake, fake, b, fake, fake, odt, dims, mode, None)
+    assert call(bdla.Dims(4, 2, 2, 128, 128)) == 2           # T must be 1
+    assert call(bdla.Dims(4, 1, 2, 96, 128)) == 5            # dk 96 unsupported
+    assert call(bdla.Dims(4, 1, 2, 128, 128), b=0.5) == 4    # b > 0
+    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=None) == 1
+    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=ctypes.c_void_p((1 << 20) + 4)) == 3
+    assert call(bdla.Dims(4, 1, 2, 128, 128), odt=7) == 5
+
+
 def test_host_validation_before_launch(L):
     assert _fwd(L, chunk=32) == 5                     # chunk != 16
     assert _fwd(L, b=0.5) == 4                        # b > 0
