@@ -428,8 +428,62 @@ def ours_arm(args, w, inp):
         dist.destroy_process_group()
 
 
+def decode_arm(args):
+    """Decode steps (bdla_decode): `--workload decode` times one new token for
+    each of 256 sequences x 32 heads (dk = dv = 128) against resident fp32
+    states (0.54 GB, larger than L2), a step reading and writing every state
+    once.  Single GPU; prints one JSON line."""
+    import torch
+
+    from chunked_linear_attention_bounded_gb300 import bdla as B
+    n_seq, H, dk, dv = 256, 32, 128, 128
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(1100)
+    q = (torch.randn((n_seq, H, dk), generator=g) / dk ** 0.5).bfloat16().to(dev)
+    k = torch.randn((n_seq, H, dk), generator=g)
+    k = (k / k.norm(dim=-1, keepdim=True)).bfloat16().to(dev)
+    v = torch.randn((n_seq, H, dv), generator=g).bfloat16().to(dev)
+    a = torch.randn((n_seq, H), generator=g).to(dev)
+    state = (torch.randn((n_seq, H, dk, dv), generator=g) * 0.1).to(dev)
+    o = torch.empty((n_seq, H, dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        B.decode(q, k, v, a, state, out=o)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = args.steps
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for _ in range(K):
+            B.decode(q, k, v, a, state, out=o)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    state_bytes = n_seq * H * dk * dv * 4
+    step_bytes = 2 * state_bytes + n_seq * H * (2 * dk * 2 + 2 * dv * 2 + 4)
+    hbm, hbm_src = peaks()
+    achieved = step_bytes / (ms / 1000.0) / 1e9
+    out = {"metric": "decode tokens/s (256 sequences x 32 heads, d=128, fp32 state)",
+           "value": n_seq / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+           "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": "decode", "sequences": n_seq, "H": H, "dk": dk, "dv": dv,
+                      "l2": "state larger than L2 (%.2f GB)" % (state_bytes / 1e9)},
+           "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
+                        "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
+                        "traffic": None, "algorithmic_bytes_per_launch": step_bytes},
+           "gpu_launches": K, "clocks": clk.summary()}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload == "decode":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the decode mode has no oracle timing arm"}))
+            return
+        decode_arm(args)
+        return
     from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS, make_inputs
     import dataclasses
     rank, world, _ = dist_env()
