@@ -348,9 +348,21 @@ def ours_arm(args, w, inp):
               for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # copies spread over several streams per direction (one large tensor each)
+    n_in, n_out = 2, 3
+    s_in = [torch.cuda.Stream(dev) for _ in range(n_in)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(n_out)]
     ev = lambda: torch.cuda.Event()
-    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    h2d_done = [[ev() for _ in range(n_in)] for _ in range(2)]
+    d2h_done = [[ev() for _ in range(n_out)] for _ in range(2)]
+    comp_done = [ev(), ev()]
+    # inputs split over the copy-in streams by size (largest first, to the lighter stream)
+    in_groups, loads = [[] for _ in range(n_in)], [0] * n_in
+    for k_, v_ in sorted(((k_, v_) for k_, v_ in host_in.items() if v_ is not None),
+                         key=lambda kv: -kv[1].numel() * kv[1].element_size()):
+        gi = loads.index(min(loads))
+        in_groups[gi].append(k_)
+        loads[gi] += v_.numel() * v_.element_size()
 
     def step_into(src, dst):
         do, dhT_, dq_, dk_, dv_, da_ = dst
@@ -364,31 +376,39 @@ def ours_arm(args, w, inp):
     def e2e_run(n):
         for i in range(n):
             b = i & 1
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(comp_done[b])          # step i-2 is done with these inputs
-                for k_, v_ in host_in.items():
-                    if v_ is not None:
-                        dev_in[b][k_].copy_(v_, non_blocking=True)
-                h2d_done[b].record(s_in)
-            stream.wait_event(h2d_done[b])
+            for si, st_ in enumerate(s_in):
+                with torch.cuda.stream(st_):
+                    if i >= 2:
+                        st_.wait_event(comp_done[b])      # step i-2 is done with these inputs
+                    for k_ in in_groups[si]:
+                        dev_in[b][k_].copy_(host_in[k_], non_blocking=True)
+                    h2d_done[b][si].record(st_)
+            for e_ in h2d_done[b]:
+                stream.wait_event(e_)
             if i >= 2:
-                stream.wait_event(d2h_done[b])             # step i-2's outputs have been copied out
+                for e_ in d2h_done[b]:
+                    stream.wait_event(e_)                  # step i-2's outputs have been copied out
             step_into(dev_in[b], dev_outs[b])
             comp_done[b].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(comp_done[b])
-                for hst, src in zip(host_out[b], dev_outs[b]):
-                    hst.copy_(src, non_blocking=True)
-                d2h_done[b].record(s_out)
+            for so, st_ in enumerate(s_out):
+                with torch.cuda.stream(st_):
+                    st_.wait_event(comp_done[b])
+                    # o, hT, dq, dk, dv, da: the three gradients on their own streams
+                    for idx in ((0, 1, 2, 5), (3,), (4,))[so]:
+                        host_out[b][idx].copy_(dev_outs[b][idx], non_blocking=True)
+                    d2h_done[b][so].record(st_)
 
     e2e_run(2)
     torch.cuda.synchronize()
     barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(s_in)
+    f0.record(stream)
+    for st_ in s_in:
+        st_.wait_event(f0)
     e2e_run(K)
-    f1.record(s_out)
+    for st_ in s_out:
+        stream.wait_stream(st_)
+    f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = replicas.max_over_ranks(f0.elapsed_time(f1) / K, world, dev)
     for code in (ws_f.read_status(), ws_b.read_status()):
