@@ -91,6 +91,12 @@ def algorithmic_bytes(w, n_seq):
 NCU_TRAFFIC = {
     ("fwd", "varlen64k"): (1643851264 + 1054437888, "f58929385e15a899"),
     ("bwd", "varlen64k"): (2735280384 + 3188669184, "cdb54b5ecc0d20d0"),
+    ("decode", "decode"): (543210000 + 478080000, "243a14f8e322bc2c"),
+}
+KERNEL_SOURCES = {
+    "fwd": ("bdla_fwd_sm100.cu", "bdla_sm100.cuh", "bdla_common.cuh"),
+    "bwd": ("bdla_bwd_sm100.cu", "bdla_sm100.cuh", "bdla_common.cuh"),
+    "decode": ("bdla_decode.cu", "bdla_common.cuh"),
 }
 
 
@@ -98,7 +104,7 @@ def kernel_digest(kernel: str) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "chunked_linear_attention_bounded_gb300", "csrc")
     m = hashlib.sha256()
-    for f in (f"bdla_{kernel}_sm100.cu", "bdla_sm100.cuh", "bdla_common.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]
@@ -491,7 +497,8 @@ def decode_arm(args):
                       "l2": "state larger than L2 (%.2f GB)" % (state_bytes / 1e9)},
            "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
                         "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
-                        "traffic": None, "algorithmic_bytes_per_launch": step_bytes},
+                        "traffic": measured_traffic("decode", "decode"),
+                        "algorithmic_bytes_per_launch": step_bytes},
            "gpu_launches": K, "clocks": clk.summary()}
     print(json.dumps(out), flush=True)
 
