@@ -200,7 +200,11 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    // checkpoints the forward writes itself: strides that are multiples of the
+    // 128-token block, or (fp32) block starts of strides dividing it
     const bool fused_ckpt = ckpt && ckpt_stride % kBlock == 0;
+    const bool split_ckpt = ckpt && !fused_ckpt && kBlock % ckpt_stride == 0 && ckpt_dtype == BDLA_F32 &&
+                            (int64_t)total_tokens(d) / kBlock + (varlen ? n_docs : d.B) < 65535;
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     mark_start(BDLA_KERNEL_DECAY, p.stream);
     BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
@@ -216,10 +220,15 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     }
     mark_start(BDLA_KERNEL_FWD, p.stream);
     BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
-                               fused_ckpt ? ckpt : nullptr, ckpt_dtype == BDLA_BF16, ckpt_stride,
-                               seg));
+                               (fused_ckpt || split_ckpt) ? ckpt : nullptr, ckpt_dtype == BDLA_BF16,
+                               ckpt_stride, seg));
     mark_stop(BDLA_KERNEL_FWD, p.stream);
-    if (ckpt && !fused_ckpt) {
+    if (split_ckpt) {
+        // the states inside each block, all blocks in parallel
+        mark_start(BDLA_KERNEL_STATES, p.stream);
+        BDLA_CUDA(launch_ckpt_expand(p, kb, vb, gamma, static_cast<float *>(ckpt), ckpt_stride));
+        mark_stop(BDLA_KERNEL_STATES, p.stream);
+    } else if (ckpt && !fused_ckpt) {
         // checkpoints inside the 128-token blocks: tile-serial state pass (fp32)
         mark_start(BDLA_KERNEL_STATES, p.stream);
         BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr,

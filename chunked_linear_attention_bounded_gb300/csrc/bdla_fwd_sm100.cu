@@ -540,8 +540,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             {
                 const float el = expf(lend);
                 const int64_t jd = span.blk_base + j;   // doc-local block
-                const bool ck_block = ckpt != nullptr && ckpt_stride % BT == 0 &&
-                                      (jd * BT) % ckpt_stride == 0;
+                // checkpoints at block starts: strides that are multiples of the
+                // block (every stride-th token) or divide it (every block start;
+                // the states inside the block are filled in afterwards)
+                const bool ck_block = ckpt != nullptr && (jd * BT) % ckpt_stride == 0 &&
+                                      (ckpt_stride % BT == 0 || BT % ckpt_stride == 0);
                 const bool wck = ck_block && !ck_tma && r < dk;   // fp32 checkpoints: per-row stores
                 const size_t ckoff = wck ? ((size_t)h * n_slots +
                                             ckpt_slot(span.doc_start, n, jd * BT / ckpt_stride, ckpt_stride)) *

@@ -85,8 +85,15 @@ cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv
                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
                             int o_f32, float *hT, float *ckpt, int ckpt_stride, const SegPlan &seg);
 
+// Fills fp32 checkpoints whose stride divides 128 inside each 128-token block
+// from the block-start states the tensor-core forward wrote (one CTA per
+// block, slice and head).
+cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                               const float *gamma, float *ckpt, int ckpt_stride);
+
 // Tensor-core forward (tcgen05 / TMEM / TMA): o, hT and checkpoints whose
-// stride is a multiple of 128 tokens.
+// stride is a multiple of 128 tokens, or the block-start ones of fp32
+// checkpoints whose stride divides 128.
 // o == nullptr runs the state chain only (checkpoints for the backward).
 // With segments, seg.buf holds each segment's initial state (seg_scan).
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,

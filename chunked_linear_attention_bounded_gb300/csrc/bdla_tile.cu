@@ -13,6 +13,7 @@
 // gamma = Gamma at the tile's last token; S is written to the checkpoint
 // array at every multiple of the stride.
 #include "bdla_internal.h"
+#include "bdla_sm100.cuh"
 
 namespace bdla {
 
@@ -154,6 +155,111 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     }
 }
 
+// Checkpoints inside the 128-token blocks.  The tensor-core forward has
+// written the state at every block start (fp32, same slot layout); this
+// kernel fills the states at the block's inner multiples of the stride, one
+// CTA per (64-column slice, head, block), all blocks at once: from the block
+// start S, each 16-token tile c applies
+//   S <- e^{gamma_c} S + sum_{t in tile} e^{gamma_c - Gamma_t} k_t v_t^T
+// (Gamma tile-local, gamma_c its value at the tile's last token; every weight
+// <= 1).  The block's keys and value slice are staged in shared memory once;
+// threads own 4 columns x DK/16 rows of the state (16 column groups x 16 row
+// groups).
+constexpr int kExpThreads = 256;
+
+template <int DK>
+struct ExpSmem {
+    __nv_bfloat16 k[128][DK];
+    __nv_bfloat16 v[128][kDvSlice];
+    float w[128];        // e^{gamma_c - Gamma_t} for the token's tile c
+    float eg[128 / kChunk];
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kExpThreads, 3)
+ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                   const float *__restrict__ gamma, const int32_t *__restrict__ cu, int T,
+                   int64_t tokens, int n_docs, int H, int dv, float *__restrict__ ckpt,
+                   int ckpt_stride, int64_t n_slots)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ExpSmem<DK> &sm = *reinterpret_cast<ExpSmem<DK> *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int j0 = blockIdx.x * kDvSlice, h = blockIdx.y;
+    const SegSpan blk = seg_span(cu, T, tokens, n_docs, blockIdx.z, 1);   // one 128-token block
+    if (!blk.valid || blk.len <= kChunk)
+        return;   // no tile boundary inside the block
+    const int n = blk.n;
+    const int64_t off0 = (int64_t)blk.blk_base * 128;   // doc-local first token
+    const int ntiles = (int)((blk.len + kChunk - 1) / kChunk);
+    const int m = (ntiles - 1) * kChunk;   // tokens feeding the inner states (full tiles)
+    // stage keys, values and weights of the block's first ntiles - 1 tiles
+    for (int e = tid; e < m * (DK / 8); e += kExpThreads) {
+        const int t = e / (DK / 8), c8 = e % (DK / 8);
+        reinterpret_cast<uint4 *>(&sm.k[t][0])[c8] =
+            reinterpret_cast<const uint4 *>(k + ((size_t)(blk.start + t) * H + h) * DK)[c8];
+    }
+    for (int e = tid; e < m * (kDvSlice / 8); e += kExpThreads) {
+        const int t = e / (kDvSlice / 8), c8 = e % (kDvSlice / 8);
+        reinterpret_cast<uint4 *>(&sm.v[t][0])[c8] =
+            reinterpret_cast<const uint4 *>(v + ((size_t)(blk.start + t) * H + h) * dv + j0)[c8];
+    }
+    if (tid < m) {
+        const float gt = gamma[(int64_t)h * tokens + blk.start + tid];
+        const float gend = gamma[(int64_t)h * tokens + blk.start + (tid | (kChunk - 1))];
+        sm.w[tid] = expf(gend - gt);
+        if ((tid & (kChunk - 1)) == kChunk - 1)
+            sm.eg[tid / kChunk] = expf(gend);
+    }
+    const size_t sstride = (size_t)DK * dv;
+    const int cg = tid % 16, rg = tid / 16;
+    const int col = j0 + 4 * cg;
+    constexpr int kRows = DK / 16;
+    float4 S[kRows];
+    {
+        const int64_t slot = ckpt_slot(blk.doc_start, n, off0 / ckpt_stride, ckpt_stride);
+        const float *src = ckpt + ((size_t)h * n_slots + slot) * sstride;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+            S[i] = *reinterpret_cast<const float4 *>(src + (size_t)(rg + 16 * i) * dv + col);
+    }
+    __syncthreads();
+    for (int c = 0; c + 1 < ntiles; ++c) {   // the last tile ends the block: not needed here
+        const float eg = sm.eg[c];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            S[i].x *= eg;
+            S[i].y *= eg;
+            S[i].z *= eg;
+            S[i].w *= eg;
+        }
+#pragma unroll 4
+        for (int tt = 0; tt < kChunk; ++tt) {
+            const int t = c * kChunk + tt;
+            const float wt = sm.w[t];
+            const uint2 vraw = *reinterpret_cast<const uint2 *>(&sm.v[t][4 * cg]);
+            const float v0 = wt * sm100::bf16_lo(vraw.x), v1 = wt * sm100::bf16_hi(vraw.x);
+            const float v2 = wt * sm100::bf16_lo(vraw.y), v3 = wt * sm100::bf16_hi(vraw.y);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                const float kk = bf2f(sm.k[t][rg + 16 * i]);
+                S[i].x = fmaf(kk, v0, S[i].x);
+                S[i].y = fmaf(kk, v1, S[i].y);
+                S[i].z = fmaf(kk, v2, S[i].z);
+                S[i].w = fmaf(kk, v3, S[i].w);
+            }
+        }
+        const int64_t tl = off0 + (int64_t)(c + 1) * kChunk;   // doc-local token the state precedes
+        if (tl % ckpt_stride == 0) {
+            const int64_t slot = ckpt_slot(blk.doc_start, n, tl / ckpt_stride, ckpt_stride);
+            float *dst = ckpt + ((size_t)h * n_slots + slot) * sstride;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i)
+                *reinterpret_cast<float4 *>(dst + (size_t)(rg + 16 * i) * dv + col) = S[i];
+        }
+    }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes)
 {
@@ -185,6 +291,35 @@ cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv
         kern<<<grid, kThreads, sizeof(FwdSmem<128>), p.stream>>>(q, k, v, gamma, p.cu, p.T,
             p.tokens, p.H, p.dv, h0, o, o_f32, hT, ckpt, ckpt_stride, n_slots, p.n_docs,
             seg.seg_blk, seg.buf);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                               const float *gamma, float *ckpt, int ckpt_stride)
+{
+    if (p.n_docs <= 0 || p.tokens <= 0)
+        return cudaSuccess;
+    const int64_t n_slots = ckpt_slots(p, ckpt_stride);
+    const int64_t blocks = (p.tokens + 127) / 128 + p.n_docs;   // block slots (seg_span with 1-block segments)
+    if (blocks > 65535)
+        return cudaErrorInvalidValue;
+    dim3 grid(p.dv / kDvSlice, p.H, (unsigned)blocks);
+    cudaError_t err;
+    if (p.dk == 64) {
+        auto kern = ckpt_expand_kernel<64>;
+        if ((err = set_smem(kern, sizeof(ExpSmem<64>))) != cudaSuccess)
+            return err;
+        kern<<<grid, kExpThreads, sizeof(ExpSmem<64>), p.stream>>>(k, v, gamma, p.cu, p.T, p.tokens,
+                                                                  p.n_docs, p.H, p.dv, ckpt, ckpt_stride,
+                                                                  n_slots);
+    } else {
+        auto kern = ckpt_expand_kernel<128>;
+        if ((err = set_smem(kern, sizeof(ExpSmem<128>))) != cudaSuccess)
+            return err;
+        kern<<<grid, kExpThreads, sizeof(ExpSmem<128>), p.stream>>>(k, v, gamma, p.cu, p.T, p.tokens,
+                                                                   p.n_docs, p.H, p.dv, ckpt, ckpt_stride,
+                                                                   n_slots);
     }
     return cudaGetLastError();
 }
