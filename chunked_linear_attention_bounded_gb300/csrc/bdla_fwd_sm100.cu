@@ -53,13 +53,12 @@ struct FwdSmem {
     alignas(1024) unsigned char q[2][2 * kPanel];   // stages x dk panels
     alignas(1024) unsigned char k[2][2 * kPanel];
     alignas(1024) unsigned char v[(DV / 64) * kPanel];
-    alignas(1024) unsigned char p[2 * kPanel];      // P: rows t, panels over s
     alignas(1024) unsigned char sb[(DV / 64) * kPanel];  // state bf16: rows dk, panels over dv
     float cdiag[BT];     // e^{-Gamma_s}
     float coff[BT];      // e^{gamma_sig - Gamma_s}
     float gq[BT];        // Gamma per row (ablation diagonal path)
     float gam[BT / kChunk];
-    uint64_t full_qk[2], empty_qk[2], score_full[2], score_free[2];
+    uint64_t full_qk[2], empty_qk[2], score_full[2];
     uint64_t full_v, empty_v, p_ready, o_full, p_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -153,7 +152,6 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_init(&sm.full_qk[s], 1);
             mbar_init(&sm.empty_qk[s], 1);
             mbar_init(&sm.score_full[s], 1);
-            mbar_init(&sm.score_free[s], kEpiThreads);
         }
         mbar_init(&sm.full_v, 1);
         mbar_init(&sm.empty_v, 1);
@@ -233,13 +231,14 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t id_kv = idesc_bf16_f32(128, DV, true, true);
             const uint32_t sq[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
             const uint32_t sk[2] = {smem_u32(sm.k[0]), smem_u32(sm.k[1])};
-            const uint32_t sv = smem_u32(sm.v), sp = smem_u32(sm.p), ssb = smem_u32(sm.sb);
+            const uint32_t sv = smem_u32(sm.v), ssb = smem_u32(sm.sb);
             bool ok = true;
             auto issue_qk = [&](int j) -> bool {
                 const int s = j & 1;
                 if (!mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs))
                     return false;
-                if (j >= 2 && !mbar_wait(&sm.score_free[s], ((j >> 1) - 1) & 1, kWaitNs))
+                // the P of block j - 2 (in this score buffer) has been read by its P V GEMM
+                if (j >= 2 && !mbar_wait(&sm.p_free, j & 1, kWaitNs))
                     return false;
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks) {
@@ -266,11 +265,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 tc_fence_after();
                 if (!STATES) {
-                    // O = P V
+                    // O = P V, P from tensor memory
                     for (int ks = 0; ks < BT / 16; ++ks)
-                        umma_bf16(t_o, sdesc_sw128(sp + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
-                                  sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
-                    umma_commit(&sm.p_free);   // the P tile may be rewritten once this GEMM is done
+                        umma_bf16_ts(t_o, t_score0 + 128 * s + ks * 8,
+                                     sdesc_sw128(sv + ks * 2048, kPanel, 1024), id_pv, ks > 0);
+                    umma_commit(&sm.p_free);   // the score buffer may take new scores once this GEMM is done
                     // O += (Q o e^{Lam}) S_in
                     for (int ks = 0; ks < dk / 16; ++ks)
                         umma_bf16(t_o, sdesc_sw128(sq[s] + (ks >> 2) * kPanel + (ks & 3) * 32, 16, 1024),
@@ -419,41 +418,39 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (STATES) {
                 ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
             } else {
-                // scores of this block, and the previous block's P read by its P V GEMM
-                bool got = mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs);
-                if (j > 0)
-                    got = got && mbar_wait(&sm.p_free, (j - 1) & 1, kWaitNs);
-                ok = epi_all(got) && !*abort_flag;
+                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
             }
             if (!ok)
                 break;
             tc_fence_after();
 
+            // explicit position-pair path for the diagonal tile (ablation): the
+            // warp whose columns hold the rows' diagonal tile (chunk q4) computes
+            // all 16 pairs of each row; they replace the GEMM values in P below
+            uint32_t pair[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (ABL) {
-                // explicit position-pair path for the diagonal tile: each half
-                // computes 8 of the row's 16 pairs and writes them, as one
-                // 16-byte chunk, straight into P
-                float pr[8];
+                if ((q4 & 1) == half) {
+                    float pr[16];
 #pragma unroll 1
-                for (int i = 0; i < 8; ++i) {
-                    const int sc = 16 * tau + 8 * half + i;
-                    float acc = 0.0f;
-                    if (valid && sc <= r) {
-                        for (int p = 0; p < kpan; ++p)
+                    for (int i = 0; i < 16; ++i) {
+                        const int sc = 16 * tau + i;
+                        float acc = 0.0f;
+                        if (valid && sc <= r) {
+                            for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
-                                const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k[s] + p * kPanel + sw128_offset(sc, c8));
-                                acc = dot_bf16x8(qa, kk, acc);
-                            }
-                        acc *= expf(g - sm.gq[sc]);
+                                for (int c8 = 0; c8 < 8; ++c8) {
+                                    const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
+                                    const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k[s] + p * kPanel + sw128_offset(sc, c8));
+                                    acc = dot_bf16x8(qa, kk, acc);
+                                }
+                            acc *= expf(g - sm.gq[sc]);
+                        }
+                        pr[i] = acc;
                     }
-                    pr[i] = acc;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pair[i] = pack_bf16(pr[2 * i], pr[2 * i + 1]);
                 }
-                const int cidx = 2 * tau + half;   // 16-byte chunk of the row (of 16)
-                *reinterpret_cast<uint4 *>(sm.p + (cidx >> 3) * kPanel + sw128_offset(r, cidx & 7)) =
-                    make_uint4(pack_bf16(pr[0], pr[1]), pack_bf16(pr[2], pr[3]), pack_bf16(pr[4], pr[5]),
-                               pack_bf16(pr[6], pr[7]));
                 epi_sync();   // every thread is done with the raw K rows
             }
             // ---- fold the decay into Q and K in place (row r, half the chunks)
@@ -468,15 +465,18 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         *qa = scale_bf16x8(*qa, qsc);
                     }
                 }
-            // ---- P = decay-weighted causal scores (bf16, K-major rows t)
+            // ---- P = decay-weighted causal scores, bf16 pairs written back into
+            //      this block's score buffer (columns 16c .. 16c + 15 for chunk
+            //      c), where the P V GEMM reads them
             if (!STATES) {
+                uint32_t uu[2][16];
                 float f[BT / kChunk];   // per source tile: e^{G_tau - G_sig+1} e^{Gamma_t}
 #pragma unroll
                 for (int sg = 0; sg < BT / kChunk; ++sg)
                     f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
 #pragma unroll
                 for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
-                    uint32_t u[16];
+                    uint32_t (&u)[16] = uu[c >> 1];
                     if (c <= q4) {   // chunks above the warp's rows are causally zero
                         uint32_t x[32];
                         tmem_ld32(t_score0 + 128 * s + lane_off + c * 32, x);
@@ -505,22 +505,26 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             u[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                        if (ABL && c == q4) {
+                            // the row's diagonal tile: columns 16 (tau & 1) .. + 15 of this chunk
+                            const bool upper = (tau & 1) != 0;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                u[i] = upper ? u[i] : pair[i];
+                                u[8 + i] = upper ? pair[i] : u[8 + i];
+                            }
+                        }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             u[i] = 0u;
                     }
-                    unsigned char *pp = sm.p + (c >> 1) * kPanel;
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        if (ABL && 2 * c + (k4 >> 1) == tau)
-                            continue;   // the diagonal tile was written by the pair path
-                        *reinterpret_cast<uint4 *>(pp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                            make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
-                    }
                 }
-                tc_fence_before();
-                mbar_arrive(&sm.score_free[s]);
+                epi_sync();   // every score of the buffer is read before P lands on it
+#pragma unroll
+                for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half)
+                    tmem_st16(t_score0 + 128 * s + lane_off + 16 * c, uu[c >> 1]);
+                tmem_st_wait();
             }
 
             // ---- output of the previous block
