@@ -27,7 +27,9 @@
 // warp 1 allocates TMEM and issues the MMAs, warps 2-9 (two per TMEM lane
 // quarter, splitting the columns) turn scores into P, fold the decay into Q
 // and K in place, move the state between TMEM and its bf16 shared copy, and
-// store O.
+// store O.  P is written back (bf16) into its block's score buffer in TMEM,
+// from where the P V GEMM reads its A operand; the score GEMM of block j+2
+// reuses that buffer once block j's P V GEMM has completed.
 // Every wait is bounded; on expiry the CTA records BDLA_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -494,7 +496,6 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                 const int col = c * 32 + i;
                                 const int sg = col >> 4;
                                 const float sc = __uint_as_float(x[i]);
-                                float val;
                                 // branch-free: rows of one warp sit in two different tiles
                                 const bool diag = (sg == tau);
                                 const bool live = (sg < tau) || (!ABL && diag && col <= r);
