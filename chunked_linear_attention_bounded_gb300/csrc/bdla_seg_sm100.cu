@@ -36,8 +36,8 @@ using namespace sm100;
 
 constexpr int BT = 128;
 constexpr int kStages = 3;
-constexpr int kRowThreads = 128;                  // warps 2-5: one token row (then one key row) each
-constexpr int kSegThreads = 64 + kRowThreads;     // + producer warp and MMA warp
+constexpr int kRowThreads = 128;                       // warps 2-5: one token row each
+constexpr int kSegThreads = 64 + 2 * kRowThreads;      // + producer, MMA and 4 epilogue warps
 constexpr uint32_t kPanel = 16384;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -46,7 +46,7 @@ struct SegSmem {
     alignas(1024) unsigned char x[kStages][2 * kPanel];          // rows: tokens, panels: dk
     alignas(1024) unsigned char y[kStages][(DV / 64) * kPanel];  // rows: tokens, panels: dv
     float gam[BT / kChunk];
-    uint64_t full[kStages], xready[kStages], empty[kStages], done;
+    uint64_t full[kStages], xready[kStages], empty[kStages], acc_full[2], acc_free[2], drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -79,33 +79,41 @@ __device__ __forceinline__ uint4 scale_row8(uint4 x, float s)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One CTA per (dv slice, head, segment slot).  BWD selects the weights
-// e^{Lam_t} (blocks in token order) instead of e^{Lam_end - Lam_t} (blocks
-// from the segment end).
+// Persistent: each CTA walks the (segment slot, head, dv slice) items
+// blockIdx.x, blockIdx.x + gridDim.x, ...; the TMA ring and the MMA
+// pipeline run on across items, two TMEM accumulators let one item's sums
+// drain while the next accumulates.  Warp 0 loads, warp 1 issues the MMAs,
+// warps 2-5 scale the x rows, warps 6-9 write the sums.  BWD selects the
+// weights e^{Lam_t} (blocks in token order) instead of e^{Lam_end - Lam_t}
+// (blocks from the segment end).
 template <int DV, bool BWD>
 __global__ void __launch_bounds__(kSegThreads, 1)
 seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty,
                    const float *__restrict__ gamma, const int32_t *__restrict__ cu, int T,
-                   int64_t tokens, int n_docs, int H, int dk, int dv, int seg_blk,
+                   int64_t tokens, int n_docs, int H, int dk, int dv, int seg_blk, int64_t n_items,
                    float *__restrict__ sums, float *__restrict__ lsum, DeviceStatus *st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     SegSmem<DV> &sm = *reinterpret_cast<SegSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j0 = blockIdx.x * DV, h = blockIdx.y, slot = blockIdx.z;
-    const SegSpan g = seg_span(cu, T, tokens, n_docs, slot, seg_blk);
-    if (!g.valid)
-        return;
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (tid == 0)
             set_status(st, BDLA_ERR_DEVICE, 0xC11u);
         return;
     }
-    const int nblk = (int)((g.len + BT - 1) / BT);
     const int kpan = dk / 64;
+    const int slices = dv / DV;
+    // item -> (slot, head, slice) and its segment (len < 0: nothing to do)
+    auto item = [&](int64_t i, int &slot, int &h, int &j0, SegSpan &g) -> int {
+        j0 = (int)(i % slices) * DV;
+        h = (int)((i / slices) % H);
+        slot = (int)(i / ((int64_t)slices * H));
+        g = seg_span(cu, T, tokens, n_docs, slot, seg_blk);
+        return g.valid ? (int)((g.len + BT - 1) / BT) : -1;
+    };
 
     if (warp == 1) {
-        tmem_alloc(&sm.tmem_base, DV);
+        tmem_alloc(&sm.tmem_base, 2 * DV);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -114,7 +122,11 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
             mbar_init(&sm.xready[s], kRowThreads);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.done, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_free[a], kRowThreads);
+        }
+        mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
     }
@@ -137,119 +149,162 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
             tma_prefetch_desc(&tx);
             tma_prefetch_desc(&ty);
             const uint32_t bytes = (uint32_t)(kpan + DV / 64) * kPanel;
-            int last[kStages];
-            for (int s = 0; s < kStages; ++s)
-                last[s] = -1;
+            int64_t gb = 0;   // blocks loaded by this CTA
             bool ok = true;
-            for (int i = 0; i < nblk; ++i) {
-                if (*abort_flag) {
-                    ok = false;
-                    break;
+            for (int64_t i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+                int slot, h, j0;
+                SegSpan g;
+                const int nblk = item(i, slot, h, j0, g);
+                for (int b = 0; b < nblk; ++b, ++gb) {
+                    const int j = BWD ? b : nblk - 1 - b;
+                    const int s = (int)(gb % kStages);
+                    if (*abort_flag || (gb >= kStages && !mbar_wait(&sm.empty[s], ((gb / kStages) - 1) & 1, kWaitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    const int t0 = (int)(g.start + (int64_t)j * BT);
+                    mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    for (int p = 0; p < kpan; ++p)
+                        tma_load_3d(sm.x[s] + p * kPanel, &tx, &sm.full[s], p * 64, h, t0);
+                    for (int p = 0; p < DV / 64; ++p)
+                        tma_load_3d(sm.y[s] + p * kPanel, &ty, &sm.full[s], j0 + p * 64, h, t0);
                 }
-                const int j = BWD ? i : nblk - 1 - i;
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(&sm.empty[s], ((i / kStages) - 1) & 1, kWaitNs)) {
-                    ok = false;
-                    break;
-                }
-                const int t0 = (int)(g.start + (int64_t)j * BT);
-                mbar_arrive_expect_tx(&sm.full[s], bytes);
-                for (int p = 0; p < kpan; ++p)
-                    tma_load_3d(sm.x[s] + p * kPanel, &tx, &sm.full[s], p * 64, h, t0);
-                for (int p = 0; p < DV / 64; ++p)
-                    tma_load_3d(sm.y[s] + p * kPanel, &ty, &sm.full[s], j0 + p * 64, h, t0);
-                last[s] = i;
             }
             if (!ok) {
                 *abort_flag = 1;
                 set_status(st, BDLA_ERR_TIMEOUT, 21u);
-                for (int s = 0; s < kStages; ++s)
-                    if (last[s] >= 0)
-                        mbar_wait(&sm.full[s], (last[s] / kStages) & 1, kWaitNs);
             }
+            // the copies this thread started have landed before the CTA exits
+            for (int64_t b = gb - kStages < 0 ? 0 : gb - kStages; b < gb; ++b)
+                mbar_wait(&sm.full[b % kStages], (b / kStages) & 1, kWaitNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t id = idesc_bf16_f32(128, DV, true, true);   // [dk x dv] += X^T Y
+            int64_t gb = 0, la = 0;   // blocks consumed, items accumulated
             bool ok = true;
-            for (int i = 0; i < nblk; ++i) {
-                const int s = i % kStages;
-                if (*abort_flag || !mbar_wait(&sm.xready[s], (i / kStages) & 1, kWaitNs)) {
+            for (int64_t i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+                int slot, h, j0;
+                SegSpan g;
+                const int nblk = item(i, slot, h, j0, g);
+                if (nblk <= 0)
+                    continue;
+                const int a = (int)(la & 1);
+                if (la >= 2 && !mbar_wait(&sm.acc_free[a], ((la / 2) - 1) & 1, kWaitNs)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t sx = smem_u32(sm.x[s]), sy = smem_u32(sm.y[s]);
-                for (int ks = 0; ks < BT / 16; ++ks)
-                    umma_bf16(tmem, sdesc_sw128(sx + ks * 2048, kPanel, 1024),
-                              sdesc_sw128(sy + ks * 2048, kPanel, 1024), id, (i > 0 || ks > 0) ? 1 : 0);
-                umma_commit(&sm.empty[s]);
+                for (int b = 0; b < nblk; ++b, ++gb) {
+                    const int s = (int)(gb % kStages);
+                    if (*abort_flag || !mbar_wait(&sm.xready[s], (gb / kStages) & 1, kWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sx = smem_u32(sm.x[s]), sy = smem_u32(sm.y[s]);
+                    for (int ks = 0; ks < BT / 16; ++ks)
+                        umma_bf16(tmem + a * DV, sdesc_sw128(sx + ks * 2048, kPanel, 1024),
+                                  sdesc_sw128(sy + ks * 2048, kPanel, 1024), id, (b > 0 || ks > 0) ? 1 : 0);
+                    umma_commit(&sm.empty[s]);
+                }
+                if (!ok)
+                    break;
+                umma_commit(&sm.acc_full[a]);
+                ++la;
             }
             if (!ok) {
                 *abort_flag = 1;
                 set_status(st, BDLA_ERR_TIMEOUT, 22u);
             }
-            if (nblk > 0) {
-                // every MMA issued above completes before TMEM is read or released
-                umma_commit(&sm.done);
-                mbar_wait(&sm.done, 0, kWaitNs);
+            // every MMA issued above completes before TMEM is released
+            umma_commit(&sm.drain);
+            mbar_wait(&sm.drain, 0, kWaitNs);
+        }
+    } else if (warp < 6) {
+        // ---------------------------------------------------------------- row warps
+        const int r = 32 * (warp & 3) + lane;   // token row of the block
+        int64_t gb = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+            int slot, h, j0;
+            SegSpan g;
+            const int nblk = item(i, slot, h, j0, g);
+            if (nblk < 0)
+                continue;
+            float run = 0.0f;   // summed log-decay of the blocks already taken
+            for (int b = 0; b < nblk; ++b, ++gb) {
+                const int j = BWD ? b : nblk - 1 - b;
+                const int s = (int)(gb % kStages);
+                const int Lb = (int)(g.len - (int64_t)j * BT < BT ? g.len - (int64_t)j * BT : BT);
+                const bool valid = r < Lb;
+                const int tau = r >> 4;
+                const float gv = valid ? gamma[(int64_t)h * tokens + g.start + (int64_t)j * BT + r] : 0.0f;
+                const int lastr = min(16 * tau + 15, Lb - 1);
+                const float g_last = __shfl_sync(0xffffffffu, gv, lastr & 31);
+                row_sync();   // every row has read the previous block's tile totals
+                if ((r & 15) == 0)
+                    sm.gam[tau] = (16 * tau < Lb) ? g_last : 0.0f;
+                row_sync();
+                float Gt = 0.0f, lend = 0.0f;
+#pragma unroll
+                for (int u = 0; u < BT / kChunk; ++u) {
+                    Gt += (u < tau) ? sm.gam[u] : 0.0f;
+                    lend += sm.gam[u];
+                }
+                const float lam = Gt + gv;   // inclusive cumulative log-decay inside the block
+                const float c = BWD ? run + lam : run + (lend - lam);
+                const float w = valid ? expf(c) : 0.0f;
+                run += lend;
+                ok = row_all(mbar_wait(&sm.full[s], (gb / kStages) & 1, kWaitNs)) && !*abort_flag;
+                if (!ok)
+                    break;
+#pragma unroll 1
+                for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        uint4 *xa = reinterpret_cast<uint4 *>(sm.x[s] + p * kPanel + sw128_offset(r, c8));
+                        *xa = scale_row8(*xa, w);
+                    }
+                fence_proxy_async_smem();
+                mbar_arrive(&sm.xready[s]);
             }
+            if (ok && r == 0 && j0 == 0)
+                lsum[(size_t)slot * H + h] = run;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0)
+                set_status(st, BDLA_ERR_TIMEOUT, 23u);
         }
     } else {
-        // ---------------------------------------------------------------- row warps
+        // ---------------------------------------------------------------- sum writers
         const int q4 = warp & 3;               // TMEM lane quarter this warp may access
-        const int r = 32 * q4 + lane;
+        const int r = 32 * q4 + lane;          // key row of the sums
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        float run = 0.0f;   // summed log-decay of the blocks already taken
+        int64_t la = 0;
         bool ok = true;
-        for (int i = 0; i < nblk; ++i) {
-            const int j = BWD ? i : nblk - 1 - i;
-            const int s = i % kStages;
-            const int Lb = (int)(g.len - (int64_t)j * BT < BT ? g.len - (int64_t)j * BT : BT);
-            const bool valid = r < Lb;
-            const int tau = r >> 4;
-            const float gv = valid ? gamma[(int64_t)h * tokens + g.start + (int64_t)j * BT + r] : 0.0f;
-            const int lastr = min(16 * tau + 15, Lb - 1);
-            const float g_last = __shfl_sync(0xffffffffu, gv, lastr & 31);
-            row_sync();   // every row has read the previous block's tile totals
-            if ((r & 15) == 0)
-                sm.gam[tau] = (16 * tau < Lb) ? g_last : 0.0f;
-            row_sync();
-            float Gt = 0.0f, lend = 0.0f;
-#pragma unroll
-            for (int u = 0; u < BT / kChunk; ++u) {
-                Gt += (u < tau) ? sm.gam[u] : 0.0f;
-                lend += sm.gam[u];
-            }
-            const float lam = Gt + gv;   // inclusive cumulative log-decay inside the block
-            const float c = BWD ? run + lam : run + (lend - lam);
-            const float w = valid ? expf(c) : 0.0f;
-            run += lend;
-            ok = row_all(mbar_wait(&sm.full[s], (i / kStages) & 1, kWaitNs)) && !*abort_flag;
-            if (!ok)
-                break;
-#pragma unroll 1
-            for (int p = 0; p < kpan; ++p)
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint4 *a = reinterpret_cast<uint4 *>(sm.x[s] + p * kPanel + sw128_offset(r, c8));
-                    *a = scale_row8(*a, w);
-                }
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.xready[s]);
-        }
-        if (ok && nblk > 0)
-            ok = row_all(mbar_wait(&sm.done, 0, kWaitNs)) && !*abort_flag;
-        if (ok) {
-            tc_fence_after();
+        for (int64_t i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+            int slot, h, j0;
+            SegSpan g;
+            const int nblk = item(i, slot, h, j0, g);
+            if (nblk < 0)
+                continue;
             const size_t base = ((size_t)slot * H + h) * (size_t)dk * dv;
+            const int a = (int)(la & 1);
+            if (nblk > 0) {
+                if (!mbar_wait(&sm.acc_full[a], (la / 2) & 1, kWaitNs) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
             if (r < dk) {
 #pragma unroll 1
                 for (int c = 0; c < DV / 32; ++c) {
                     uint32_t x[32];
                     if (nblk > 0) {
-                        tmem_ld32(tmem + lane_off + c * 32, x);
+                        tmem_ld32(tmem + a * DV + lane_off + c * 32, x);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
@@ -262,19 +317,23 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
                         dst[k4] = make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
                 }
             }
-            if (r == 0 && blockIdx.x == 0)
-                lsum[(size_t)slot * H + h] = run;
-        } else {
+            if (nblk > 0) {
+                tc_fence_before();
+                mbar_arrive(&sm.acc_free[a]);
+                ++la;
+            }
+        }
+        if (!ok) {
             *abort_flag = 1;
             if (lane == 0)
-                set_status(st, BDLA_ERR_TIMEOUT, 23u);
+                set_status(st, BDLA_ERR_TIMEOUT, 24u);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
-        tmem_dealloc(tmem, DV);
+        tmem_dealloc(tmem, 2 * DV);
 }
 
 // One thread per 4 consecutive state entries of one (document, head); the
@@ -365,7 +424,9 @@ cudaError_t launch_seg_summary(const Problem &p, const __nv_bfloat16 *x, const _
     if (!make_token_map(&mx, x, p.dk, p.H, p.tokens) || !make_token_map(&my, y, p.dv, p.H, p.tokens))
         return cudaErrorInvalidValue;
     const int DVs = p.dv >= 128 ? 128 : 64;
-    dim3 grid(p.dv / DVs, p.H, (unsigned)seg.n_slots);
+    const int64_t n_items = (int64_t)(p.dv / DVs) * p.H * seg.n_slots;
+    const int64_t n_cta = n_items < sm_count() ? n_items : sm_count();
+    dim3 grid((unsigned)n_cta);
     cudaError_t err;
 #define BDLA_SEG_GO(DV_, B_)                                                                       \
     do {                                                                                           \
@@ -375,8 +436,8 @@ cudaError_t launch_seg_summary(const Problem &p, const __nv_bfloat16 *x, const _
                                         (int)smem)) != cudaSuccess)                                \
             return err;                                                                            \
         kern<<<grid, kSegThreads, smem, p.stream>>>(mx, my, gamma, p.cu, p.T, p.tokens, p.n_docs, \
-                                                    p.H, p.dk, p.dv, seg.seg_blk, seg.buf,         \
-                                                    seg.lsum, p.st);                               \
+                                                    p.H, p.dk, p.dv, seg.seg_blk, n_items,         \
+                                                    seg.buf, seg.lsum, p.st);                      \
     } while (0)
     if (DVs == 64) {
         if (backward)
