@@ -22,10 +22,11 @@
 // Phases of one block (MMA warp <-> eight epilogue warps, two per TMEM lane
 // quarter splitting the columns):
 //   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
-//   EA  P (smem) and dP (registers), W sums, V -> V o w_s, E -> bf16 copy;
+//   EA  P (smem) and dP (registers), W sums, E -> bf16 copy;
 //       then, while Mb runs, E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
-//   Mb  C2 = P^T dO, C1 = (V o w_s) E^T
-//   Eb  k . dk_inter, dP -> smem; then, while Md runs, dO -> e^{Lam} o dO
+//   Mb  C2 = P^T dO, C1 = V E^T
+//   Eb  C1 <- w_s o C1, k . dk_inter, dP -> smem; then, while Md runs,
+//       dO -> e^{Lam} o dO
 //   Md  C1 += dP^T Q, C3 += dP K
 //   Ee  K -> K o w_s in place
 //   Mf  C2 += (K o w_s) E, E += Q^T (e^{Lam} o dO)
@@ -886,14 +887,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 sm.colsum[q4][c * 32 + lane] = cs;
             }
             sm.rowpart[half][r] = rowsum;
-            // V -> V o w_s in place
-#pragma unroll
-            for (int p = 0; p < DV / 64; ++p)
-#pragma unroll
-                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
-                    uint4 *va = reinterpret_cast<uint4 *>(sm.v + p * kPanel + sw128_offset(r, c8));
-                    *va = scale_bf16x8(*va, wsc);
-                }
             // E -> bf16 copy (z)
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
@@ -956,7 +949,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             sm.ypart[half][r] = yv;
             tmem_st_wait();   // visible to Md and Mf through the fence before eb_done
 
-            // ---- Eb: k . dk_inter, then dP -> smem
+            // ---- Eb: C1 <- w_s o C1 (the inter-block part of dk), k . dk_inter,
+            //      then dP -> smem
             ok = epi_all(mbar_wait(&sm.mb_done, par, kWaitNs)) && !*abort_flag;
             if (!ok)
                 break;
@@ -978,8 +972,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         kd = fmaf(bf16_hi(w[i]), __uint_as_float(x[8 * k4 + 2 * i + 1]), kd);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[i] = __float_as_uint(__uint_as_float(x[i]) * wsc);
+                tmem_st32(t_c1 + lane_off + c * 32, x);
             }
-            sm.kdpart[half][r] = kd;
+            sm.kdpart[half][r] = kd * wsc;
 #pragma unroll
             for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
                 const int cc = c >> 1;
@@ -990,6 +988,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         make_uint4(dpk[cc * 16 + 4 * k4], dpk[cc * 16 + 4 * k4 + 1],
                                    dpk[cc * 16 + 4 * k4 + 2], dpk[cc * 16 + 4 * k4 + 3]);
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.eb_done);
