@@ -17,16 +17,20 @@
 //   dlam_r = sum_{u<r} X_u + sum_{t>=r} Y_t + e^{Lam_end} <S_in, E>
 //   X_u = sum_{t>u} W_tu - sum_{s<u} W_us + k_u . dk_inter_u,   Y_t = q_t . dq_inter_t
 //   da = dlam * d lambda / d a.
+// P is causal, so the column sums come from the P^T dO GEMM:
+//   sum_{t>=u} W_tu = v_u . (P^T dO)_u,   X_u = v_u . (P^T dO)_u - sum_{s<=u} W_us + k_u . dk_inter_u
+// (the diagonal term cancels).  The row sums take the same bf16 P as that GEMM,
+// so every pair inside the block cancels exactly in the prefix sums.
 // S_in (the state before the block) comes from forward checkpoints.
 //
 // Phases of one block (MMA warp <-> eight epilogue warps, two per TMEM lane
 // quarter splitting the columns):
 //   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
-//   EA  P (smem) and dP (registers), W sums, E -> bf16 copy;
+//   EA  P (smem) and dP (registers), W row sums, E -> bf16 copy;
 //       then, while Mb runs, E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
 //   Mb  C2 = P^T dO, C1 = V E^T
 //   Eb  C1 <- w_s o C1, k . dk_inter, dP -> smem; then, while Md runs,
-//       dO -> e^{Lam} o dO
+//       dO -> e^{Lam} o dO and the W column sums v . (P^T dO)
 //   Md  C1 += dP^T Q, C3 += dP K
 //   Ee  K -> K o w_s in place
 //   Mf  C2 += (K o w_s) E, E += Q^T (e^{Lam} o dO)
@@ -89,8 +93,9 @@ struct BwdSmem {
     alignas(1024) unsigned char x[2 * kPanel];           // P, then dP: rows t, panels s
     float cdiag[BT];
     float coff[BT];
-    float colsum[4][BT];
-    float rowpart[2][BT];   // per column half: sum_{s<t} W_ts, k.dk_inter, q.dq_inter
+    // per row and column half: v_s . (P^T dO)_s, sum_{s<=t} W_ts, k.dk_inter, q.dq_inter
+    float colpart[2][BT];
+    float rowpart[2][BT];
     float kdpart[2][BT];
     float ypart[2][BT];
     float scan[2][4];
@@ -153,20 +158,12 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// Sum over the warp of 32 per-lane values; lane l ends with the total of value l.
-__device__ __forceinline__ float warp_reduce_scatter32(float (&vals)[32], int lane)
+// fp32 -> nearest bf16 -> fp32
+__device__ __forceinline__ float bf16_round(float x)
 {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < off; ++i) {
-            const float send = upper ? vals[i] : vals[i + off];
-            const float keep = upper ? vals[i + off] : vals[i];
-            vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-    return vals[0];
+    unsigned short h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+    return __uint_as_float((uint32_t)h << 16);
 }
 
 // Exclusive prefix sum over the 128 epilogue rows (row = 32 * q4 + lane).
@@ -657,11 +654,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
             // decay gradient of the block (both halves compute it; half 0 stores)
-            float col = 0.0f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                col += sm.colsum[w][r];
-            const float X = col - (sm.rowpart[0][r] + sm.rowpart[1][r]) + (sm.kdpart[0][r] + sm.kdpart[1][r]);
+            const float X = (sm.colpart[0][r] + sm.colpart[1][r]) - (sm.rowpart[0][r] + sm.rowpart[1][r]) +
+                            (sm.kdpart[0][r] + sm.kdpart[1][r]);
             const float Yv = sm.ypart[0][r] + sm.ypart[1][r];
             float tx, ty;
             const float px = block_exclusive_scan(X, sm.scan[0], q4, lane, tx);
@@ -826,7 +820,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
                 const int cc = c >> 1;   // this half's chunk index 0..1
-                float pv[32], wv[32];
+                float pv[32];   // bf16-rounded: the P the GEMMs and the row sums use
                 uint32_t dpu[32];
                 if (c <= q4) {
                     uint32_t xs[32], xa[32];
@@ -856,10 +850,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                 p = (col <= r) ? sm.dgp[r][col & 15] : 0.0f;
                                 dp = (col <= r) ? sm.dgd[r][col & 15] : 0.0f;
                             }
-                            pv[i] = p;
-                            const float wt = (col < r) ? p * av : 0.0f;
-                            wv[i] = wt;
-                            rowsum += wt;
+                            pv[i] = bf16_round(p);
+                            rowsum = fmaf(pv[i], av, rowsum);   // p = 0 past the diagonal
                             dpu[i] = __float_as_uint(dp);
                         }
                     }
@@ -867,7 +859,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         pv[i] = 0.0f;
-                        wv[i] = 0.0f;
                         dpu[i] = 0u;
                     }
                 }
@@ -883,8 +874,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int k4 = 0; k4 < 4; ++k4)
                     *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
                         make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
-                const float cs = warp_reduce_scatter32(wv, lane);
-                sm.colsum[q4][c * 32 + lane] = cs;
             }
             sm.rowpart[half][r] = rowsum;
             // E -> bf16 copy (z)
@@ -1000,6 +989,28 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     uint4 *oa = reinterpret_cast<uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
                     *oa = scale_bf16x8(*oa, qsc);
                 }
+            // and the column sums of W: v_s . (P^T dO)_s (C2 and V stay untouched until Mf)
+            {
+                float vc = 0.0f;
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                    uint32_t x[32];
+                    tmem_ld32(t_c2 + lane_off + c * 32, x);
+                    tmem_ld_wait();
+                    const unsigned char *vp = sm.v + (c >> 1) * kPanel;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const uint4 vv = *reinterpret_cast<const uint4 *>(vp + sw128_offset(r, (c & 1) * 4 + k4));
+                        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            vc = fmaf(bf16_lo(w[i]), __uint_as_float(x[8 * k4 + 2 * i]), vc);
+                            vc = fmaf(bf16_hi(w[i]), __uint_as_float(x[8 * k4 + 2 * i + 1]), vc);
+                        }
+                    }
+                }
+                sm.colpart[half][r] = vc;
+            }
 
             // ---- Ee: K -> K o w_s in place
             ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;

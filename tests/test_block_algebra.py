@@ -150,3 +150,32 @@ def test_two_level_factors_never_exceed_the_tile_reciprocal():
         for sig in range(tau):
             assert G[tau] - G[sig + 1] <= 0.0
             assert np.all(gam[sig] - Gam[sig * C:(sig + 1) * C] <= 1e-12)
+
+
+@pytest.mark.parametrize("L", [128, 77])
+def test_column_sums_of_w_from_the_pdo_gemm(L):
+    """The backward takes the column sums of W = P o dA from the P^T dO GEMM:
+    P is causal, so sum_{t>=u} W_tu = v_u . (P^T dO)_u, and
+      X_u = v_u . (P^T dO)_u - sum_{s<=u} W_us + k_u . dk_inter_u
+    equals the pair-sum form (the diagonal W_uu enters both terms).  The same
+    P on both sides (the kernel's bf16 P) keeps every pair inside the block
+    cancelling in the prefix sums: sum_{u<r} X_u is then the sum over the
+    pairs that cross r, for any P, rounded or not."""
+    rng = np.random.default_rng(L)
+    dk, dv = 8, 6
+    Q, K = rng.standard_normal((L, dk)) * 0.4, rng.standard_normal((L, dk)) * 0.4
+    V, G = rng.standard_normal((L, dv)), rng.standard_normal((L, dv))
+    E = rng.standard_normal((dk, dv)) * 0.3
+    lam = _lam(rng.standard_normal(L), -5.0, oracle.BOUNDED)
+    Wd, Lam, Lend = block_weights(lam)
+    dA = G @ V.T
+    kd = np.einsum("ud,ud->u", K, np.exp(Lend - Lam)[:, None] * (V @ E.T))
+    for P in (Wd * (Q @ K.T), np.tril(rng.standard_normal((L, L)))):   # exact, and any causal P
+        Wp = np.tril(P * dA, -1)
+        X_pairs = Wp.sum(axis=0) - Wp.sum(axis=1) + kd
+        X_gemm = np.einsum("ud,ud->u", V, P.T @ G) - np.tril(P * dA).sum(axis=1) + kd
+        np.testing.assert_allclose(X_gemm, X_pairs, rtol=1e-10, atol=1e-10)
+        W = np.tril(P * dA)
+        prefix = np.concatenate([[0.0], np.cumsum(X_gemm - kd)[:-1]])
+        crossing = np.array([W[r:, :r].sum() for r in range(L)])
+        np.testing.assert_allclose(prefix, crossing, rtol=1e-10, atol=1e-9)
