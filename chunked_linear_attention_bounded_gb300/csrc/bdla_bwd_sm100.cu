@@ -30,9 +30,10 @@
 //       then, while Mb runs, E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
 //   Mb  C2 = P^T dO, C1 = V E^T
 //   Eb  C1 <- w_s o C1, k . dk_inter, dP -> smem; then, while Md runs,
-//       dO -> e^{Lam} o dO and the W column sums v . (P^T dO)
+//       dO -> e^{Lam} o dO, the W column sums v . (P^T dO) and K o w_s into
+//       V's tile (V is not read again in the block; when dv < dk it does
+//       not hold K, and K is scaled in place once Md has read it)
 //   Md  C1 += dP^T Q, C3 += dP K
-//   Ee  K -> K o w_s in place
 //   Mf  C2 += (K o w_s) E, E += Q^T (e^{Lam} o dO)
 //   Eg  dq = C3, dk = C1, dv = C2, da      (overlaps the next block's loads)
 #include <cudaTypedefs.h>
@@ -293,6 +294,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     }
     const int nblk = (int)((d.len + BT - 1) / BT);
     const int kpan = dk / 64;
+    // Mf reads K o w_s from V's tile when that tile has room for K
+    const bool khat_v = DV / 64 >= kpan;
     const size_t sstride = (size_t)dk * dv;
     const int64_t unit = (int64_t)n * H + h;
     const float *einit = seg_blk > 0 ? seg_init : dhT;
@@ -454,7 +457,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks)
-                    umma_bf16(t_c2, kmaj(sk, ks), mnmaj(sz, ks), id_ke, 1);
+                    umma_bf16(t_c2, kmaj(khat_v ? sv : sk, ks), mnmaj(sz, ks), id_ke, 1);
                 for (int ks = 0; ks < BT / 16; ++ks)
                     umma_bf16(t_e, mnmaj(sq, ks), mnmaj(sdo, ks), id_qdo, 1);
                 umma_commit(&sm.mf_done);
@@ -1012,18 +1015,30 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 sm.colpart[half][r] = vc;
             }
 
-            // ---- Ee: K -> K o w_s in place
-            ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;
-            if (!ok)
-                break;
-            tc_fence_after();
+            if (khat_v) {
+                // K o w_s for Mf into V's tile: this thread has read its part of
+                // V row r above and writes only that part; Md reads K, not V
 #pragma unroll 1
-            for (int p = 0; p < kpan; ++p)
+                for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
-                    uint4 *ka = reinterpret_cast<uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
-                    *ka = scale_bf16x8(*ka, wsc);
-                }
+                    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
+                        const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
+                        *reinterpret_cast<uint4 *>(sm.v + p * kPanel + sw128_offset(r, c8)) = scale_bf16x8(kk, wsc);
+                    }
+            } else {
+                // ---- Ee: K -> K o w_s in place once Md has read K
+                ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;
+                if (!ok)
+                    break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int p = 0; p < kpan; ++p)
+#pragma unroll
+                    for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
+                        uint4 *ka = reinterpret_cast<uint4 *>(sm.k + p * kPanel + sw128_offset(r, c8));
+                        *ka = scale_bf16x8(*ka, wsc);
+                    }
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.ee_done);
