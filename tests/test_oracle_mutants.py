@@ -1,0 +1,93 @@
+"""Planted mistakes: the oracle's pins must catch each one.
+
+Each case copies the ``oracle`` package into a temporary directory, plants one
+plausible slip in the copy of ``bdla_oracle.c`` (a wrong sign, a dropped term,
+a wrong operand, the decay applied after instead of before the update, a wrong
+gate derivative, an adjoint that is not decayed, a checkpoint window read from
+the wrong place, an ignored initial state), and runs ``test_oracle_pins.py``
+against the copy in a fresh interpreter.  The pins pass on an unmodified copy
+and fail on every mutant.  The committed oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+# (name, text in bdla_oracle.c, replacement): each text occurs exactly once
+MUTANTS = [
+    ("sigmoid of -a", "return b / (1.0 + exp(-a));", "return b / (1.0 + exp(a));"),
+    ("softplus term subtracted", "return -(fmax(a, 0.0) + log1p(exp(-fabs(a))));",
+     "return -(fmax(a, 0.0) - log1p(exp(-fabs(a))));"),
+    ("gate derivative without (1 - s)", "return b * s * (1.0 - s);", "return b * s;"),
+    ("decay applied after the update", "Si[j] = g * Si[j] + ki * vt[j];",
+     "Si[j] = g * (Si[j] + ki * vt[j]);"),
+    ("output reads k instead of q", "const double qi = qt[i];", "const double qi = kt[i];"),
+    ("initial state ignored in the forward",
+     "memcpy(S, h0 + (size_t)u * ssz, ssz * sizeof(double));\n"
+     "            else\n"
+     "                memset(S, 0, ssz * sizeof(double));\n"
+     "            for (int64_t t = cu[n];",
+     "memset(S, 0, ssz * sizeof(double));\n"
+     "            else\n"
+     "                memset(S, 0, ssz * sizeof(double));\n"
+     "            for (int64_t t = cu[n];"),
+    ("dq drops the current token", "acc += (g * Sp[(size_t)i * dv + j] + kt[i] * vt[j]) * gt[j];",
+     "acc += g * Sp[(size_t)i * dv + j] * gt[j];"),
+    ("dq with an undecayed previous state", "acc += (g * Sp[(size_t)i * dv + j] + kt[i] * vt[j]) * gt[j];",
+     "acc += (Sp[(size_t)i * dv + j] + kt[i] * vt[j]) * gt[j];"),
+    ("dk reads dO instead of v", "acc += D[(size_t)i * dv + j] * vt[j];",
+     "acc += D[(size_t)i * dv + j] * gt[j];"),
+    ("dv reads q instead of k", "dvt[j] += D[(size_t)i * dv + j] * kt[i];",
+     "dvt[j] += D[(size_t)i * dv + j] * qt[i];"),
+    ("da without the gate factor g", "da[tt * H + h] = g * dot * log_decay_deriv(at, b, mode);",
+     "da[tt * H + h] = dot * log_decay_deriv(at, b, mode);"),
+    ("adjoint not decayed", "D[e] *= g;", "D[e] *= 1.0;"),
+    ("every window restarts from the first checkpoint",
+     "memcpy(S, ck + (size_t)w * ssz, ssz * sizeof(double));", "memcpy(S, ck, ssz * sizeof(double));"),
+]
+
+
+def _copy_oracle(dst, mutation=None):
+    pkg = os.path.join(dst, "oracle")
+    os.makedirs(pkg)
+    shutil.copy(os.path.join(ROOT, "oracle", "__init__.py"), pkg)
+    with open(os.path.join(ROOT, "oracle", "bdla_oracle.c")) as f:
+        src = f.read()
+    if mutation is not None:
+        old, new = mutation
+        assert src.count(old) == 1, f"mutation site not unique or gone: {old!r}"
+        src = src.replace(old, new)
+    with open(os.path.join(pkg, "bdla_oracle.c"), "w") as f:
+        f.write(src)
+
+
+def _run_pins(cwd):
+    """The pins in a fresh interpreter whose `import oracle` finds the copy in
+    cwd (no conftest, so the repository root is not put ahead of it)."""
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    env.pop("PYTHONPATH", None)
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "--noconftest", "-p", "no:cacheprovider",
+                           PINS], cwd=cwd, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_unmodified_copy_passes_the_pins(tmp_path):
+    _copy_oracle(str(tmp_path))
+    where = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__)"], cwd=str(tmp_path),
+                           capture_output=True, text=True, timeout=120)
+    assert where.stdout.strip().startswith(str(tmp_path)), where.stdout + where.stderr
+    r = _run_pins(str(tmp_path))
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    _copy_oracle(str(tmp_path), (old, new))
+    r = _run_pins(str(tmp_path))
+    # 1 = some pin failed (not a crash, not a collection error)
+    assert r.returncode == 1, f"{name}: pins returned {r.returncode}\n" + r.stdout[-3000:] + r.stderr[-2000:]
+    assert " failed" in r.stdout, r.stdout[-3000:]
