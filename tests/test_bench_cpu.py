@@ -27,3 +27,23 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "varlen64k"
     assert d["gpu_launches"] == 0
+
+
+def test_algorithmic_bytes_of_the_measured_workload():
+    """The roofline numerator, counted by hand for the packed 64K workload
+    (65536 tokens x 32 heads, dk = dv = 128, 8 documents with h0):
+    forward q, k, v, o bf16 (2 B each) + a fp32 per (token, head), plus h0 in
+    and hT out per (document, head); backward q, k, v, dO bf16 and a in, dq,
+    dk, dv, da fp32 out, plus h0 per (document, head)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS
+    w = WORKLOADS["varlen64k"]
+    th, units, state = 65536 * 32, 8 * 32, 128 * 128 * 4
+    per_fwd = 2 * 128 * 4 + 4               # q, k, v, o at 2 B + a
+    per_bwd = 2 * 128 * 4 + 4 + 4 * 128 * 3 + 4   # q, k, v, dO in + a; dq, dk, dv, da out
+    assert (per_fwd, per_bwd) == (1028, 2568)
+    got = bench.algorithmic_bytes(w, 8)
+    assert got["fwd"] == th * per_fwd + 2 * units * state
+    assert got["bwd"] == th * per_bwd + units * state
+    assert got["bwd"] == 5402263552
