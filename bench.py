@@ -313,7 +313,7 @@ def ours_arm(args, w, inp):
     for _ in range(max(3, args.warmup)):
         step(g)
     torch.cuda.synchronize()
-    for code in (ws_f.read_status(), ws_b.read_status()):
+    for code in (ws_f.read_device_status(), ws_b.read_device_status()):
         if code:
             raise RuntimeError(f"device status {code} after warm-up")
 
@@ -417,7 +417,7 @@ def ours_arm(args, w, inp):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = replicas.max_over_ranks(f0.elapsed_time(f1) / K, world, dev)
-    for code in (ws_f.read_status(), ws_b.read_status()):
+    for code in (ws_f.read_device_status(), ws_b.read_device_status()):
         if code:
             raise RuntimeError(f"device status {code} after the timed steps")
 

@@ -22,15 +22,20 @@ SOFTPLUS = 1   # BDLA_DECAY_NEG_SOFTPLUS:    log g = -softplus(a)   (ablation)
 CHUNK = 16
 OP_FWD, OP_BWD, OP_DECAY = 0, 1, 2
 
-STATUS_NAMES = {0: "BDLA_OK", 1: "BDLA_ERR_NULL", 2: "BDLA_ERR_SHAPE", 3: "BDLA_ERR_ALIGN",
-                4: "BDLA_ERR_RANGE", 5: "BDLA_ERR_UNSUPPORTED", 6: "BDLA_ERR_WORKSPACE",
-                7: "BDLA_ERR_CUDA", 8: "BDLA_ERR_TIMEOUT", 9: "BDLA_ERR_DEVICE",
-                10: "BDLA_ERR_TOO_LARGE"}
+# bdla_status values (include/bdla.h)
+OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_RANGE, ERR_UNSUPPORTED = 0, 1, 2, 3, 4, 5, 6
+ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE, ERR_TOO_LARGE = 7, 8, 9, 10, 11
+STATUS_NAMES = {OK: "BDLA_OK", ERR_NULL: "BDLA_ERR_NULL", ERR_SHAPE: "BDLA_ERR_SHAPE",
+                ERR_DTYPE: "BDLA_ERR_DTYPE", ERR_ALIGN: "BDLA_ERR_ALIGN", ERR_RANGE: "BDLA_ERR_RANGE",
+                ERR_UNSUPPORTED: "BDLA_ERR_UNSUPPORTED", ERR_WORKSPACE: "BDLA_ERR_WORKSPACE",
+                ERR_CUDA: "BDLA_ERR_CUDA", ERR_TIMEOUT: "BDLA_ERR_TIMEOUT", ERR_DEVICE: "BDLA_ERR_DEVICE",
+                ERR_TOO_LARGE: "BDLA_ERR_TOO_LARGE"}
 
-# Every symbol include/bdla.h declares.
+# Every symbol include/*.h declares.
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
-           "bdla_bwd_varlen", "bdla_read_status", "bdla_status_string", "bdla_version",
-           "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_set_seq_split", "bdla_decode")
+           "bdla_bwd_varlen", "bdla_read_device_status", "bdla_status_string", "bdla_version",
+           "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
+           "bdla_set_seq_split", "bdla_decode")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 
 
@@ -69,9 +74,10 @@ def lib():
         L.bdla_bwd_varlen.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, ci, ci, vp, vp, vp,
                                       vp, vp, Dims, ci, vp, sz, vp]
         for name in ("bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd", "bdla_bwd_varlen",
-                     "bdla_read_status"):
+                     "bdla_read_device_status", "bdla_noalloc_read_status"):
             getattr(L, name).restype = ci
-        L.bdla_read_status.argtypes = [vp, vp]
+        L.bdla_read_device_status.argtypes = [vp, vp]
+        L.bdla_noalloc_read_status.argtypes = [vp]
         L.bdla_status_string.argtypes = [ci]
         L.bdla_status_string.restype = ctypes.c_char_p
         L.bdla_version.restype = ci
@@ -175,8 +181,8 @@ class Workspace:
     def ptr(self):
         return ctypes.c_void_p(self.buf.data_ptr())
 
-    def read_status(self, stream=None) -> int:
-        return int(lib().bdla_read_status(self.ptr, _stream_handle(stream)))
+    def read_device_status(self, stream=None) -> int:
+        return int(lib().bdla_read_device_status(self.ptr, _stream_handle(stream)))
 
 
 def workspace_bytes(op: int, q_shape, dv: int, n_docs: int = 0, mode: int = BOUNDED,
@@ -188,7 +194,7 @@ def workspace_bytes(op: int, q_shape, dv: int, n_docs: int = 0, mode: int = BOUN
 def _ws_for(op, q, v, n_docs, mode, ckpt_stride, ws: Optional[Workspace]) -> Workspace:
     need = workspace_bytes(op, tuple(q.shape), v.shape[-1], n_docs, mode, ckpt_stride)
     if need == 0:
-        raise BdlaError(2, "bdla_workspace_bytes")
+        raise BdlaError(ERR_SHAPE, "bdla_workspace_bytes")
     if ws is None:
         return Workspace(need, q.device)
     return ws.ensure(need)
@@ -226,7 +232,7 @@ def decode(q, k, v, a, state, b: float = -5.0, mode: int = BOUNDED, o_dtype=torc
     B, H, dk = q.shape
     dv = v.shape[-1]
     if tuple(state.shape) != (B, H, dk, dv) or tuple(a.shape) != (B, H):
-        raise BdlaError(2, "decode shapes")
+        raise BdlaError(ERR_SHAPE, "decode shapes")
     o = out if out is not None else torch.empty((B, H, dv), dtype=o_dtype, device=q.device)
     st = lib().bdla_decode(_p(q), _p(k), _p(v), _p(a), b, _p(state), _p(o), _dtype_code(o.dtype),
                            Dims(B, 1, H, dk, dv), mode, _stream_handle(stream))

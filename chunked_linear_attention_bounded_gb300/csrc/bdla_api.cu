@@ -10,7 +10,38 @@ using namespace bdla;
 
 namespace bdla {
 KernelEvents g_kernel_events[BDLA_KERNEL_COUNT];
+
+bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs)
+{
+    if (d.T < 0 || d.H < 1 || d.B < 1)
+        return BDLA_ERR_SHAPE;
+    if (varlen && (d.B != 1 || n_docs < 1))
+        return BDLA_ERR_SHAPE;
+    if ((varlen ? n_docs : d.B) > 65535)   // documents are a grid extent
+        return BDLA_ERR_UNSUPPORTED;
+    if (d.dk != 64 && d.dk != 128)
+        return BDLA_ERR_UNSUPPORTED;
+    if (d.dv != 64 && d.dv != 128 && d.dv != 256)
+        return BDLA_ERR_UNSUPPORTED;
+    return BDLA_OK;
 }
+
+bdla_status check_decay(float b, int chunk, int mode)
+{
+    if (chunk != kChunk)
+        return BDLA_ERR_UNSUPPORTED;
+    if (mode != BDLA_DECAY_BOUNDED_SIGMOID && mode != BDLA_DECAY_NEG_SOFTPLUS)
+        return BDLA_ERR_UNSUPPORTED;
+    if (mode == BDLA_DECAY_BOUNDED_SIGMOID) {
+        if (!isfinite(b) || b > 0.0f)
+            return BDLA_ERR_RANGE;
+        // the bound must keep e^{-Gamma} = e^{chunk |b|} representable
+        if ((double)chunk * fabs((double)b) > 80.0)
+            return BDLA_ERR_RANGE;
+    }
+    return BDLA_OK;
+}
+}  // namespace bdla
 
 namespace {
 
@@ -88,37 +119,6 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
     return L;
 }
 
-bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs)
-{
-    if (d.T < 0 || d.H < 1 || d.B < 1)
-        return BDLA_ERR_SHAPE;
-    if (varlen && (d.B != 1 || n_docs < 1))
-        return BDLA_ERR_SHAPE;
-    if ((varlen ? n_docs : d.B) > 65535)   // documents are a grid extent
-        return BDLA_ERR_UNSUPPORTED;
-    if (d.dk != 64 && d.dk != 128)
-        return BDLA_ERR_UNSUPPORTED;
-    if (d.dv != 64 && d.dv != 128 && d.dv != 256)
-        return BDLA_ERR_UNSUPPORTED;
-    return BDLA_OK;
-}
-
-bdla_status check_decay(float b, int chunk, int mode)
-{
-    if (chunk != kChunk)
-        return BDLA_ERR_UNSUPPORTED;
-    if (mode != BDLA_DECAY_BOUNDED_SIGMOID && mode != BDLA_DECAY_NEG_SOFTPLUS)
-        return BDLA_ERR_UNSUPPORTED;
-    if (mode == BDLA_DECAY_BOUNDED_SIGMOID) {
-        if (!isfinite(b) || b > 0.0f)
-            return BDLA_ERR_RANGE;
-        // the bound must keep e^{-Gamma} = e^{chunk |b|} representable
-        if ((double)chunk * fabs((double)b) > 80.0)
-            return BDLA_ERR_RANGE;
-    }
-    return BDLA_OK;
-}
-
 bdla_status check_ws(void *ws, size_t ws_bytes, size_t need)
 {
     if (ws == nullptr || ws_bytes < need || !aligned16(ws))
@@ -186,11 +186,11 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
         !aligned16(hT) || !aligned16(ckpt) || !aligned16(a))
         return BDLA_ERR_ALIGN;
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
-        return BDLA_ERR_UNSUPPORTED;
+        return BDLA_ERR_DTYPE;
     if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
         return BDLA_ERR_SHAPE;
     if (ckpt && ckpt_dtype != BDLA_F32 && ckpt_dtype != BDLA_BF16)
-        return BDLA_ERR_UNSUPPORTED;
+        return BDLA_ERR_DTYPE;
     if (ckpt && ckpt_dtype == BDLA_BF16 && ckpt_stride % kBlock != 0)
         return BDLA_ERR_UNSUPPORTED;
     const Layout L = layout(BDLA_OP_FWD, d, varlen ? n_docs : d.B, 0);
@@ -206,34 +206,39 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     const bool split_ckpt = ckpt && !fused_ckpt && kBlock % ckpt_stride == 0 && ckpt_dtype == BDLA_F32 &&
                             (int64_t)total_tokens(d) / kBlock + (varlen ? n_docs : d.B) < 65535;
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
-    mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
-    if (seg.order)
-        BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
-    mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    {
+        KernelMark mark_(BDLA_KERNEL_DECAY, p.stream);
+        BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
+        if (seg.order)
+            BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
+    }
     if (seg.seg_blk > 0) {
         // the state entering every segment
-        mark_start(BDLA_KERNEL_SEG, p.stream);
-        BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
-        BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
-        mark_stop(BDLA_KERNEL_SEG, p.stream);
+        {
+        KernelMark mark_(BDLA_KERNEL_SEG, p.stream);
+            BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
+            BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
+        }
     }
-    mark_start(BDLA_KERNEL_FWD, p.stream);
-    BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
-                               (fused_ckpt || split_ckpt) ? ckpt : nullptr, ckpt_dtype == BDLA_BF16,
-                               ckpt_stride, seg));
-    mark_stop(BDLA_KERNEL_FWD, p.stream);
+    {
+        KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
+        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
+                                   (fused_ckpt || split_ckpt) ? ckpt : nullptr, ckpt_dtype == BDLA_BF16,
+                                   ckpt_stride, seg));
+    }
     if (split_ckpt) {
         // the states inside each block, all blocks in parallel
-        mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_ckpt_expand(p, kb, vb, gamma, static_cast<float *>(ckpt), ckpt_stride));
-        mark_stop(BDLA_KERNEL_STATES, p.stream);
+        {
+        KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
+            BDLA_CUDA(launch_ckpt_expand(p, kb, vb, gamma, static_cast<float *>(ckpt), ckpt_stride));
+        }
     } else if (ckpt && !fused_ckpt) {
         // checkpoints inside the 128-token blocks: tile-serial state pass (fp32)
-        mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr,
-                                  static_cast<float *>(ckpt), ckpt_stride, seg));
-        mark_stop(BDLA_KERNEL_STATES, p.stream);
+        {
+        KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
+            BDLA_CUDA(launch_fwd_tile(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr,
+                                      static_cast<float *>(ckpt), ckpt_stride, seg));
+        }
     }
     return BDLA_OK;
 }
@@ -257,7 +262,7 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     if (ckpt && (ckpt_stride <= 0 || ckpt_stride % kChunk != 0))
         return BDLA_ERR_SHAPE;
     if (ckpt && ckpt_dtype != BDLA_F32 && ckpt_dtype != BDLA_BF16)
-        return BDLA_ERR_UNSUPPORTED;
+        return BDLA_ERR_DTYPE;
     const int stride = ckpt ? ckpt_stride : 0;
     const int ck_bf16 = ckpt && ckpt_dtype == BDLA_BF16;
     const Layout L = layout(BDLA_OP_BWD, d, varlen ? n_docs : d.B, stride);
@@ -271,40 +276,45 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const auto *dob = static_cast<const __nv_bfloat16 *>(dO);
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
-    mark_start(BDLA_KERNEL_DECAY, p.stream);
-    BDLA_CUDA(launch_decay(p, a, gamma, dfac));
-    if (seg.order)
-        BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
-    mark_stop(BDLA_KERNEL_DECAY, p.stream);
+    {
+        KernelMark mark_(BDLA_KERNEL_DECAY, p.stream);
+        BDLA_CUDA(launch_decay(p, a, gamma, dfac));
+        if (seg.order)
+            BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
+    }
     const void *states = ckpt;
     int st_bf16 = ck_bf16, st_stride = stride;
     if (!bwd_ckpt_usable(stride)) {
         void *stb = wsb + L.states;
         if (seg.seg_blk > 0) {
-            mark_start(BDLA_KERNEL_SEG, p.stream);
-            BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
-            BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
-            mark_stop(BDLA_KERNEL_SEG, p.stream);
+            {
+                KernelMark mark_(BDLA_KERNEL_SEG, p.stream);
+                BDLA_CUDA(launch_seg_summary(p, kb, vb, gamma, false, seg));
+                BDLA_CUDA(launch_seg_scan(p, h0, false, seg));
+            }
         }
-        mark_start(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock, seg));
-        mark_stop(BDLA_KERNEL_STATES, p.stream);
+        {
+        KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
+            BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock, seg));
+        }
         states = stb;
         st_bf16 = 1;
         st_stride = kBlock;
     }
     if (seg.seg_blk > 0) {
         // the adjoint entering every segment from its end
-        mark_start(BDLA_KERNEL_SEG, p.stream);
-        BDLA_CUDA(launch_seg_summary(p, qb, dob, gamma, true, seg));
-        BDLA_CUDA(launch_seg_scan(p, dhT, true, seg));
-        mark_stop(BDLA_KERNEL_SEG, p.stream);
+        {
+        KernelMark mark_(BDLA_KERNEL_SEG, p.stream);
+            BDLA_CUDA(launch_seg_summary(p, qb, dob, gamma, true, seg));
+            BDLA_CUDA(launch_seg_scan(p, dhT, true, seg));
+        }
     }
     float *part = L.part ? reinterpret_cast<float *>(wsb + L.part) : nullptr;
-    mark_start(BDLA_KERNEL_BWD, p.stream);
-    BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride, dhT, dq,
-                               dk, dv, da, dh0, part, seg));
-    mark_stop(BDLA_KERNEL_BWD, p.stream);
+    {
+        KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride, dhT, dq,
+                                   dk, dv, da, dh0, part, seg));
+    }
     return BDLA_OK;
 }
 
@@ -380,7 +390,7 @@ bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const f
                     ckpt_stride, ckpt_dtype, dq, dk, dv, da, dh0, d, mode, ws, ws_bytes, stream);
 }
 
-bdla_status bdla_read_status(void *ws, void *stream)
+bdla_status bdla_read_device_status(void *ws, void *stream)
 {
     if (ws == nullptr)
         return BDLA_ERR_WORKSPACE;
@@ -401,9 +411,10 @@ const char *bdla_status_string(bdla_status s)
     case BDLA_OK: return "ok";
     case BDLA_ERR_NULL: return "a required pointer is NULL";
     case BDLA_ERR_SHAPE: return "a size is negative or inconsistent";
+    case BDLA_ERR_DTYPE: return "an output or checkpoint dtype is not BDLA_BF16 or BDLA_F32";
     case BDLA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case BDLA_ERR_RANGE: return "decay bound out of range (b > 0, not finite, or chunk*|b| > 80)";
-    case BDLA_ERR_UNSUPPORTED: return "unsupported chunk, head width or decay mode";
+    case BDLA_ERR_UNSUPPORTED: return "unsupported chunk, head width, decay mode or document count";
     case BDLA_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
     case BDLA_ERR_CUDA: return "a CUDA runtime call failed";
     case BDLA_ERR_TIMEOUT: return "device: a bounded wait expired";
@@ -417,8 +428,8 @@ bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_eve
 {
     if (kernel < 0 || kernel >= BDLA_KERNEL_COUNT)
         return BDLA_ERR_SHAPE;
-    g_kernel_events[kernel].start = reinterpret_cast<cudaEvent_t>(start_event);
-    g_kernel_events[kernel].stop = reinterpret_cast<cudaEvent_t>(stop_event);
+    g_kernel_events[kernel].start.store(reinterpret_cast<cudaEvent_t>(start_event));
+    g_kernel_events[kernel].stop.store(reinterpret_cast<cudaEvent_t>(stop_event));
     return BDLA_OK;
 }
 
@@ -436,7 +447,7 @@ bdla_status bdla_decode(const void *q, const void *k, const void *v, const float
         !aligned16(a))
         return BDLA_ERR_ALIGN;
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
-        return BDLA_ERR_UNSUPPORTED;
+        return BDLA_ERR_DTYPE;
     BDLA_CUDA(launch_decode(d.B, d.H, d.dk, d.dv, static_cast<const __nv_bfloat16 *>(q),
                             static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
                             a, b, mode, state, o, o_dtype == BDLA_F32,
@@ -446,10 +457,10 @@ bdla_status bdla_decode(const void *q, const void *k, const void *v, const float
 
 bdla_status bdla_set_seq_split(int blocks)
 {
-    g_seq_split = blocks;
+    g_seq_split.store(blocks);
     return BDLA_OK;
 }
 
-int bdla_version(void) { return 200; }
+int bdla_version(void) { return 300; }
 
 }  // extern "C"

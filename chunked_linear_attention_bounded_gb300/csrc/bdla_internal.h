@@ -3,8 +3,12 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
+#include <atomic>
+
+#include "../../include/bdla_tuning.h"
 #include "bdla_common.cuh"
 
 namespace bdla {
@@ -20,6 +24,13 @@ struct Problem {
     DeviceStatus *st;
     cudaStream_t stream;
 };
+
+// Host-side argument checks shared by the entry points: sizes (documents
+// are a grid extent, so at most 65535; dk in {64, 128}; dv in {64, 128, 256})
+// and the decay parameters (chunk 16; bounded mode needs b finite, b <= 0 and
+// chunk * |b| <= 80).
+bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs);
+bdla_status check_decay(float b, int chunk, int mode);
 
 // Slots of a checkpoint array with the given stride.
 inline int64_t ckpt_slots(const Problem &p, int stride)
@@ -49,25 +60,48 @@ cudaError_t launch_doc_order(const Problem &p, int32_t *order);
 // four segments per SM when the (document, head, dv slice) units are fewer
 // than the GPU's SMs.  Pointers are left null.
 SegPlan plan_segments(const Problem &p);
-extern int g_seq_split;
+extern std::atomic<int> g_seq_split;
 
 // Events recorded around a kernel's launches (measurement hook, see
 // bdla_set_kernel_events); null when unset.
 struct KernelEvents {
-    cudaEvent_t start = nullptr, stop = nullptr;
+    std::atomic<cudaEvent_t> start{nullptr}, stop{nullptr};
 };
 extern KernelEvents g_kernel_events[BDLA_KERNEL_COUNT];
 
-inline void mark_start(int kernel, cudaStream_t s)
+// Every kernel's launches sit inside an NVTX range named after it, so a
+// timeline tool shows the launches and the gaps between them; the caller's
+// measurement events (if set) are recorded at the same two points.
+inline const char *kernel_range_name(int kernel)
 {
-    if (g_kernel_events[kernel].start)
-        cudaEventRecord(g_kernel_events[kernel].start, s);
+    static const char *names[BDLA_KERNEL_COUNT] = {"bdla:decay", "bdla:fwd", "bdla:bwd",
+                                                   "bdla:states", "bdla:seg"};
+    return names[kernel];
 }
-inline void mark_stop(int kernel, cudaStream_t s)
-{
-    if (g_kernel_events[kernel].stop)
-        cudaEventRecord(g_kernel_events[kernel].stop, s);
-}
+// Scope of one kernel's launches: pushes the NVTX range and records the
+// caller's start event on entry, records the stop event and pops the range on
+// exit (early returns included).
+class KernelMark {
+  public:
+    KernelMark(int kernel, cudaStream_t s) : kernel_(kernel), s_(s)
+    {
+        nvtxRangePushA(kernel_range_name(kernel));
+        if (cudaEvent_t e = g_kernel_events[kernel].start.load())
+            cudaEventRecord(e, s);
+    }
+    ~KernelMark()
+    {
+        if (cudaEvent_t e = g_kernel_events[kernel_].stop.load())
+            cudaEventRecord(e, s_);
+        nvtxRangePop();
+    }
+    KernelMark(const KernelMark &) = delete;
+    KernelMark &operator=(const KernelMark &) = delete;
+
+  private:
+    int kernel_;
+    cudaStream_t s_;
+};
 
 // One recurrent step per sequence: state <- e^{lambda} state + k v^T in place,
 // o = state^T q.  q, k bf16 [B, H, dk]; v bf16 [B, H, dv]; a fp32 [B, H];

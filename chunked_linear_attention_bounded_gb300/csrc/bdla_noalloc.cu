@@ -10,7 +10,9 @@
 // outputs.  The price is a fixed maximum problem size and a shared scratch.
 //
 // The arrays are part of the library's device image: every GPU that loads
-// the library holds them (8 MiB + 256 B) until the process exits.
+// the library holds them (8 MiB + 256 B) until the process exits.  The
+// status word keeps the first device-side error of any call (it starts at
+// zero with the image) until bdla_noalloc_read_status reads and clears it.
 #include <mutex>
 
 #include "bdla_internal.h"
@@ -66,19 +68,14 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
                                         bdla_dtype o_dtype, float *hT, bdla_dims d,
                                         bdla_decay_mode mode, void *stream)
 {
-    if (d.T < 0 || d.H < 1 || d.B < 1)
-        return BDLA_ERR_SHAPE;
-    if (d.dk != 64 && d.dk != 128)
-        return BDLA_ERR_UNSUPPORTED;
-    if (d.dv != 64 && d.dv != 128 && d.dv != 256)
-        return BDLA_ERR_UNSUPPORTED;
-    if (chunk != kChunk || (mode != BDLA_DECAY_BOUNDED_SIGMOID && mode != BDLA_DECAY_NEG_SOFTPLUS))
-        return BDLA_ERR_UNSUPPORTED;
-    if (mode == BDLA_DECAY_BOUNDED_SIGMOID &&
-        (!isfinite(b) || b > 0.0f || (double)chunk * fabs((double)b) > 80.0))
-        return BDLA_ERR_RANGE;
+    bdla_status s = check_dims(d, false, 0);
+    if (s != BDLA_OK)
+        return s;
+    if ((s = check_decay(b, chunk, mode)) != BDLA_OK)
+        return s;
+    // B * T * H (token, head) pairs, compared without forming the product
     const int64_t tokens = (int64_t)d.B * d.T;
-    if ((size_t)tokens * (size_t)d.H > kNoAllocMaxTokenHeads)
+    if (tokens > (int64_t)(kNoAllocMaxTokenHeads / (size_t)d.H))
         return BDLA_ERR_TOO_LARGE;
     if (tokens > 0 && (!q || !k || !v || !a || !o))
         return BDLA_ERR_NULL;
@@ -86,11 +83,10 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
     if (!a16(q) || !a16(k) || !a16(v) || !a16(o) || !a16(a) || !a16(h0) || !a16(hT))
         return BDLA_ERR_ALIGN;
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
-        return BDLA_ERR_UNSUPPORTED;
+        return BDLA_ERR_DTYPE;
 
     NoAllocPtrs ptrs;
-    const bdla_status s = noalloc_setup(ptrs);
-    if (s != BDLA_OK)
+    if ((s = noalloc_setup(ptrs)) != BDLA_OK)
         return s;
 
     Problem p;
@@ -103,11 +99,10 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
     p.dv = d.dv;
     p.b = b;
     p.mode = mode;
+    // the first device-side error of any call stays in the status word until
+    // bdla_noalloc_read_status reads and clears it
     p.st = ptrs.status;
     p.stream = reinterpret_cast<cudaStream_t>(stream);
-    // the status word is shared by every call: start each call from zero
-    if (cudaMemsetAsync(ptrs.status, 0, sizeof(DeviceStatus), p.stream) != cudaSuccess)
-        return BDLA_ERR_CUDA;
     if (launch_decay(p, a, ptrs.gamma, nullptr) != cudaSuccess)
         return BDLA_ERR_CUDA;
     if (launch_fwd_sm100(p, static_cast<const __nv_bfloat16 *>(q),
@@ -116,4 +111,23 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
                          o_dtype == BDLA_F32, hT, nullptr, 0, 0, SegPlan{}) != cudaSuccess)
         return BDLA_ERR_CUDA;
     return BDLA_OK;
+}
+
+extern "C" bdla_status bdla_noalloc_read_status(void *stream)
+{
+    NoAllocPtrs ptrs;
+    const bdla_status s = noalloc_setup(ptrs);
+    if (s != BDLA_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    // a plain copy out of the library's own array: no allocation, and the
+    // stream is idle, so no call is writing the word meanwhile
+    unsigned int code = 0;
+    if (cudaMemcpy(&code, &ptrs.status->code, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    if (code != 0 && cudaMemset(ptrs.status, 0, sizeof(DeviceStatus)) != cudaSuccess)
+        return BDLA_ERR_CUDA;
+    return static_cast<bdla_status>(code);
 }

@@ -28,7 +28,7 @@ namespace bdla {
 
 bool make_token_map(CUtensorMap *map, const void *ptr, int d, int H, int64_t tokens);
 
-int g_seq_split = 0;
+std::atomic<int> g_seq_split{0};
 
 namespace {
 
@@ -390,14 +390,17 @@ int sm_count()
 SegPlan plan_segments(const Problem &p)
 {
     SegPlan sp;
-    if (p.tokens <= 0 || p.n_docs <= 0 || g_seq_split < 0)
+    const int split = g_seq_split.load();
+    // the slot count (at most 65535) must leave room for at least one token
+    // block beside the documents
+    if (p.tokens <= 0 || p.n_docs <= 0 || split < 0 || p.n_docs >= 65535 - 1)
         return sp;
     const int slices = p.dv > 128 ? p.dv / 128 : 1;
     const int64_t units = (int64_t)p.n_docs * p.H * slices;
     const int64_t nblk = (p.tokens + BT - 1) / BT;
     int64_t sb;
-    if (g_seq_split > 0) {
-        sb = g_seq_split;
+    if (split > 0) {
+        sb = split;
     } else {
         const int sms = sm_count();
         if (units >= sms)

@@ -29,7 +29,8 @@
  *    asynchronous and stream-ordered.
  *  - Host-detectable errors return a status before any launch.  Errors found
  *    on the device (a bounded wait that expired, malformed cu_seqlens) are
- *    recorded in a status word inside `ws`; read it with bdla_read_status.
+ *    recorded in a status word inside `ws`; read it with
+ *    bdla_read_device_status.
  *
  * Shapes (bdla_dims): fixed-length calls take [B, T, H, d] tensors; the
  * _varlen calls take packed documents [1, T, H, d] with B = 1, T = total
@@ -37,7 +38,9 @@
  * cu[n_docs] = T).  Tiles restart at each document start; the last tile of a
  * document may be shorter than 16.  For fixed-length calls the documents are
  * the B rows (n_docs = B).
- *   q, k      bf16  [B, T, H, dk]          dk in {64, 128}
+ *   q, k      bf16  [B, T, H, dk]          dk in {64, 128}; dk = 256 is refused
+ *             (BDLA_ERR_UNSUPPORTED): the kernels hold the dk x dv state in
+ *             tensor memory with dk on its 128 lanes
  *   v, dO     bf16  [B, T, H, dv]          dv in {64, 128, 256}
  *   a, da     fp32  [B, T, H]              decay logits and their gradient
  *   o         bf16 or fp32 [B, T, H, dv]
@@ -64,14 +67,15 @@ typedef enum {
     BDLA_OK = 0,
     BDLA_ERR_NULL = 1,         /* a required pointer is NULL */
     BDLA_ERR_SHAPE = 2,        /* a size is negative or inconsistent */
-    BDLA_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
-    BDLA_ERR_RANGE = 4,        /* b > 0, b not finite, or chunk*|b| > 80 (bounded) */
-    BDLA_ERR_UNSUPPORTED = 5,  /* chunk != 16, dk/dv outside the supported set */
-    BDLA_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or too small */
-    BDLA_ERR_CUDA = 7,         /* a CUDA runtime call (launch, attribute) failed */
-    BDLA_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up */
-    BDLA_ERR_DEVICE = 9,       /* device: malformed cu_seqlens or another device check */
-    BDLA_ERR_TOO_LARGE = 10    /* bdla_fwd_noalloc: problem larger than its fixed scratch */
+    BDLA_ERR_DTYPE = 3,        /* o_dtype / ckpt_dtype is not a bdla_dtype value */
+    BDLA_ERR_ALIGN = 4,        /* a pointer is not 16-byte aligned */
+    BDLA_ERR_RANGE = 5,        /* b > 0, b not finite, or chunk*|b| > 80 (bounded) */
+    BDLA_ERR_UNSUPPORTED = 6,  /* chunk != 16, dk/dv outside the supported set, too many documents */
+    BDLA_ERR_WORKSPACE = 7,    /* workspace NULL, misaligned or too small */
+    BDLA_ERR_CUDA = 8,         /* a CUDA runtime call (launch, attribute) failed */
+    BDLA_ERR_TIMEOUT = 9,      /* device: a bounded wait gave up */
+    BDLA_ERR_DEVICE = 10,      /* device: malformed cu_seqlens or another device check */
+    BDLA_ERR_TOO_LARGE = 11    /* bdla_fwd_noalloc: problem larger than its fixed scratch */
 } bdla_status;
 
 typedef enum {
@@ -94,11 +98,13 @@ enum { BDLA_OP_FWD = 0, BDLA_OP_BWD = 1, BDLA_OP_DECAY = 2 };
 /*
  * Bytes of device workspace an op needs.  `op` is BDLA_OP_*, `n_docs` the
  * document count of a varlen call (0 for fixed-length calls), `ckpt_stride`
- * the stride of the fp32 checkpoints the backward will be handed (0 if none;
- * bf16 checkpoints: pass their stride only when dv <= 128).
- * Returns 0 on invalid dims.  The first 256 bytes of every workspace are the
- * device status word: zero them once after allocating the workspace
- * (bdla_read_status clears them again).
+ * the stride of the checkpoints the backward will be handed (0 if none).
+ * The stride matters because a backward handed no usable checkpoints
+ * (stride 0, or a stride that does not divide 128) recomputes the states
+ * before every 128-token block into the workspace.  `mode` does not change
+ * the size.  Returns 0 on invalid dims.  The first 256 bytes of every
+ * workspace are the device status word: zero them once after allocating the
+ * workspace (bdla_read_device_status clears them again).
  */
 size_t bdla_workspace_bytes(int op, bdla_dims d, int n_docs, bdla_decay_mode mode, int ckpt_stride);
 
@@ -155,21 +161,10 @@ bdla_status bdla_bwd_varlen(const void *q, const void *k, const void *v, const f
 /*
  * Synchronises `stream`, returns the device status word recorded in `ws` by
  * earlier calls (BDLA_OK if none) and clears it.  BDLA_ERR_CUDA if the
- * synchronisation itself fails.
+ * synchronisation itself fails.  Only the first device-side error since the
+ * last read is kept (later ones are dropped).
  */
-bdla_status bdla_read_status(void *ws, void *stream);
-
-/*
- * Measurement hook.  Until called again with NULL events, every later call
- * that launches kernel `kernel` (BDLA_KERNEL_*) records `start_event` just
- * before and `stop_event` just after that launch, on the call's stream, so
- * the caller can time the kernel alone (cudaEventElapsedTime).  Both events
- * are cudaEvent_t created by the caller.  Not thread-safe; meant for
- * benchmarks.  Returns BDLA_ERR_SHAPE for an unknown kernel id.
- */
-enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KERNEL_STATES = 3,
-       BDLA_KERNEL_SEG = 4, BDLA_KERNEL_COUNT = 5 };
-bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
+bdla_status bdla_read_device_status(void *ws, void *stream);
 
 /*
  * One recurrent (decode) step per sequence: the same recurrence for a single
@@ -191,28 +186,6 @@ bdla_status bdla_decode(const void *q, const void *k, const void *v, const float
                         bdla_decay_mode mode, void *stream);
 
 /*
- * Sequence parallelism inside one GPU.  The pages pass a state from chunk to
- * chunk ("Engineering Long-Context Training for Trillion-Parameter MoE
- * Models", sec. 3.1), so a (document, head) pair is a chain of 128-token
- * blocks.  When those pairs are too few to occupy the GPU, the library cuts
- * each document into segments of `blocks` 128-token blocks, first computes
- * the state (forward) or adjoint state (backward) entering every segment
- * (kernel id BDLA_KERNEL_SEG: one summary GEMM pass and one scan over the
- * segments), then runs one CTA per segment.  The result is the same up to
- * floating-point rounding order.
- *   blocks == 0 (default): automatic; documents are cut, into about four
- *                          segments per SM, only when (documents x heads x
- *                          dv/128 slices) is below the GPU's SM count.
- *   blocks <  0: never cut.
- *   blocks >  0: always cut into segments of `blocks` blocks (at least as
- *                long as needed to keep the segment count within 65535).
- * The setting is process-wide and read when a call (or
- * bdla_workspace_bytes) is made: the workspace size depends on it, so size
- * the workspace after changing it.  Not thread-safe.  Always BDLA_OK.
- */
-bdla_status bdla_set_seq_split(int blocks);
-
-/*
  * Forward pass for callers that cannot allocate device memory (no workspace
  * argument).  The pages have no counterpart: this is an interface for
  * callers, such as code running inside an allocator's callbacks or a runtime
@@ -228,11 +201,20 @@ bdla_status bdla_set_seq_split(int blocks);
  * shares the one array: calls that overlap on the GPU (different streams
  * without ordering) race and give wrong results; order them.  Device-side
  * errors (a bounded wait that expired) are recorded in the library's own
- * status word, which each call clears, and are not reported.
+ * status word, which keeps the first error until bdla_noalloc_read_status
+ * reads and clears it.  Sizes are checked as for bdla_fwd (B <= 65535).
  */
 bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void *v, const float *a,
                              float b, int chunk, const float *h0, void *o, bdla_dtype o_dtype,
                              float *hT, bdla_dims d, bdla_decay_mode mode, void *stream);
+
+/*
+ * Status of the bdla_fwd_noalloc calls on the current device: synchronises
+ * `stream`, returns the first device-side error recorded since the last read
+ * (BDLA_OK if none) and clears it.  Allocates nothing; BDLA_ERR_CUDA if the
+ * synchronisation or the copy fails.  No counterpart on the pages either.
+ */
+bdla_status bdla_noalloc_read_status(void *stream);
 
 /* Static English description of a status code. */
 const char *bdla_status_string(bdla_status s);

@@ -92,8 +92,8 @@ def run_gpu(g, b, mode, with_grad=True, o_dtype=torch.bfloat16, dhT=None, ckpt_s
                                        want_dh0=True, ws=ws_b)
         out.update(dq=dq, dk=dk, dv=dv, da=da, dh0=dh0)
     torch.cuda.synchronize()
-    assert ws_f.read_status() == 0, "forward recorded a device-side error"
-    assert ws_b.read_status() == 0, "backward recorded a device-side error"
+    assert ws_f.read_device_status() == 0, "forward recorded a device-side error"
+    assert ws_b.read_device_status() == 0, "backward recorded a device-side error"
     return out
 
 

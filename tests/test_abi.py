@@ -21,9 +21,13 @@ def L():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "bdla.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return set(re.findall(r"\b(bdla_\w+)\s*\(", src))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(bdla_\w+)\s*\(", src))
+    return names
 
 
 def test_exports_every_declared_symbol(L):
@@ -34,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(11):
+    for code in range(12):
         assert bdla.status_string(code) not in ("", "unknown status")
     assert bdla.status_string(123) == "unknown status"
     assert L.bdla_version() >= 100
@@ -90,41 +94,59 @@ def test_decode_host_validation(L):
     fake = ctypes.c_void_p(1 << 20)
     call = lambda dims, b=-5.0, mode=0, ptr=fake, odt=0: L.bdla_decode(
         ptr, fake, fake, fake, b, fake, fake, odt, dims, mode, None)
-    assert call(bdla.Dims(4, 2, 2, 128, 128)) == 2           # T must be 1
-    assert call(bdla.Dims(4, 1, 2, 96, 128)) == 5            # dk 96 unsupported
-    assert call(bdla.Dims(4, 1, 2, 128, 128), b=0.5) == 4    # b > 0
-    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=None) == 1
-    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=ctypes.c_void_p((1 << 20) + 4)) == 3
-    assert call(bdla.Dims(4, 1, 2, 128, 128), odt=7) == 5
+    assert call(bdla.Dims(4, 2, 2, 128, 128)) == bdla.ERR_SHAPE          # T must be 1
+    assert call(bdla.Dims(4, 1, 2, 96, 128)) == bdla.ERR_UNSUPPORTED     # dk 96 unsupported
+    assert call(bdla.Dims(4, 1, 2, 128, 128), b=0.5) == bdla.ERR_RANGE   # b > 0
+    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=None) == bdla.ERR_NULL
+    assert call(bdla.Dims(4, 1, 2, 128, 128), ptr=ctypes.c_void_p((1 << 20) + 4)) == bdla.ERR_ALIGN
+    assert call(bdla.Dims(4, 1, 2, 128, 128), odt=7) == bdla.ERR_DTYPE
 
 
 def test_host_validation_before_launch(L):
-    assert _fwd(L, chunk=32) == 5                     # chunk != 16
-    assert _fwd(L, b=0.5) == 4                        # b > 0
-    assert _fwd(L, b=float("nan")) == 4
-    assert _fwd(L, b=-5.5) == 4                       # 16 * 5.5 > 80
-    assert _fwd(L, b=-9.0, mode=1, ws_bytes=16) == 6  # ablation ignores b; stops at the ws check
-    assert _fwd(L, mode=7) == 5
-    assert _fwd(L, dims=(1, 64, 2, 96, 64)) == 5
-    assert _fwd(L, dims=(1, -1, 2, 64, 64)) == 2
-    assert _fwd(L, dims=(0, 64, 2, 64, 64)) == 2
-    assert _fwd(L, q=None) == 1
-    assert _fwd(L, q=ctypes.c_void_p((1 << 20) + 8)) == 3
-    assert _fwd(L, ws=None) == 6
-    assert _fwd(L, ws_bytes=16) == 6
-    assert _fwd(L, ckpt=FAKE, stride=24) == 2
-    assert _fwd(L, o_dtype=5) == 5
-    assert _fwd(L, ckpt=FAKE, stride=64, ck_dtype=0) == 5    # bf16 checkpoints need stride % 128 == 0
-    assert _fwd(L, ckpt=FAKE, stride=128, ck_dtype=7) == 5
+    E = bdla
+    assert _fwd(L, chunk=32) == E.ERR_UNSUPPORTED              # chunk != 16
+    assert _fwd(L, b=0.5) == E.ERR_RANGE                       # b > 0
+    assert _fwd(L, b=float("nan")) == E.ERR_RANGE
+    assert _fwd(L, b=-5.5) == E.ERR_RANGE                      # 16 * 5.5 > 80
+    assert _fwd(L, b=-9.0, mode=1, ws_bytes=16) == E.ERR_WORKSPACE   # ablation ignores b
+    assert _fwd(L, mode=7) == E.ERR_UNSUPPORTED
+    assert _fwd(L, dims=(1, 64, 2, 96, 64)) == E.ERR_UNSUPPORTED
+    assert _fwd(L, dims=(1, 64, 2, 256, 64)) == E.ERR_UNSUPPORTED   # dk = 256 refused
+    assert _fwd(L, dims=(1, -1, 2, 64, 64)) == E.ERR_SHAPE
+    assert _fwd(L, dims=(0, 64, 2, 64, 64)) == E.ERR_SHAPE
+    assert _fwd(L, dims=(65536, 1, 1, 64, 64)) == E.ERR_UNSUPPORTED  # documents are a grid extent
+    assert _fwd(L, q=None) == E.ERR_NULL
+    assert _fwd(L, q=ctypes.c_void_p((1 << 20) + 8)) == E.ERR_ALIGN
+    assert _fwd(L, ws=None) == E.ERR_WORKSPACE
+    assert _fwd(L, ws_bytes=16) == E.ERR_WORKSPACE
+    assert _fwd(L, ckpt=FAKE, stride=24) == E.ERR_SHAPE
+    assert _fwd(L, o_dtype=5) == E.ERR_DTYPE
+    assert _fwd(L, ckpt=FAKE, stride=64, ck_dtype=0) == E.ERR_UNSUPPORTED   # bf16 needs stride % 128 == 0
+    assert _fwd(L, ckpt=FAKE, stride=128, ck_dtype=7) == E.ERR_DTYPE
     st = L.bdla_bwd(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, None, None, None, 0, 1, FAKE, FAKE, FAKE,
                     FAKE, None, bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
-    assert st == 1                                    # dO missing
+    assert st == E.ERR_NULL                                    # dO missing
+    st = L.bdla_bwd(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, FAKE, None, FAKE, 128, 9, FAKE, FAKE, FAKE,
+                    FAKE, None, bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
+    assert st == E.ERR_DTYPE                                   # checkpoint dtype 9
     st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 2, None, FAKE, 0, None, None, 0, 1,
                            bdla.Dims(1, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
-    assert st == 1                                    # cu_seqlens missing
+    assert st == E.ERR_NULL                                    # cu_seqlens missing
     st = L.bdla_fwd_varlen(FAKE, FAKE, FAKE, FAKE, -5.0, 16, FAKE, 2, None, FAKE, 0, None, None, 0, 1,
                            bdla.Dims(2, 64, 2, 64, 64), 0, FAKE, 1 << 40, None)
-    assert st == 2                                    # varlen needs B == 1
+    assert st == E.ERR_SHAPE                                   # varlen needs B == 1
+
+
+def test_segment_plan_with_the_largest_document_count(L):
+    """65535 documents (the grid limit) leave no room for segment slots: a
+    forced cut is then skipped instead of dividing by zero while planning."""
+    try:
+        bdla.set_seq_split(1)
+        n = bdla.workspace_bytes(bdla.OP_FWD, (1, 65535 * 2, 1, 64), 64, n_docs=65535)
+        bdla.set_seq_split(-1)
+        assert n == bdla.workspace_bytes(bdla.OP_FWD, (1, 65535 * 2, 1, 64), 64, n_docs=65535) > 0
+    finally:
+        bdla.set_seq_split(0)
 
 
 def test_package_exports():

@@ -77,13 +77,17 @@ def test_edge_lengths(T):
     compare_all(gpu, ref)
 
 
-def test_fp32_output_matches_tightly():
+def test_fp32_output_is_closer_than_bf16_output():
+    """The 256-token parity workload asks for an fp32 o: it skips the final
+    bf16 rounding of o, so its error against the oracle is below the bf16
+    output's (both within the bar)."""
     w = WORKLOADS["pr1"]
     inp = make_inputs(w)
-    gpu = run_gpu(to_device(inp), w.b, w.mode, with_grad=False, o_dtype=torch.float32)
     ref = run_oracle(inp, w.b, w.mode, with_grad=False)
-    errs = compare_all(gpu, ref)
-    assert errs["o"] < 5e-3
+    e32 = compare_all(run_gpu(to_device(inp), w.b, w.mode, with_grad=False, o_dtype=torch.float32), ref)
+    e16 = compare_all(run_gpu(to_device(inp), w.b, w.mode, with_grad=False, o_dtype=torch.bfloat16), ref)
+    print("rel L2 of o: fp32 output %.3e, bf16 output %.3e" % (e32["o"], e16["o"]))
+    assert e32["o"] < e16["o"]
 
 
 def test_varlen_with_empty_documents():
@@ -137,7 +141,7 @@ def test_bf16_block_checkpoints_feed_the_backward(dv):
                                     cu_seqlens=g["cu_seqlens"], ckpt=ck, ckpt_stride=128, want_dh0=True,
                                     ws=ws)
     torch.cuda.synchronize()
-    assert ws.read_status() == 0
+    assert ws.read_device_status() == 0
     gpu = dict(o=o, hT=hT, dq=dq, dk=dk, dv=dv_, da=da, dh0=dh0)
     compare_all(gpu, run_oracle(inp, w.b, w.mode))
 
@@ -150,18 +154,18 @@ def test_bad_cu_seqlens_set_device_status(cu):
     g["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device="cuda")
     ws = bdla.Workspace(1 << 20, "cuda")
     bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=g["cu_seqlens"], ws=ws)
-    assert ws.read_status() == 9
-    assert ws.read_status() == 0          # cleared after reading
+    assert ws.read_device_status() == bdla.ERR_DEVICE
+    assert ws.read_device_status() == 0          # cleared after reading
     # the context is still usable
     o, _, _ = bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=g["cu_seqlens"][:1].new_tensor([0, 300]), ws=ws)
     torch.cuda.synchronize()
-    assert ws.read_status() == 0
+    assert ws.read_device_status() == 0
 
 
 # Full-size workloads: the GPU runs the whole input, the oracle checks a
 # sample of heads (every document of those heads, every token).
-FULL = [("pr1", None), ("c8k", [0, 9]), ("varlen64k", [0, 17, 31]), ("c256k", [5]), ("c1m", [3]),
-        ("c1m_ablation", [6])]
+FULL = [("pr1", None), ("c8k", [0, 9]), ("varlen64k", [0, 17, 31]), ("c256k", [5, 12]),
+        ("c1m", [3, 6]), ("c1m_ablation", [1, 6])]
 
 
 @pytest.mark.slow

@@ -86,7 +86,7 @@ def test_checkpoints_written_by_segments_feed_the_backward(split, stride, dtype)
                                    cu_seqlens=g["cu_seqlens"], ckpt=ck, ckpt_stride=stride,
                                    want_dh0=True, ws=ws)
     torch.cuda.synchronize()
-    assert ws.read_status() == 0
+    assert ws.read_device_status() == 0
     gpu = dict(o=o, hT=hT, dq=dq, dk=dk, dv=dv, da=da, dh0=dh0)
     compare_all(gpu, run_oracle(inp, w.b, w.mode))
     # the same checkpoints as a single CTA per document writes
@@ -94,7 +94,7 @@ def test_checkpoints_written_by_segments_feed_the_backward(split, stride, dtype)
     _, _, ck1 = bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
                          ckpt_stride=stride, ckpt_dtype=dtype, ws=ws)
     torch.cuda.synchronize()
-    assert ws.read_status() == 0
+    assert ws.read_device_status() == 0
     # compare the slots the forward writes: block starts at multiples of the stride
     cu = inp["cu_seqlens"].tolist()
     slots = [c0 // stride + n + c for n, (c0, c1) in enumerate(zip(cu[:-1], cu[1:]))
