@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="varlen64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the 1M-token bounded-vs-ablation comparison")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -428,6 +430,9 @@ def ours_arm(args, w, inp):
     ab = algorithmic_bytes(w, n_seq)
     dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
     achieved = ab[dom] / (kernel_ms[dom] / 1000.0) / 1e9
+    abl = None
+    if world == 1 and not args.no_ablation:
+        abl = ablation_leg(dev)
     out = None
     if rank == 0:
         cpu = None
@@ -448,10 +453,66 @@ def ours_arm(args, w, inp):
                        "d2h_bytes_per_step": d2h},
                "gpu_launches": launches_per_step * K,
                "clocks": clk.summary(),
-               "cpu_baseline": cpu}
+               "cpu_baseline": cpu,
+               "ablation": abl}
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def ablation_leg(dev, steps: int = 5, warmup: int = 3):
+    """The pages' one performance claim, measured: at the 1M-token stage
+    (T=1048576, H=8, dk=dv=128) one fwd+bwd step with the bounded decay (every
+    diagonal tile through the tensor-core GEMMs) against the same step with the
+    unbounded -softplus decay, whose diagonal tiles take the explicit
+    position-pair path.  Same call sequence as the headline step (bf16 states
+    handed from the forward to the backward every 128 tokens); inputs drawn
+    on the device with the workloads' recipe."""
+    import torch
+
+    import chunked_linear_attention_bounded_gb300 as bdla
+    from chunked_linear_attention_bounded_gb300 import bdla as B
+    from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS, make_inputs_on
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("c1m", "c1m_ablation"):
+        w = WORKLOADS[name]
+        g = make_inputs_on(w, dev)
+        ws_f = B.Workspace(B.workspace_bytes(B.OP_FWD, tuple(g["q"].shape), w.dv, 0, w.mode), dev)
+        ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, 0, w.mode,
+                                             ckpt_stride=128), dev)
+        o = torch.empty(g["v"].shape, dtype=torch.bfloat16, device=dev)
+        ck = torch.empty((w.H, B.n_slots(w.B * w.T, w.B, 128), w.dk, w.dv), dtype=torch.bfloat16,
+                         device=dev)
+        hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+        outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
+                torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
+                torch.empty(g["v"].shape, dtype=torch.float32, device=dev),
+                torch.empty(g["a"].shape, dtype=torch.float32, device=dev))
+
+        def step():
+            bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, mode=w.mode, ws=ws_f, out=o, hT_out=hT,
+                     ckpt_stride=128, ckpt_out=ck)
+            bdla.bwd(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, ckpt=ck, ckpt_stride=128,
+                     mode=w.mode, ws=ws_b, outs=outs)
+        for _ in range(warmup):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        for code in (ws_f.read_device_status(), ws_b.read_device_status()):
+            if code:
+                raise RuntimeError(f"device status {code} in the {name} steps")
+        res[name] = e0.elapsed_time(e1) / steps
+        del g, ws_f, ws_b, o, ck, hT, outs
+        torch.cuda.empty_cache()
+    return {"workload": "1M-token stage, T=1048576, H=8, dk=dv=128, fwd+bwd step",
+            "bounded_ms": res["c1m"], "ablation_ms": res["c1m_ablation"],
+            "ablation_over_bounded": res["c1m_ablation"] / res["c1m"], "steps": steps}
 
 
 def decode_arm(args):

@@ -35,8 +35,9 @@ STATUS_NAMES = {OK: "BDLA_OK", ERR_NULL: "BDLA_ERR_NULL", ERR_SHAPE: "BDLA_ERR_S
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
            "bdla_bwd_varlen", "bdla_read_device_status", "bdla_status_string", "bdla_version",
            "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
-           "bdla_set_seq_split", "bdla_decode")
+           "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
+STALL_NONE, STALL_PRODUCER, STALL_MMA, STALL_EPILOGUE = 0, 1, 2, 3
 
 
 class BdlaError(RuntimeError):
@@ -89,6 +90,10 @@ def lib():
         L.bdla_set_seq_split.restype = ci
         L.bdla_decode.argtypes = [vp, vp, vp, vp, f32, vp, vp, ci, Dims, ci, vp]
         L.bdla_decode.restype = ci
+        L.bdla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.bdla_set_wait_limit_ns.restype = ci
+        L.bdla_set_test_stall.argtypes = [ci, ci]
+        L.bdla_set_test_stall.restype = ci
         del i32
         _lib = L
     return _lib
@@ -101,6 +106,20 @@ def set_kernel_events(kernel: int, start=None, stop=None):
     st = lib().bdla_set_kernel_events(int(kernel), h(start), h(stop))
     if st:
         raise BdlaError(st, "bdla_set_kernel_events")
+
+
+def set_wait_limit_ns(ns: int):
+    """Limit of the kernels' pipeline waits for later launches (0 = the
+    default 2 s); a test hook (include/bdla_tuning.h)."""
+    lib().bdla_set_wait_limit_ns(int(ns))
+
+
+def set_test_stall(kernel: int, role: int):
+    """Test hook: `role` (STALL_*) of `kernel` (KERNEL_*) waits on a barrier
+    nothing arrives at, so the bounded wait runs out (STALL_NONE clears)."""
+    st = lib().bdla_set_test_stall(int(kernel), int(role))
+    if st:
+        raise BdlaError(st, "bdla_set_test_stall")
 
 
 _seq_split = 0

@@ -10,6 +10,8 @@ using namespace bdla;
 
 namespace bdla {
 KernelEvents g_kernel_events[BDLA_KERNEL_COUNT];
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_test_stall[BDLA_KERNEL_COUNT];
 
 bdla_status check_dims(const bdla_dims &d, bool varlen, int n_docs)
 {
@@ -458,6 +460,20 @@ bdla_status bdla_decode(const void *q, const void *k, const void *v, const float
 bdla_status bdla_set_seq_split(int blocks)
 {
     g_seq_split.store(blocks);
+    return BDLA_OK;
+}
+
+bdla_status bdla_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+    return BDLA_OK;
+}
+
+bdla_status bdla_set_test_stall(int kernel, int role)
+{
+    if (kernel < 0 || kernel >= BDLA_KERNEL_COUNT || role < BDLA_STALL_NONE || role > BDLA_STALL_EPILOGUE)
+        return BDLA_ERR_SHAPE;
+    g_test_stall[kernel].store(role);
     return BDLA_OK;
 }
 

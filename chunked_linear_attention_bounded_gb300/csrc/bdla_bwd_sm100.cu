@@ -81,7 +81,8 @@ constexpr int BT = 128;
 constexpr int kEpiThreads = 256;                 // 8 epilogue warps, two per TMEM lane quarter
 constexpr int kBwdThreads = 64 + kEpiThreads;    // + producer warp and MMA warp
 constexpr uint32_t kPanel = 16384;
-constexpr uint64_t kWaitNs = 2000000000ull;
+// drains of a CTA's own copies and MMAs before it exits keep the full limit
+constexpr uint64_t kWaitNs = kDefaultWaitNs;
 
 template <int DV>
 struct BwdSmem {
@@ -94,19 +95,22 @@ struct BwdSmem {
     alignas(1024) unsigned char x[2 * kPanel];           // P, then dP: rows t, panels s
     float cdiag[BT];
     float coff[BT];
-    // per row and column half: v_s . (P^T dO)_s, sum_{s<=t} W_ts, k.dk_inter, q.dq_inter
-    float colpart[2][BT];
-    float rowpart[2][BT];
-    float kdpart[2][BT];
-    float ypart[2][BT];
+    // per block parity, row and column half: v_s . (P^T dO)_s, sum_{s<=t} W_ts,
+    // k.dk_inter, q.dq_inter, and per parity and epilogue warp <S_in, E>: a
+    // block's decay gradient is summed up while the next block runs
+    float colpart[2][2][BT];
+    float rowpart[2][2][BT];
+    float kdpart[2][2][BT];
+    float ypart[2][2][BT];
     float scan[2][4];
     float gam[BT / kChunk];
-    float se[8];
+    float se[2][8];
     float gq[BT];                  // Gamma per row (ablation diagonal path)
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
     uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
         mf_done, acc_free, drain, full_z, z_free;
+    uint64_t never;   // nothing arrives here: the wait of the stall test hook
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -265,7 +269,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  float *__restrict__ dvv, float *__restrict__ da_base, float *__restrict__ dh0,
                  float *__restrict__ part, int64_t part_qk, int64_t part_a, int n_docs, int seg_blk,
                  const float *__restrict__ seg_init, const int32_t *__restrict__ doc_order,
-                 DeviceStatus *st)
+                 DeviceStatus *st, uint64_t wait_ns, int stall)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
@@ -293,6 +297,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         return;
     }
     const int nblk = (int)((d.len + BT - 1) / BT);
+    // test hook: the stalling role waits at this block (its second, or its only one)
+    const int stall_blk = nblk > 1 ? 1 : 0;
     const int kpan = dk / 64;
     // Mf reads K o w_s from V's tile when that tile has room for K
     const bool khat_v = DV / 64 >= kpan;
@@ -320,6 +326,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.drain, 1);
         mbar_init(&sm.full_z, 1);
         mbar_init(&sm.z_free, 1);
+        mbar_init(&sm.never, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
     }
@@ -352,13 +359,14 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             int last = -1;
             bool ok = true;
             for (int jj = 0; jj < nblk; ++jj) {
-                if (*abort_flag) {
+                if (*abort_flag || (stall == BDLA_STALL_PRODUCER && jj == stall_blk &&
+                                    !mbar_wait(&sm.never, 0, wait_ns))) {
                     ok = false;
                     break;
                 }
                 const int j = nblk - 1 - jj;
                 const int t0 = (int)(d.start + (int64_t)j * BT);
-                if (jj > 0 && !mbar_wait(&sm.free_in, (jj - 1) & 1, kWaitNs)) {
+                if (jj > 0 && !mbar_wait(&sm.free_in, (jj - 1) & 1, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -375,7 +383,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 if (st_tma) {
                     // bf16 state before the block, straight into the z tile, once the
                     // previous block's output staging has left z
-                    if (jj > 0 && !mbar_wait(&sm.z_free, (jj - 1) & 1, kWaitNs)) {
+                    if (jj > 0 && !mbar_wait(&sm.z_free, (jj - 1) & 1, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -416,10 +424,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             bool ok = true;
             for (int jj = 0; jj < nblk && ok; ++jj) {
                 const uint32_t par = jj & 1;
-                if (*abort_flag || !mbar_wait(&sm.full_in, par, kWaitNs) ||
+                if (*abort_flag ||
+                    (stall == BDLA_STALL_MMA && jj == stall_blk && !mbar_wait(&sm.never, 0, wait_ns)) ||
+                    !mbar_wait(&sm.full_in, par, wait_ns) ||
                     // S_in: straight from its TMA load, or once the epilogue converted it
-                    !mbar_wait(st_tma ? &sm.full_z : &sm.z_ready, par, kWaitNs) ||
-                    (jj > 0 && !mbar_wait(&sm.acc_free, (jj - 1) & 1, kWaitNs))) {
+                    !mbar_wait(st_tma ? &sm.full_z : &sm.z_ready, par, wait_ns) ||
+                    (jj > 0 && !mbar_wait(&sm.acc_free, (jj - 1) & 1, wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -431,7 +441,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
                 }
                 umma_commit(&sm.m1_done);
-                if (!mbar_wait(&sm.ea_done, par, kWaitNs)) {
+                if (!mbar_wait(&sm.ea_done, par, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -441,7 +451,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int ks = 0; ks < DV / 16; ++ks)
                     umma_bf16(t_c1, kmaj(sv, ks), kmaj(sz, ks), id_ve, ks > 0);
                 umma_commit(&sm.mb_done);
-                if (!mbar_wait(&sm.eb_done, par, kWaitNs)) {
+                if (!mbar_wait(&sm.eb_done, par, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -451,7 +461,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     umma_bf16(t_c3, kmaj(sx, ks), mnmaj(sk, ks), id_dpk, 1);
                 }
                 umma_commit(&sm.md_done);
-                if (!mbar_wait(&sm.ee_done, par, kWaitNs)) {
+                if (!mbar_wait(&sm.ee_done, par, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -491,14 +501,20 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
             tmem_st_wait();
         }
-        // values of the block whose outputs are still pending (written in Eg)
+        // the block whose outputs are still pending (written in Eg)
         int pend_j = -1;
-        float pend_fac = 0.0f, pend_lend = 0.0f;
+        // the block whose decay gradient is still pending: its partial sums
+        // (parity da_par), its scalars and row
+        bool da_pend = false, da_valid = false;
+        int da_par = 0;
+        float da_fac = 0.0f, da_lend = 0.0f, pend_fac = 0.0f, pend_lend = 0.0f;
+        int64_t da_t = 0;
+        uint32_t pend_par = 0;
 
         auto finish_block = [&]() -> bool {
             // Eg: outputs of block pend_j once Mf has completed
             const int jj = nblk - 1 - pend_j;
-            if (!epi_all(mbar_wait(&sm.mf_done, jj & 1, kWaitNs)) || *abort_flag)
+            if (!epi_all(mbar_wait(&sm.mf_done, jj & 1, wait_ns)) || *abort_flag)
                 return false;
             tc_fence_after();
             const int64_t t = d.start + (int64_t)pend_j * BT + r;
@@ -656,22 +672,35 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
             tc_fence_before();
             mbar_arrive(&sm.acc_free);
-            // decay gradient of the block (both halves compute it; half 0 stores)
-            const float X = (sm.colpart[0][r] + sm.colpart[1][r]) - (sm.rowpart[0][r] + sm.rowpart[1][r]) +
-                            (sm.kdpart[0][r] + sm.kdpart[1][r]);
-            const float Yv = sm.ypart[0][r] + sm.ypart[1][r];
+            // its decay gradient is summed up later, off the path to the next EA
+            da_pend = true;
+            da_valid = valid;
+            da_t = t;
+            da_par = (int)pend_par;
+            da_fac = pend_fac;
+            da_lend = pend_lend;
+            return true;
+        };
+
+        // decay gradient of the pending block (both halves compute it; half 0 stores)
+        auto block_da = [&]() {
+            const int bp = da_par;
+            const float X = (sm.colpart[bp][0][r] + sm.colpart[bp][1][r]) -
+                            (sm.rowpart[bp][0][r] + sm.rowpart[bp][1][r]) +
+                            (sm.kdpart[bp][0][r] + sm.kdpart[bp][1][r]);
+            const float Yv = sm.ypart[bp][0][r] + sm.ypart[bp][1][r];
             float tx, ty;
             const float px = block_exclusive_scan(X, sm.scan[0], q4, lane, tx);
             const float py = block_exclusive_scan(Yv, sm.scan[1], q4, lane, ty);
             float se = 0.0f;
 #pragma unroll
             for (int w = 0; w < 8; ++w)
-                se += sm.se[w];
-            const float C = expf(pend_lend) * se;
-            if (valid && half == 0)
-                da[(size_t)t * H + h] = (px + (ty - py) + C) * pend_fac;
-            epi_sync();   // scan scratch and the per-block partials are reused by the next block
-            return true;
+                se += sm.se[bp][w];
+            const float C = expf(da_lend) * se;
+            if (da_valid && half == 0)
+                da[(size_t)da_t * H + h] = (px + (ty - py) + C) * da_fac;
+            epi_sync();   // the scan scratch is reused by the next block
+            da_pend = false;
         };
 
         bool ok = true;
@@ -682,6 +711,11 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
+            if (stall == BDLA_STALL_EPILOGUE && jj == stall_blk) {
+                ok = epi_all(mbar_wait(&sm.never, 0, wait_ns));
+                if (!ok)
+                    break;
+            }
             // the decay scalars load overlaps the previous block's output stores
             const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
             const float fac = valid ? dfac[(int64_t)h * tokens + t0 + r] : 0.0f;
@@ -719,34 +753,20 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float wsc = valid ? expf(lend - lam_r) : 0.0f;
 
-            // ---- S_in row r -> bf16 copy (z) and <S_in, E>
+            const int bp = (int)par;   // parity of this block's partial sums
             if (st_tma) {
-                // the producer loaded S_in (bf16) into z
-                ok = epi_all(mbar_wait(&sm.full_z, par, kWaitNs)) && !*abort_flag;
+                // the producer loaded S_in (bf16) into z; <S_in, E> is taken in EA
+                ok = epi_all(mbar_wait(&sm.full_z, par, wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
-            }
-            {
+            } else {
+                // ---- S_in row r -> bf16 copy (z) and <S_in, E>
                 float se = 0.0f;
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
                     uint32_t e[32];
                     tmem_ld32(t_e + lane_off + c * 32, e);
                     unsigned char *zp = sm.z + (c >> 1) * kPanel;
-                    if (st_tma) {
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const uint4 zz = *reinterpret_cast<const uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4));
-                            const uint32_t w4[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                se = fmaf(bf16_lo(w4[i]), __uint_as_float(e[8 * k4 + 2 * i]), se);
-                                se = fmaf(bf16_hi(w4[i]), __uint_as_float(e[8 * k4 + 2 * i + 1]), se);
-                            }
-                        }
-                        continue;
-                    }
                     float s_in[32];
                     if (r < dk)
                         load_state_row(states, st_bf16, st_stride, n_slots, span.doc_start, n, h, span.blk_base + j, dk, dv, j0, r, s_in, c);
@@ -769,48 +789,56 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 se = warp_sum(se);
                 if (lane == 0)
-                    sm.se[warp - 2] = se;
+                    sm.se[bp][warp - 2] = se;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&sm.z_ready);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sm.z_ready);
 
             // ---- EA (P goes into x: the previous block's output stores are done reading it)
             if (warp == 2 && lane == 0)
                 tma_store_wait_read();
-            ok = epi_all(mbar_wait(&sm.m1_done, par, kWaitNs)) && !*abort_flag;
+            ok = epi_all(mbar_wait(&sm.m1_done, par, wait_ns)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
             if (ABL) {
                 // explicit position-pair path for the diagonal tile:
-                // P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}, dP_ts = (dO_t . v_s) e^{Gamma_t - Gamma_s}
+                // P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}, dP_ts = (dO_t . v_s) e^{Gamma_t - Gamma_s};
+                // each half takes 8 of the row's 16 pairs, reading each 16-byte
+                // chunk of its q and dO rows once
+                float pq[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                float pd[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                const int s0 = 16 * tau + 8 * half;
 #pragma unroll 1
-                for (int i = 8 * half; i < 8 * half + 8; ++i) {
-                    const int sc = 16 * tau + i;
-                    float pq = 0.0f, pd = 0.0f;
-                    if (valid && sc <= r) {
-                        for (int p = 0; p < kpan; ++p)
+                for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
-                                const uint4 kb = *reinterpret_cast<const uint4 *>(sm.k + p * kPanel + sw128_offset(sc, c8));
-                                pq = dot_bf16x8(qa, kb, pq);
-                            }
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
 #pragma unroll
-                        for (int p = 0; p < DV / 64; ++p)
-#pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 oa = *reinterpret_cast<const uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
-                                const uint4 vb = *reinterpret_cast<const uint4 *>(sm.v + p * kPanel + sw128_offset(sc, c8));
-                                pd = dot_bf16x8(oa, vb, pd);
-                            }
-                        const float e = expf(g - sm.gq[sc]);
-                        pq *= e;
-                        pd *= e;
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 kb = *reinterpret_cast<const uint4 *>(sm.k + p * kPanel + sw128_offset(s0 + i, c8));
+                            pq[i] = dot_bf16x8(qa, kb, pq[i]);
+                        }
                     }
-                    sm.dgp[r][i] = pq;
-                    sm.dgd[r][i] = pd;
+#pragma unroll 1
+                for (int p = 0; p < DV / 64; ++p)
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 oa = *reinterpret_cast<const uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 vb = *reinterpret_cast<const uint4 *>(sm.v + p * kPanel + sw128_offset(s0 + i, c8));
+                            pd[i] = dot_bf16x8(oa, vb, pd[i]);
+                        }
+                    }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int sc = s0 + i;
+                    const bool live = valid && sc <= r;
+                    const float e = live ? expf(g - sm.gq[sc]) : 0.0f;
+                    sm.dgp[r][8 * half + i] = pq[i] * e;
+                    sm.dgd[r][8 * half + i] = pd[i] * e;
                 }
                 epi_sync();   // all raw V rows read before any row is rescaled below
             }
@@ -878,42 +906,55 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
                         make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
             }
-            sm.rowpart[half][r] = rowsum;
-            // E -> bf16 copy (z)
+            sm.rowpart[bp][half][r] = rowsum;
+            // E in one pass: <S_in, E> with the S_in row in z (bf16 checkpoints),
+            // then the bf16 copy of E over it (z) and E <- e^{Lam_end} E in
+            // tensor memory (read only by Mf, after ea_done)
+            {
+                const float el = expf(lend);
+                float se = 0.0f;
 #pragma unroll
-            for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
-                uint32_t e[32];
-                tmem_ld32(t_e + lane_off + c * 32, e);
-                tmem_ld_wait();
-                uint32_t u[16];
+                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
+                    uint32_t e[32];
+                    tmem_ld32(t_e + lane_off + c * 32, e);
+                    tmem_ld_wait();
+                    unsigned char *zp = sm.z + (c >> 1) * kPanel;
+                    uint32_t u[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    u[i] = pack_bf16(__uint_as_float(e[2 * i]), __uint_as_float(e[2 * i + 1]));
-                unsigned char *zp = sm.z + (c >> 1) * kPanel;
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        uint4 *zq = reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4));
+                        if (st_tma) {
+                            const uint4 zz = *zq;
+                            const uint32_t w4[4] = {zz.x, zz.y, zz.z, zz.w};
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                    *reinterpret_cast<uint4 *>(zp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                        make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                            for (int i = 0; i < 4; ++i) {
+                                se = fmaf(bf16_lo(w4[i]), __uint_as_float(e[8 * k4 + 2 * i]), se);
+                                se = fmaf(bf16_hi(w4[i]), __uint_as_float(e[8 * k4 + 2 * i + 1]), se);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            u[4 * k4 + i] = pack_bf16(__uint_as_float(e[8 * k4 + 2 * i]),
+                                                      __uint_as_float(e[8 * k4 + 2 * i + 1]));
+                        *zq = make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        e[i] = __float_as_uint(__uint_as_float(e[i]) * el);
+                    tmem_st32(t_e + lane_off + c * 32, e);
+                }
+                if (st_tma) {
+                    se = warp_sum(se);
+                    if (lane == 0)
+                        sm.se[bp][warp - 2] = se;
+                }
+                tmem_st_wait();
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.ea_done);
 
             // ---- while Mb runs (it touches neither E nor C3):
-            // E <- e^{Lam_end} E
-            {
-                const float el = expf(lend);
-#pragma unroll
-                for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
-                    uint32_t e[32];
-                    tmem_ld32(t_e + lane_off + c * 32, e);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        e[i] = __float_as_uint(__uint_as_float(e[i]) * el);
-                    tmem_st32(t_e + lane_off + c * 32, e);
-                }
-            }
             // C3 <- e^{Lam_t} C3 (the inter-block part of dq) and Y_t = q_t . dq_inter_t
             float yv = 0.0f;
 #pragma unroll
@@ -938,12 +979,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
                 tmem_st32(t_c3 + lane_off + c * 32, x);
             }
-            sm.ypart[half][r] = yv;
+            sm.ypart[bp][half][r] = yv;
             tmem_st_wait();   // visible to Md and Mf through the fence before eb_done
 
             // ---- Eb: C1 <- w_s o C1 (the inter-block part of dk), k . dk_inter,
             //      then dP -> smem
-            ok = epi_all(mbar_wait(&sm.mb_done, par, kWaitNs)) && !*abort_flag;
+            ok = epi_all(mbar_wait(&sm.mb_done, par, wait_ns)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
@@ -969,7 +1010,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     x[i] = __float_as_uint(__uint_as_float(x[i]) * wsc);
                 tmem_st32(t_c1 + lane_off + c * 32, x);
             }
-            sm.kdpart[half][r] = kd * wsc;
+            sm.kdpart[bp][half][r] = kd * wsc;
 #pragma unroll
             for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
                 const int cc = c >> 1;
@@ -1012,7 +1053,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         }
                     }
                 }
-                sm.colpart[half][r] = vc;
+                sm.colpart[bp][half][r] = vc;
             }
 
             if (khat_v) {
@@ -1027,7 +1068,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
             } else {
                 // ---- Ee: K -> K o w_s in place once Md has read K
-                ok = epi_all(mbar_wait(&sm.md_done, par, kWaitNs)) && !*abort_flag;
+                ok = epi_all(mbar_wait(&sm.md_done, par, wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -1042,13 +1083,19 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.ee_done);
+            // the previous block's decay gradient, while Md and Mf run
+            if (da_pend)
+                block_da();
 
             pend_j = j;
             pend_fac = fac;
             pend_lend = lend;
+            pend_par = par;
         }
         if (ok && pend_j >= 0)
             ok = finish_block();
+        if (ok && da_pend)
+            block_da();
         if (ok && dh0 != nullptr && span.s == 0 && r < dk) {
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
@@ -1118,12 +1165,14 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
     const int slices = p.dv / DV;
     const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
     dim3 grid(p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs, slices);
+    const WaitCfg wc = wait_cfg(BDLA_KERNEL_BWD);
     kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma,
                                                 gamma, dfac, p.cu, p.T,
                                                 p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,
                                                 ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
-                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st);
+                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st,
+                                                wc.ns, wc.stall);
     if ((err = cudaGetLastError()) != cudaSuccess || slices == 1)
         return err;
     add_partials_kernel<<<1184, 256, 0, p.stream>>>(dq, dk, da, part, n_qk, n_a, slices - 1);

@@ -48,7 +48,8 @@ constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kFwdThreads = 64 + kEpiThreads;   // producer warp, MMA warp, epilogue
 constexpr uint32_t kPanel = 16384;  // one 128-row x 128-byte swizzled panel
-constexpr uint64_t kWaitNs = 2000000000ull;
+// drains of a CTA's own copies and MMAs before it exits keep the full limit
+constexpr uint64_t kWaitNs = kDefaultWaitNs;
 
 template <int DV>
 struct FwdSmem {
@@ -60,8 +61,10 @@ struct FwdSmem {
     float coff[BT];      // e^{gamma_sig - Gamma_s}
     float gq[BT];        // Gamma per row (ablation diagonal path)
     float gam[BT / kChunk];
+    uint32_t abl_pair[BT][4];   // ablation: one half's 8 position-pair values of a row (bf16 pairs)
     uint64_t full_qk[2], empty_qk[2], score_full[2];
     uint64_t full_v, empty_v, p_ready, o_full, p_free, drain;
+    uint64_t never;   // nothing arrives here: the wait of the stall test hook
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -117,7 +120,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                  float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
                  int64_t n_slots, int n_docs, int seg_blk, const float *__restrict__ seg_init,
-                 const int32_t *__restrict__ doc_order, DeviceStatus *st)
+                 const int32_t *__restrict__ doc_order, DeviceStatus *st, uint64_t wait_ns, int stall)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     FwdSmem<DV> &sm = *reinterpret_cast<FwdSmem<DV> *>(smem_raw);
@@ -139,6 +142,8 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         return;
     }
     const int nblk = (int)((d.len + BT - 1) / BT);
+    // test hook: the stalling role waits at this block (its second, or its only one)
+    const int stall_blk = nblk > 1 ? 1 : 0;
     const int kpan = dk / 64;
     const size_t sstride = (size_t)dk * dv;
     const int64_t unit = (int64_t)n * H + h;
@@ -161,6 +166,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.o_full, 1);
         mbar_init(&sm.p_free, 1);
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.never, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
     }
@@ -192,9 +198,13 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int j = 0; j < nblk; ++j) {
                 if (*abort_flag)
                     break;
+                if (stall == BDLA_STALL_PRODUCER && j == stall_blk && !mbar_wait(&sm.never, 0, wait_ns)) {
+                    consumed = false;
+                    break;
+                }
                 const int s = j & 1;
                 const int t0 = (int)(d.start + (int64_t)j * BT);
-                if (j >= 2 && !mbar_wait(&sm.empty_qk[s], ((j >> 1) - 1) & 1, kWaitNs)) {
+                if (j >= 2 && !mbar_wait(&sm.empty_qk[s], ((j >> 1) - 1) & 1, wait_ns)) {
                     consumed = false;
                     break;
                 }
@@ -205,7 +215,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tma_load_3d(sm.k[s] + p * kPanel, &tk, &sm.full_qk[s], p * 64, h, t0);
                 }
                 last_qk[s] = j;
-                if (j >= 1 && !mbar_wait(&sm.empty_v, (j - 1) & 1, kWaitNs)) {
+                if (j >= 1 && !mbar_wait(&sm.empty_v, (j - 1) & 1, wait_ns)) {
                     consumed = false;
                     break;
                 }
@@ -237,10 +247,10 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             bool ok = true;
             auto issue_qk = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs))
+                if (!mbar_wait(&sm.full_qk[s], (j >> 1) & 1, wait_ns))
                     return false;
                 // the P of block j - 2 (in this score buffer) has been read by its P V GEMM
-                if (j >= 2 && !mbar_wait(&sm.p_free, j & 1, kWaitNs))
+                if (j >= 2 && !mbar_wait(&sm.p_free, j & 1, wait_ns))
                     return false;
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks) {
@@ -255,13 +265,14 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 ok = issue_qk(0);
             for (int j = 0; ok && j < nblk; ++j) {
                 const int s = j & 1;
-                if (*abort_flag) {
+                if (*abort_flag ||
+                    (stall == BDLA_STALL_MMA && j == stall_blk && !mbar_wait(&sm.never, 0, wait_ns))) {
                     ok = false;
                     break;
                 }
                 if (!STATES && j + 1 < nblk && !(ok = issue_qk(j + 1)))
                     break;
-                if (!mbar_wait(&sm.p_ready, j & 1, kWaitNs) || !mbar_wait(&sm.full_v, j & 1, kWaitNs)) {
+                if (!mbar_wait(&sm.p_ready, j & 1, wait_ns) || !mbar_wait(&sm.full_v, j & 1, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -383,6 +394,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
+            if (stall == BDLA_STALL_EPILOGUE && j == stall_blk) {
+                ok = epi_all(mbar_wait(&sm.never, 0, wait_ns));
+                if (!ok)
+                    break;
+            }
             // ---- decay scalars of this block
             const float g = g_next;
             if (j + 1 < nblk) {
@@ -418,42 +434,56 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float ksc = valid ? expf(lend - lam_r) : 0.0f;
 
             if (STATES) {
-                ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+                ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, wait_ns)) && !*abort_flag;
             } else {
-                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, kWaitNs)) && !*abort_flag;
+                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, wait_ns)) && !*abort_flag;
             }
             if (!ok)
                 break;
             tc_fence_after();
 
             // explicit position-pair path for the diagonal tile (ablation): the
-            // warp whose columns hold the rows' diagonal tile (chunk q4) computes
-            // all 16 pairs of each row; they replace the GEMM values in P below
+            // two warps of a lane quarter each compute 8 of the 16 pairs of a
+            // row (half 0 the first 8), reading each 16-byte chunk of the q row
+            // once; the values replace the GEMM ones in P below, in the warp
+            // whose columns hold the rows' diagonal tile (chunk q4)
             uint32_t pair[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (ABL) {
-                if ((q4 & 1) == half) {
-                    float pr[16];
+                float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                const int s0 = 16 * tau + 8 * half;   // first key row of this half's pairs
 #pragma unroll 1
-                    for (int i = 0; i < 16; ++i) {
-                        const int sc = 16 * tau + i;
-                        float acc = 0.0f;
-                        if (valid && sc <= r) {
-                            for (int p = 0; p < kpan; ++p)
+                for (int p = 0; p < kpan; ++p)
 #pragma unroll
-                                for (int c8 = 0; c8 < 8; ++c8) {
-                                    const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
-                                    const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k[s] + p * kPanel + sw128_offset(sc, c8));
-                                    acc = dot_bf16x8(qa, kk, acc);
-                                }
-                            acc *= expf(g - sm.gq[sc]);
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q[s] + p * kPanel + sw128_offset(r, c8));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 kk = *reinterpret_cast<const uint4 *>(sm.k[s] + p * kPanel + sw128_offset(s0 + i, c8));
+                            acc[i] = dot_bf16x8(qa, kk, acc[i]);
                         }
-                        pr[i] = acc;
                     }
+                uint32_t mine[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pair[i] = pack_bf16(pr[2 * i], pr[2 * i + 1]);
+                for (int i = 0; i < 4; ++i) {
+                    const int sa = s0 + 2 * i, sb = sa + 1;
+                    const float va = (valid && sa <= r) ? acc[2 * i] * expf(g - sm.gq[sa]) : 0.0f;
+                    const float vb = (valid && sb <= r) ? acc[2 * i + 1] * expf(g - sm.gq[sb]) : 0.0f;
+                    mine[i] = pack_bf16(va, vb);
                 }
-                epi_sync();   // every thread is done with the raw K rows
+                const bool owner = (q4 & 1) == half;
+                if (!owner) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        sm.abl_pair[r][i] = mine[i];
+                }
+                epi_sync();   // every thread is done with the raw K rows; the other half's pairs are in
+                if (owner) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        pair[4 * half + i] = mine[i];
+                        pair[4 * (1 - half) + i] = sm.abl_pair[r][i];
+                    }
+                }
             }
             // ---- fold the decay into Q and K in place (row r, half the chunks)
 #pragma unroll 1
@@ -532,7 +562,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (j > 0) {
                 if (ck_tma && warp == 2 && lane == 0)
                     tma_store_wait_read();   // previous checkpoint store is done with sb
-                ok = epi_all(mbar_wait(&sm.o_full, (j - 1) & 1, kWaitNs)) && !*abort_flag;
+                ok = epi_all(mbar_wait(&sm.o_full, (j - 1) & 1, wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -607,7 +637,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         if (ck_tma && warp == 2 && lane == 0)
             tma_store_wait_read();
         if (ok && nblk > 0) {
-            ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, kWaitNs)) && !*abort_flag;
+            ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, wait_ns)) && !*abort_flag;
             if (ok) {
                 tc_fence_after();
                 if (!STATES)
@@ -710,9 +740,11 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
         return err;
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
     dim3 grid(p.dv / DV, p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs);
+    const WaitCfg wc = wait_cfg(STATES ? BDLA_KERNEL_STATES : BDLA_KERNEL_FWD);
     kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
                                                 p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
-                                                n_slots, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st);
+                                                n_slots, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st,
+                                                wc.ns, wc.stall);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,17 @@ inline const char *kernel_range_name(int kernel)
                                                    "bdla:states", "bdla:seg"};
     return names[kernel];
 }
+// Bounded waits (bdla_set_wait_limit_ns, bdla_set_test_stall): the limit of
+// the pipeline waits and, per kernel, the role that stalls (test hook).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+extern std::atomic<uint64_t> g_wait_ns;
+extern std::atomic<int> g_test_stall[BDLA_KERNEL_COUNT];
+struct WaitCfg {
+    uint64_t ns;   // limit of the pipeline waits
+    int stall;     // BDLA_STALL_* role that waits on a barrier nothing arrives at
+};
+inline WaitCfg wait_cfg(int kernel) { return WaitCfg{g_wait_ns.load(), g_test_stall[kernel].load()}; }
+
 // Scope of one kernel's launches: pushes the NVTX range and records the
 // caller's start event on entry, records the stop event and pops the range on
 // exit (early returns included).

@@ -39,7 +39,8 @@ constexpr int kStages = 3;
 constexpr int kRowThreads = 128;                       // warps 2-5: one token row each
 constexpr int kSegThreads = 64 + 2 * kRowThreads;      // + producer, MMA and 4 epilogue warps
 constexpr uint32_t kPanel = 16384;
-constexpr uint64_t kWaitNs = 2000000000ull;
+// drains of a CTA's own copies and MMAs before it exits keep the full limit
+constexpr uint64_t kWaitNs = kDefaultWaitNs;
 
 template <int DV>
 struct SegSmem {
@@ -47,6 +48,7 @@ struct SegSmem {
     alignas(1024) unsigned char y[kStages][(DV / 64) * kPanel];  // rows: tokens, panels: dv
     float gam[BT / kChunk];
     uint64_t full[kStages], xready[kStages], empty[kStages], acc_full[2], acc_free[2], drain;
+    uint64_t never;   // nothing arrives here: the wait of the stall test hook
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -91,7 +93,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty,
                    const float *__restrict__ gamma, const int32_t *__restrict__ cu, int T,
                    int64_t tokens, int n_docs, int H, int dk, int dv, int seg_blk, int64_t n_items,
-                   float *__restrict__ sums, float *__restrict__ lsum, DeviceStatus *st)
+                   float *__restrict__ sums, float *__restrict__ lsum, DeviceStatus *st,
+                   uint64_t wait_ns, int stall)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     SegSmem<DV> &sm = *reinterpret_cast<SegSmem<DV> *>(smem_raw);
@@ -127,6 +130,7 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
             mbar_init(&sm.acc_free[a], kRowThreads);
         }
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.never, 1);
         sm.abort_flag = 0;
         mbar_fence_init();
     }
@@ -158,7 +162,9 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
                 for (int b = 0; b < nblk; ++b, ++gb) {
                     const int j = BWD ? b : nblk - 1 - b;
                     const int s = (int)(gb % kStages);
-                    if (*abort_flag || (gb >= kStages && !mbar_wait(&sm.empty[s], ((gb / kStages) - 1) & 1, kWaitNs))) {
+                    // (test hook: the stalling role waits at its CTA's second block)
+                    if (*abort_flag || (stall == BDLA_STALL_PRODUCER && gb == 1 && !mbar_wait(&sm.never, 0, wait_ns)) ||
+                        (gb >= kStages && !mbar_wait(&sm.empty[s], ((gb / kStages) - 1) & 1, wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -191,13 +197,14 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
                 if (nblk <= 0)
                     continue;
                 const int a = (int)(la & 1);
-                if (la >= 2 && !mbar_wait(&sm.acc_free[a], ((la / 2) - 1) & 1, kWaitNs)) {
+                if (la >= 2 && !mbar_wait(&sm.acc_free[a], ((la / 2) - 1) & 1, wait_ns)) {
                     ok = false;
                     break;
                 }
                 for (int b = 0; b < nblk; ++b, ++gb) {
                     const int s = (int)(gb % kStages);
-                    if (*abort_flag || !mbar_wait(&sm.xready[s], (gb / kStages) & 1, kWaitNs)) {
+                    if (*abort_flag || (stall == BDLA_STALL_MMA && gb == 1 && !mbar_wait(&sm.never, 0, wait_ns)) ||
+                        !mbar_wait(&sm.xready[s], (gb / kStages) & 1, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -256,7 +263,9 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
                 const float c = BWD ? run + lam : run + (lend - lam);
                 const float w = valid ? expf(c) : 0.0f;
                 run += lend;
-                ok = row_all(mbar_wait(&sm.full[s], (gb / kStages) & 1, kWaitNs)) && !*abort_flag;
+                ok = row_all(mbar_wait(&sm.full[s], (gb / kStages) & 1, wait_ns) &&
+                             !(stall == BDLA_STALL_EPILOGUE && gb == 1 && !mbar_wait(&sm.never, 0, wait_ns))) &&
+                     !*abort_flag;
                 if (!ok)
                     break;
 #pragma unroll 1
@@ -293,7 +302,7 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
             const size_t base = ((size_t)slot * H + h) * (size_t)dk * dv;
             const int a = (int)(la & 1);
             if (nblk > 0) {
-                if (!mbar_wait(&sm.acc_full[a], (la / 2) & 1, kWaitNs) || *abort_flag) {
+                if (!mbar_wait(&sm.acc_full[a], (la / 2) & 1, wait_ns) || *abort_flag) {
                     ok = false;
                     break;
                 }
@@ -430,6 +439,7 @@ cudaError_t launch_seg_summary(const Problem &p, const __nv_bfloat16 *x, const _
     const int64_t n_items = (int64_t)(p.dv / DVs) * p.H * seg.n_slots;
     const int64_t n_cta = n_items < sm_count() ? n_items : sm_count();
     dim3 grid((unsigned)n_cta);
+    const WaitCfg wc = wait_cfg(BDLA_KERNEL_SEG);
     cudaError_t err;
 #define BDLA_SEG_GO(DV_, B_)                                                                       \
     do {                                                                                           \
@@ -440,7 +450,7 @@ cudaError_t launch_seg_summary(const Problem &p, const __nv_bfloat16 *x, const _
             return err;                                                                            \
         kern<<<grid, kSegThreads, smem, p.stream>>>(mx, my, gamma, p.cu, p.T, p.tokens, p.n_docs, \
                                                     p.H, p.dk, p.dv, seg.seg_blk, n_items,         \
-                                                    seg.buf, seg.lsum, p.st);                      \
+                                                    seg.buf, seg.lsum, p.st, wc.ns, wc.stall);     \
     } while (0)
     if (DVs == 64) {
         if (backward)

@@ -112,6 +112,34 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None) -> dict:
     return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu)
 
 
+def make_inputs_on(w: Workload, device, with_grad: bool = True) -> dict:
+    """The same recipe drawn directly on `device` with a device generator
+    seeded from the workload (values differ from make_inputs' CPU draws; the
+    distributions and shapes are the same).  For timing runs that compare
+    nothing with the oracle and would otherwise spend a minute drawing
+    billion-element tensors on the host."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    cu = None
+    if w.n_docs:
+        gc = torch.Generator(device="cpu")
+        gc.manual_seed(w.seed)
+        lens = doc_lengths(w, gc)
+        cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32).to(device)
+    rn = lambda shape: torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    q = (rn((B, T, H, dk)) * (1.0 / math.sqrt(dk))).to(torch.bfloat16)
+    k32 = rn((B, T, H, dk))
+    k = (k32 / k32.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(torch.bfloat16)
+    del k32
+    v = rn((B, T, H, dv)).to(torch.bfloat16)
+    a = (rn((B, T, H)) * w.a_std + w.a_mean).contiguous()
+    dO = rn((B, T, H, dv)).to(torch.bfloat16) if with_grad else None
+    n_seq = (cu.numel() - 1) if cu is not None else B
+    h0 = (rn((n_seq, H, dk, dv)) * w.h0_std) if w.h0_std > 0 else None
+    return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu)
+
+
 def small_variant(w: Workload, T: int, H: Optional[int] = None, n_docs: Optional[int] = None,
                   seed_offset: int = 0) -> Workload:
     """Same recipe at a size the oracle finishes in seconds."""

@@ -51,6 +51,29 @@ enum { BDLA_KERNEL_DECAY = 0, BDLA_KERNEL_FWD = 1, BDLA_KERNEL_BWD = 2, BDLA_KER
        BDLA_KERNEL_SEG = 4, BDLA_KERNEL_COUNT = 5 };
 bdla_status bdla_set_kernel_events(int kernel, void *start_event, void *stop_event);
 
+/*
+ * Test hooks for the bounded waits.  Every wait of a kernel's pipeline
+ * (a TMA copy landing, an MMA completing, a hand-off between warps) gives up
+ * after a time limit instead of spinning forever; the CTA then records
+ * BDLA_ERR_TIMEOUT in the call's status word, lets the copies and MMAs it
+ * started finish, frees its tensor memory and returns, so the CUDA context
+ * stays usable.  These two settings let a test exercise that path.
+ *
+ * bdla_set_wait_limit_ns: limit of the pipeline waits in nanoseconds for
+ * later launches (default 2 s; 0 restores the default).  The waits that
+ * drain a CTA's own copies and MMAs before it exits keep the default.
+ *
+ * bdla_set_test_stall: until called again with role 0, every later launch
+ * of kernel `kernel` (BDLA_KERNEL_FWD, _BWD, _STATES or _SEG) makes the
+ * warp(s) of one role wait, at their second block (their first if there is
+ * one block), on a barrier that nothing arrives at; the wait runs out after
+ * the limit above.  Returns BDLA_ERR_SHAPE for an unknown kernel or role.
+ * Off by default; not for production use.
+ */
+enum { BDLA_STALL_NONE = 0, BDLA_STALL_PRODUCER = 1, BDLA_STALL_MMA = 2, BDLA_STALL_EPILOGUE = 3 };
+bdla_status bdla_set_wait_limit_ns(uint64_t ns);
+bdla_status bdla_set_test_stall(int kernel, int role);
+
 #ifdef __cplusplus
 }
 #endif
