@@ -5,7 +5,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 package imports nothing from it.
 
 The arithmetic lives in ``bdla_oracle.c`` (token-by-token recurrence and its
-reverse mode, see the header there for the reading of the pages).  This module
+reverse mode, see the header there for the reading of the pages; the
+per-channel decay variant is ``fwd_vec`` / ``bwd_vec``).  This module
 only compiles it with gcc and marshals numpy float64 arrays through ctypes.
 """
 from __future__ import annotations
@@ -52,6 +53,10 @@ def _load():
                                        dp, dp, dp, dp, ctypes.c_double, ctypes.c_int, dp,
                                        dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int]
             lib.oracle_bwd.restype = ctypes.c_int
+            lib.oracle_fwd_vec.argtypes = lib.oracle_fwd.argtypes
+            lib.oracle_fwd_vec.restype = ctypes.c_int
+            lib.oracle_bwd_vec.argtypes = lib.oracle_bwd.argtypes
+            lib.oracle_bwd_vec.restype = ctypes.c_int
             lib.oracle_log_decay.argtypes = [ctypes.c_int64, dp, ctypes.c_double, ctypes.c_int, dp]
             lib.oracle_log_decay.restype = ctypes.c_int
             _lib = lib
@@ -120,6 +125,47 @@ def bwd(q, k, v, a, dO, b=-5.0, mode=BOUNDED, h0=None, dhT=None, cu_seqlens=None
                        _ptr(q), _ptr(k), _ptr(v), _ptr(a), float(b), int(mode), _ptr(h0),
                        _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(da),
                        _ptr(dh0), int(window), int(nthreads))
+    return dq, dkk, dvv, da, dh0
+
+
+def fwd_vec(q, k, v, a, b=-5.0, mode=BOUNDED, h0=None, cu_seqlens=None, nthreads=0):
+    """Forward recurrence with one log-decay per key channel:
+    S_t = diag(exp(lambda_t)) S_{t-1} + k_t v_t^T.  a [T,H,dk]; otherwise as
+    ``fwd``.  Returns (o, hT), float64."""
+    q, k, v, a, h0 = _f64(q), _f64(k), _f64(v), _f64(a), _f64(h0)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    assert a.shape == (T, H, dk)
+    cu = _cu(cu_seqlens, T)
+    N = cu.size - 1
+    assert cu[0] == 0 and cu[-1] == T
+    o = np.zeros((T, H, dv))
+    hT = np.zeros((N, H, dk, dv))
+    _load().oracle_fwd_vec(N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), H, dk, dv,
+                           _ptr(q), _ptr(k), _ptr(v), _ptr(a), float(b), int(mode), _ptr(h0),
+                           _ptr(o), _ptr(hT), int(nthreads))
+    return o, hT
+
+
+def bwd_vec(q, k, v, a, dO, b=-5.0, mode=BOUNDED, h0=None, dhT=None, cu_seqlens=None,
+            window=1024, nthreads=0):
+    """Reverse mode of ``fwd_vec`` for the loss <o, dO> + <hT, dhT>.  Returns
+    (dq, dk, dv, da, dh0) with da [T,H,dk], float64."""
+    q, k, v, a, dO, h0, dhT = (_f64(x) for x in (q, k, v, a, dO, h0, dhT))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    assert a.shape == (T, H, dk)
+    cu = _cu(cu_seqlens, T)
+    N = cu.size - 1
+    dq = np.zeros_like(q)
+    dkk = np.zeros_like(k)
+    dvv = np.zeros_like(v)
+    da = np.zeros_like(a)
+    dh0 = np.zeros((N, H, dk, dv))
+    _load().oracle_bwd_vec(N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), H, dk, dv,
+                           _ptr(q), _ptr(k), _ptr(v), _ptr(a), float(b), int(mode), _ptr(h0),
+                           _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(da),
+                           _ptr(dh0), int(window), int(nthreads))
     return dq, dkk, dvv, da, dh0
 
 

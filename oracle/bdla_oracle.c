@@ -259,3 +259,200 @@ int oracle_bwd(int N, const int64_t *cu, int H, int dk, int dv,
     }
     return used;
 }
+
+/*
+ * Per-channel (vector) decay, the variant the first page's "per-position
+ * cumulative decay" ([P1] sec. 3.1) also admits: one log-decay per (token,
+ * head, key channel) with the same two parameterisations ([P1] sec. 3.2),
+ *     lambda_t[i] = b * sigmoid(a_t[i])   or   -softplus(a_t[i]),
+ *     S_t = diag(exp(lambda_t)) S_{t-1} + k_t v_t^T,   S_0 = h0,
+ *     o_t = S_t^T q_t,                                 hT = S_L,
+ * i.e. row i of the dk x dv state decays by its own factor.  Layouts as
+ * above except a, da: [Ttot][H][dk].
+ */
+int oracle_fwd_vec(int N, const int64_t *cu, int H, int dk, int dv,
+                   const double *q, const double *k, const double *v,
+                   const double *a, double b, int mode, const double *h0,
+                   double *o, double *hT, int nthreads)
+{
+    int used = set_threads(nthreads);
+    const int64_t units = (int64_t)N * H;
+    const size_t ssz = (size_t)dk * dv;
+
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(ssz * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < units; ++u) {
+            const int n = (int)(u / H), h = (int)(u % H);
+            if (h0)
+                memcpy(S, h0 + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(S, 0, ssz * sizeof(double));
+            for (int64_t t = cu[n]; t < cu[n + 1]; ++t) {
+                const double *at = a + ((size_t)t * H + h) * dk;
+                const double *qt = q + ((size_t)t * H + h) * dk;
+                const double *kt = k + ((size_t)t * H + h) * dk;
+                const double *vt = v + ((size_t)t * H + h) * dv;
+                double *ot = o + ((size_t)t * H + h) * dv;
+                /* S_t = diag(g_t) S_{t-1} + k_t v_t^T: row i decays by g_t[i] */
+                for (int i = 0; i < dk; ++i) {
+                    const double gi = exp(log_decay(at[i], b, mode));
+                    double *Si = S + (size_t)i * dv;
+                    const double ki = kt[i];
+                    for (int j = 0; j < dv; ++j)
+                        Si[j] = gi * Si[j] + ki * vt[j];
+                }
+                /* o_t = S_t^T q_t */
+                for (int j = 0; j < dv; ++j)
+                    ot[j] = 0.0;
+                for (int i = 0; i < dk; ++i) {
+                    const double *Si = S + (size_t)i * dv;
+                    const double qi = qt[i];
+                    for (int j = 0; j < dv; ++j)
+                        ot[j] += qi * Si[j];
+                }
+            }
+            if (hT)
+                memcpy(hT + (size_t)u * ssz, S, ssz * sizeof(double));
+        }
+        free(S);
+    }
+    return used;
+}
+
+/*
+ * Reverse mode of oracle_fwd_vec.  With D the adjoint of S_t:
+ *   D += q_t dO_t^T;  dq_t = S_t dO_t;  dk_t = D v_t;  dv_t = D^T k_t;
+ *   dlambda_t[i] = g_t[i] sum_j D[i][j] S_{t-1}[i][j];  D <- diag(g_t) D;
+ *   dh0 = D at the end.  S_{t-1} comes from fp64 checkpoints every `window`
+ * tokens, recomputed forward inside each window.
+ */
+int oracle_bwd_vec(int N, const int64_t *cu, int H, int dk, int dv,
+                   const double *q, const double *k, const double *v,
+                   const double *a, double b, int mode, const double *h0,
+                   const double *dO, const double *dhT,
+                   double *dq, double *dkk, double *dvv, double *da,
+                   double *dh0, int window, int nthreads)
+{
+    int used = set_threads(nthreads);
+    const int64_t units = (int64_t)N * H;
+    const size_t ssz = (size_t)dk * dv;
+    if (window <= 0)
+        window = 1024;
+
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(ssz * sizeof(double));
+        double *D = (double *)malloc(ssz * sizeof(double));
+        double *g = (double *)malloc((size_t)dk * sizeof(double));
+        double *win = (double *)malloc((size_t)window * ssz * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < units; ++u) {
+            const int n = (int)(u / H), h = (int)(u % H);
+            const int64_t t0 = cu[n], L = cu[n + 1] - cu[n];
+            const int64_t nwin = (L + window - 1) / window;
+            double *ck = (double *)malloc((size_t)(nwin > 0 ? nwin : 1) * ssz * sizeof(double));
+
+            /* forward sweep: checkpoint S before each window */
+            if (h0)
+                memcpy(S, h0 + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(S, 0, ssz * sizeof(double));
+            for (int64_t t = 0; t < L; ++t) {
+                if (t % window == 0)
+                    memcpy(ck + (size_t)(t / window) * ssz, S, ssz * sizeof(double));
+                const int64_t tt = t0 + t;
+                const double *at = a + ((size_t)tt * H + h) * dk;
+                const double *kt = k + ((size_t)tt * H + h) * dk;
+                const double *vt = v + ((size_t)tt * H + h) * dv;
+                for (int i = 0; i < dk; ++i) {
+                    const double gi = exp(log_decay(at[i], b, mode));
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)i * dv + j] = gi * S[(size_t)i * dv + j] + kt[i] * vt[j];
+                }
+            }
+
+            if (dhT)
+                memcpy(D, dhT + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(D, 0, ssz * sizeof(double));
+
+            for (int64_t w = nwin - 1; w >= 0; --w) {
+                const int64_t ws = w * window;
+                const int64_t we = (ws + window < L) ? ws + window : L;
+                memcpy(S, ck + (size_t)w * ssz, ssz * sizeof(double));
+                for (int64_t t = ws; t < we; ++t) {
+                    memcpy(win + (size_t)(t - ws) * ssz, S, ssz * sizeof(double));
+                    const int64_t tt = t0 + t;
+                    const double *at = a + ((size_t)tt * H + h) * dk;
+                    const double *kt = k + ((size_t)tt * H + h) * dk;
+                    const double *vt = v + ((size_t)tt * H + h) * dv;
+                    for (int i = 0; i < dk; ++i) {
+                        const double gi = exp(log_decay(at[i], b, mode));
+                        for (int j = 0; j < dv; ++j)
+                            S[(size_t)i * dv + j] = gi * S[(size_t)i * dv + j] + kt[i] * vt[j];
+                    }
+                }
+                for (int64_t t = we - 1; t >= ws; --t) {
+                    const int64_t tt = t0 + t;
+                    const double *at = a + ((size_t)tt * H + h) * dk;
+                    const double *qt = q + ((size_t)tt * H + h) * dk;
+                    const double *kt = k + ((size_t)tt * H + h) * dk;
+                    const double *vt = v + ((size_t)tt * H + h) * dv;
+                    const double *gt = dO + ((size_t)tt * H + h) * dv;
+                    double *dqt = dq + ((size_t)tt * H + h) * dk;
+                    double *dkt = dkk + ((size_t)tt * H + h) * dk;
+                    double *dvt = dvv + ((size_t)tt * H + h) * dv;
+                    double *dat = da + ((size_t)tt * H + h) * dk;
+                    const double *Sp = win + (size_t)(t - ws) * ssz; /* S_{t-1} */
+                    for (int i = 0; i < dk; ++i)
+                        g[i] = exp(log_decay(at[i], b, mode));
+                    /* D += q_t dO_t^T  (adjoint of S_t) */
+                    for (int i = 0; i < dk; ++i)
+                        for (int j = 0; j < dv; ++j)
+                            D[(size_t)i * dv + j] += qt[i] * gt[j];
+                    /* dq_t = S_t dO_t with S_t = diag(g) S_{t-1} + k v^T */
+                    for (int i = 0; i < dk; ++i) {
+                        double acc = 0.0;
+                        for (int j = 0; j < dv; ++j)
+                            acc += (g[i] * Sp[(size_t)i * dv + j] + kt[i] * vt[j]) * gt[j];
+                        dqt[i] = acc;
+                    }
+                    /* dk_t = D v_t */
+                    for (int i = 0; i < dk; ++i) {
+                        double acc = 0.0;
+                        for (int j = 0; j < dv; ++j)
+                            acc += D[(size_t)i * dv + j] * vt[j];
+                        dkt[i] = acc;
+                    }
+                    /* dv_t = D^T k_t */
+                    for (int j = 0; j < dv; ++j)
+                        dvt[j] = 0.0;
+                    for (int i = 0; i < dk; ++i)
+                        for (int j = 0; j < dv; ++j)
+                            dvt[j] += D[(size_t)i * dv + j] * kt[i];
+                    /* dlambda_t[i] = g_t[i] <D[i,:], S_{t-1}[i,:]>;  da = dlambda * dlambda/da */
+                    for (int i = 0; i < dk; ++i) {
+                        double dot = 0.0;
+                        for (int j = 0; j < dv; ++j)
+                            dot += D[(size_t)i * dv + j] * Sp[(size_t)i * dv + j];
+                        dat[i] = g[i] * dot * log_decay_deriv(at[i], b, mode);
+                    }
+                    /* adjoint of S_{t-1}: row i decays by g_t[i] */
+                    for (int i = 0; i < dk; ++i)
+                        for (int j = 0; j < dv; ++j)
+                            D[(size_t)i * dv + j] *= g[i];
+                }
+            }
+            if (dh0)
+                memcpy(dh0 + (size_t)u * ssz, D, ssz * sizeof(double));
+            free(ck);
+        }
+        free(win);
+        free(g);
+        free(D);
+        free(S);
+    }
+    return used;
+}
