@@ -74,7 +74,11 @@ def peaks():
 
 # ---------------------------------------------------------------- algorithmic bytes
 def algorithmic_bytes(w, n_seq):
-    """Bytes the method must move at minimum (fwd, bwd, per kernel)."""
+    """Bytes the method must move at minimum (fwd, bwd, per kernel).  With
+    fp32 state checkpoints every `ckpt_stride` tokens (a config that asks for
+    them), the checkpoints are outputs: the forward writes the 128-token block
+    starts, the expansion kernel ("states") the ones inside each block, and
+    the backward reads one per block."""
     th = w.B * w.T * w.H
     units = n_seq * w.H
     st = w.dk * w.dv * 4
@@ -82,7 +86,15 @@ def algorithmic_bytes(w, n_seq):
     bwd = th * (2 * w.dk * 2 + 2 * w.dv * 2 + 4 + 4 * w.dk * 2 + 4 * w.dv + 4) + \
         (units * st if w.h0_std else 0)
     decay = th * 8
-    return {"fwd": fwd, "bwd": bwd, "decay": decay}
+    out = {"fwd": fwd, "bwd": bwd, "decay": decay}
+    if w.ckpt_stride and w.ckpt_stride < 128:
+        per_block = 128 // w.ckpt_stride
+        blocks = w.B * w.T // 128 * w.H
+        out["fwd"] = fwd + blocks * st
+        # k, v (bf16) and the tile cumsums read; the inner checkpoints written
+        out["states"] = th * (2 * w.dk + 2 * w.dv + 4) + blocks * (per_block - 1) * st
+        out["bwd"] = bwd + blocks * st
+    return out
 
 
 # ---------------------------------------------------------------- DRAM traffic
@@ -280,11 +292,15 @@ def ours_arm(args, w, inp):
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     n_seq = (g["cu_seqlens"].numel() - 1) if g["cu_seqlens"] is not None else w.B
     ws_f = B.Workspace(B.workspace_bytes(B.OP_FWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode), dev)
-    ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode, ckpt_stride=128), dev)
+    # the forward hands the backward bf16 states every 128 tokens, unless the
+    # config asks for fp32 state checkpoints at a finer stride: then those are
+    # written (block starts by the forward, the rest by the expansion kernel)
+    # and the backward reads them
+    stride = w.ckpt_stride if w.ckpt_stride else 128
+    ck_dtype = torch.float32 if w.ckpt_stride else torch.bfloat16
+    ws_b = B.Workspace(B.workspace_bytes(B.OP_BWD, tuple(g["q"].shape), w.dv, n_seq if g["cu_seqlens"] is not None else 0, w.mode, ckpt_stride=stride), dev)
     o = torch.empty(g["v"].shape, dtype=torch.bfloat16, device=dev)
-    # the forward hands the backward bf16 states every 128 tokens
-    ck = torch.empty((w.H, B.n_slots(w.B * w.T, n_seq, 128), w.dk, w.dv), dtype=torch.bfloat16,
-                     device=dev)
+    ck = torch.empty((w.H, B.n_slots(w.B * w.T, n_seq, stride), w.dk, w.dv), dtype=ck_dtype, device=dev)
     hT = torch.empty((n_seq, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
             torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
@@ -295,9 +311,9 @@ def ours_arm(args, w, inp):
     def step(src):
         bdla.fwd(src["q"], src["k"], src["v"], src["a"], w.b, h0=src["h0"],
                  cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_f, out=o, hT_out=hT,
-                 ckpt_stride=128, ckpt_out=ck)
+                 ckpt_stride=stride, ckpt_dtype=ck_dtype, ckpt_out=ck)
         bdla.bwd(src["q"], src["k"], src["v"], src["a"], src["dO"], w.b, h0=src["h0"],
-                 cu_seqlens=src["cu_seqlens"], ckpt=ck, ckpt_stride=128, mode=w.mode, ws=ws_b,
+                 cu_seqlens=src["cu_seqlens"], ckpt=ck, ckpt_stride=stride, mode=w.mode, ws=ws_b,
                  outs=outs)
 
     kernels = {"decay": B.KERNEL_DECAY, "fwd": B.KERNEL_FWD, "bwd": B.KERNEL_BWD,
@@ -307,7 +323,9 @@ def ours_arm(args, w, inp):
     # the document order in each;  segments: summary + scan in each;  dv = 256:
     # the backward adds the second slice's partial sums
     ordered = g["cu_seqlens"] is not None and not seg and 1 < n_seq <= 4096
-    launches_per_step = 4 + (2 if ordered else 0) + (4 if seg else 0) + (1 if w.dv > 128 else 0)
+    # fp32 checkpoints inside the 128-token blocks: one expansion launch
+    launches_per_step = 4 + (2 if ordered else 0) + (4 if seg else 0) + (1 if w.dv > 128 else 0) + \
+        (1 if w.ckpt_stride and w.ckpt_stride < 128 else 0)
 
     def barrier():
         replicas.barrier(world)
@@ -376,9 +394,9 @@ def ours_arm(args, w, inp):
         do, dhT_, dq_, dk_, dv_, da_ = dst
         bdla.fwd(src["q"], src["k"], src["v"], src["a"], w.b, h0=src["h0"],
                  cu_seqlens=src["cu_seqlens"], mode=w.mode, ws=ws_f, out=do, hT_out=dhT_,
-                 ckpt_stride=128, ckpt_out=ck)
+                 ckpt_stride=stride, ckpt_dtype=ck_dtype, ckpt_out=ck)
         bdla.bwd(src["q"], src["k"], src["v"], src["a"], src["dO"], w.b, h0=src["h0"],
-                 cu_seqlens=src["cu_seqlens"], ckpt=ck, ckpt_stride=128, mode=w.mode, ws=ws_b,
+                 cu_seqlens=src["cu_seqlens"], ckpt=ck, ckpt_stride=stride, mode=w.mode, ws=ws_b,
                  outs=(dq_, dk_, dv_, da_))
 
     def e2e_run(n):
@@ -428,8 +446,11 @@ def ours_arm(args, w, inp):
     e2e_value = replicas.job_throughput(tokens, world, e2e_ms)
     hbm, hbm_src = peaks()
     ab = algorithmic_bytes(w, n_seq)
-    dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
+    dom = max((n for n in ("fwd", "bwd", "states") if n in ab), key=lambda n: kernel_ms[n])
     achieved = ab[dom] / (kernel_ms[dom] / 1000.0) / 1e9
+    per_kernel = {n: {"ms": kernel_ms[n], "algorithmic_bytes": ab[n],
+                      "frac": ab[n] / (kernel_ms[n] / 1000.0) / 1e9 / hbm}
+                  for n in ("decay", "fwd", "states", "bwd") if n in ab and kernel_ms[n] > 0}
     abl = None
     if world == 1 and not args.no_ablation:
         abl = ablation_leg(dev)
@@ -448,6 +469,8 @@ def ours_arm(args, w, inp):
                             "traffic": measured_traffic(dom, w.name),
                             "algorithmic_bytes_per_launch": ab[dom]},
                "kernel_ms": kernel_ms,
+               "kernel_roofline": per_kernel,
+               "ckpt": {"stride": stride, "dtype": "f32" if w.ckpt_stride else "bf16"},
                "seq_segments": seg,
                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h},
@@ -513,6 +536,80 @@ def ablation_leg(dev, steps: int = 5, warmup: int = 3):
     return {"workload": "1M-token stage, T=1048576, H=8, dk=dv=128, fwd+bwd step",
             "bounded_ms": res["c1m"], "ablation_ms": res["c1m_ablation"],
             "ablation_over_bounded": res["c1m_ablation"] / res["c1m"], "steps": steps}
+
+
+def vec_arm(args, w, inp):
+    """Per-channel decay (bdla_fwd_vec / bdla_bwd_vec): one fwd+bwd step on
+    the packed 64K-stage documents with one decay logit per key channel.
+    Single GPU; one JSON line.  The roofline numerator counts the bytes the
+    method must move: q, k, v (bf16), a (fp32, dk per token-head), o (bf16);
+    backward q, k, v, dO, a in and dq, dk, dv, da (fp32) out."""
+    import torch
+
+    from chunked_linear_attention_bounded_gb300 import bdla as B
+    dev = torch.device("cuda", 0)
+    g = {k_: (v_.to(dev) if v_ is not None else None) for k_, v_ in inp.items()}
+    n_seq = (g["cu_seqlens"].numel() - 1) if g["cu_seqlens"] is not None else w.B
+    nd = n_seq if g["cu_seqlens"] is not None else 0
+    Dm = B.Dims(w.B, w.T, w.H, w.dk, w.dv)
+    ws_f = B.Workspace(B.lib().bdla_workspace_bytes_vec(B.OP_FWD, Dm, nd), dev)
+    ws_b = B.Workspace(B.lib().bdla_workspace_bytes_vec(B.OP_BWD, Dm, nd), dev)
+    outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["v"].shape, dtype=torch.float32, device=dev),
+            torch.empty(g["a"].shape, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"], mode=w.mode,
+                  ws=ws_f)
+        B.bwd_vec(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                  mode=w.mode, ws=ws_b, outs=outs)
+    kernels = {"fwd": B.KERNEL_FWD, "states": B.KERNEL_STATES, "bwd": B.KERNEL_BWD}
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    kev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+           for n in kernels}
+    for pairs in kev.values():
+        for a_, b_ in pairs:
+            a_.record(stream)
+            b_.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for i in range(K):
+            for n, kid in kernels.items():
+                B.set_kernel_events(kid, *kev[n][i])
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    for kid in kernels.values():
+        B.set_kernel_events(kid, None, None)
+    for code in (ws_f.read_device_status(), ws_b.read_device_status()):
+        if code:
+            raise RuntimeError(f"device status {code}")
+    ms = e0.elapsed_time(e1) / K
+    kernel_ms = {n: sum(a_.elapsed_time(b_) for a_, b_ in kev[n]) / K for n in kernels}
+    th = w.B * w.T * w.H
+    st = w.dk * w.dv * 4 * n_seq * w.H
+    ab = {"fwd": th * (2 * w.dk * 2 + 2 * w.dv + 4 * w.dk + 2 * w.dv) + 2 * st,
+          "bwd": th * (2 * w.dk * 2 + 2 * w.dv * 2 + 4 * w.dk + 4 * w.dk * 2 + 4 * w.dv + 4 * w.dk) + st}
+    hbm, hbm_src = peaks()
+    dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
+    achieved = ab[dom] / (kernel_ms[dom] / 1000.0) / 1e9
+    tokens = w.B * w.T
+    out = {"metric": "tokens/s fwd+bwd, per-channel decay (T=64K packed, H=32, d=128, bf16)",
+           "value": tokens / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+           "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, 1),
+           "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                        "frac": achieved / hbm, "peak_source": hbm_src, "traffic": None,
+                        "algorithmic_bytes_per_launch": ab[dom]},
+           "kernel_ms": kernel_ms, "gpu_launches": 3 * K, "clocks": clk.summary()}
+    print(json.dumps(out), flush=True)
 
 
 def decode_arm(args):
@@ -585,7 +682,12 @@ def main():
         return
     inp = make_inputs(w, with_grad=True)
     if args.impl == "reference":
+        if w.vec:
+            print(json.dumps({"impl": "reference", "unavailable": "the per-channel mode has no oracle timing arm"}))
+            return
         reference_arm(args, w, inp)
+    elif w.vec:
+        vec_arm(args, w, inp)
     else:
         ours_arm(args, w, inp)
 

@@ -4,8 +4,8 @@ The compute lives in libbdla.so (C ABI declared in include/bdla.h); this
 package holds the CUDA sources (csrc/), their build script, a thin ctypes
 binding and the seeded synthetic input generator.
 """
-from .bdla import (BOUNDED, CHUNK, SOFTPLUS, BdlaError, Workspace, bwd, decay, decode,  # noqa: F401
-                   fwd, lib, n_slots, workspace_bytes)
+from .bdla import (BOUNDED, CHUNK, SOFTPLUS, BdlaError, Workspace, bwd, bwd_vec, decay,  # noqa: F401
+                   decode, fwd, fwd_vec, lib, n_slots, workspace_bytes)
 
-__all__ = ["BOUNDED", "SOFTPLUS", "CHUNK", "BdlaError", "Workspace", "fwd", "bwd", "decay", "decode",
-           "lib", "n_slots", "workspace_bytes"]
+__all__ = ["BOUNDED", "SOFTPLUS", "CHUNK", "BdlaError", "Workspace", "fwd", "bwd", "fwd_vec", "bwd_vec",
+           "decay", "decode", "lib", "n_slots", "workspace_bytes"]

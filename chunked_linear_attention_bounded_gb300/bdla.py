@@ -35,7 +35,8 @@ STATUS_NAMES = {OK: "BDLA_OK", ERR_NULL: "BDLA_ERR_NULL", ERR_SHAPE: "BDLA_ERR_S
 EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", "bdla_bwd",
            "bdla_bwd_varlen", "bdla_read_device_status", "bdla_status_string", "bdla_version",
            "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
-           "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall")
+           "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall",
+           "bdla_workspace_bytes_vec", "bdla_fwd_vec", "bdla_bwd_vec")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 STALL_NONE, STALL_PRODUCER, STALL_MMA, STALL_EPILOGUE = 0, 1, 2, 3
 
@@ -94,6 +95,13 @@ def lib():
         L.bdla_set_wait_limit_ns.restype = ci
         L.bdla_set_test_stall.argtypes = [ci, ci]
         L.bdla_set_test_stall.restype = ci
+        L.bdla_workspace_bytes_vec.argtypes = [ci, Dims, ci]
+        L.bdla_workspace_bytes_vec.restype = sz
+        L.bdla_fwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, Dims, ci, vp, sz, vp]
+        L.bdla_fwd_vec.restype = ci
+        L.bdla_bwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, Dims,
+                                   ci, vp, sz, vp]
+        L.bdla_bwd_vec.restype = ci
         del i32
         _lib = L
     return _lib
@@ -367,3 +375,78 @@ def bwd(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, ckp
     if st:
         raise BdlaError(st, "bdla_bwd")
     return dq, dkk, dvv, da, dh0
+
+
+# ---------------------------------------------------------------- per-channel decay
+def _vec_checks(q, k, v, a, cu_seqlens, h0):
+    _check(q, "q", torch.bfloat16, 4)
+    _check(k, "k", torch.bfloat16, 4)
+    _check(v, "v", torch.bfloat16, 4)
+    _check(a, "a", torch.float32, 4)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or a.shape != q.shape:
+        raise ValueError("q, k, v, a shapes disagree (a is [B, T, H, dk] for per-channel decay)")
+    n_docs = 0
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, 1)
+        n_docs = cu_seqlens.numel() - 1
+    n_seq = n_docs if n_docs else B
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, 4)
+        if tuple(h0.shape) != (n_seq, H, dk, dv):
+            raise ValueError("h0 must be [n_docs, H, dk, dv]")
+    return B, T, H, dk, dv, n_docs, n_seq
+
+
+def _ws_vec(op, q, v, n_docs, ws):
+    B, T, H, dk = q.shape
+    need = int(lib().bdla_workspace_bytes_vec(op, Dims(B, T, H, dk, v.shape[-1]), n_docs))
+    if need == 0:
+        raise BdlaError(ERR_UNSUPPORTED, "bdla_workspace_bytes_vec")
+    if ws is None:
+        return Workspace(need, q.device)
+    return ws.ensure(need)
+
+
+def fwd_vec(q, k, v, a, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUNDED,
+            o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, stream=None):
+    """Forward pass with one log-decay per key channel (a [B, T, H, dk]).
+    Returns (o, hT)."""
+    B, T, H, dk, dv, n_docs, n_seq = _vec_checks(q, k, v, a, cu_seqlens, h0)
+    o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    hT = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _ws_vec(OP_FWD, q, v, n_docs, ws)
+    st = lib().bdla_fwd_vec(_p(q), _p(k), _p(v), _p(a), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0), _p(o),
+                            _dtype_code(o.dtype), _p(hT), _dims(q, v), mode, ws.ptr, ws.nbytes,
+                            _stream_handle(stream))
+    if st:
+        raise BdlaError(st, "bdla_fwd_vec")
+    return o, hT
+
+
+def bwd_vec(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, mode: int = BOUNDED,
+            want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, stream=None):
+    """Backward pass with one log-decay per key channel.  Returns
+    (dq, dk, dv, da, dh0) with da [B, T, H, dk]; dh0 is None unless asked for."""
+    B, T, H, dk, dv, n_docs, n_seq = _vec_checks(q, k, v, a, cu_seqlens, h0)
+    _check(dO, "dO", torch.bfloat16, 4)
+    if dO.shape != v.shape:
+        raise ValueError("dO must match v")
+    if dhT is not None:
+        _check(dhT, "dhT", torch.float32, 4)
+    dev = q.device
+    if outs is None:
+        outs = (torch.empty(q.shape, dtype=torch.float32, device=dev),
+                torch.empty(k.shape, dtype=torch.float32, device=dev),
+                torch.empty(v.shape, dtype=torch.float32, device=dev),
+                torch.empty(a.shape, dtype=torch.float32, device=dev))
+    dq, dk_, dv_, da = outs
+    dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
+    ws = _ws_vec(OP_BWD, q, v, n_docs, ws)
+    st = lib().bdla_bwd_vec(_p(q), _p(k), _p(v), _p(a), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0), _p(dO),
+                            _p(dhT), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dh0), _dims(q, v), mode, ws.ptr,
+                            ws.nbytes, _stream_handle(stream))
+    if st:
+        raise BdlaError(st, "bdla_bwd_vec")
+    return dq, dk_, dv_, da, dh0

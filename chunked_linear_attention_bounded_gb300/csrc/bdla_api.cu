@@ -463,6 +463,96 @@ bdla_status bdla_set_seq_split(int blocks)
     return BDLA_OK;
 }
 
+// ---------------------------------------------------------------- per-channel decay
+namespace {
+
+bdla_status check_vec(const bdla_dims &d, const int32_t *cu, int n_docs)
+{
+    BDLA_TRY(check_dims(d, cu != nullptr, n_docs));
+    if (d.dv != 64 && d.dv != 128)
+        return BDLA_ERR_UNSUPPORTED;
+    return BDLA_OK;
+}
+
+size_t vec_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off)
+{
+    size_t off = round_up(kStatusBytes);
+    *states_off = off;
+    if (op == BDLA_OP_BWD) {
+        Problem p{};
+        p.tokens = total_tokens(d);
+        p.n_docs = n_docs;
+        off += round_up((size_t)d.H * vec_state_slots(p) * d.dk * d.dv * 2);
+    }
+    return off;
+}
+
+}  // namespace
+
+size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs)
+{
+    const bool varlen = n_docs > 0;
+    if (check_vec(d, varlen ? reinterpret_cast<const int32_t *>(1) : nullptr, n_docs) != BDLA_OK)
+        return 0;
+    size_t so;
+    return vec_layout(op, d, varlen ? n_docs : d.B, &so);
+}
+
+bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const float *a, float b, int chunk,
+                         const int32_t *cu_seqlens, int n_docs, const float *h0, void *o,
+                         bdla_dtype o_dtype, float *hT, bdla_dims d, bdla_decay_mode mode, void *ws,
+                         size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    if (total_tokens(d) > 0 && (!q || !k || !v || !a || !o))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
+        !aligned16(hT) || !aligned16(a))
+        return BDLA_ERR_ALIGN;
+    if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
+        return BDLA_ERR_DTYPE;
+    size_t so;
+    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
+    KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
+    BDLA_CUDA(launch_vec_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                             static_cast<const __nv_bfloat16 *>(v), a, h0, o, o_dtype == BDLA_F32, hT, nullptr));
+    return BDLA_OK;
+}
+
+bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const float *a, float b, int chunk,
+                         const int32_t *cu_seqlens, int n_docs, const float *h0, const void *dO,
+                         const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
+                         bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    if (total_tokens(d) > 0 && (!q || !k || !v || !a || !dO || !dq || !dk || !dv || !da))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(a) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(da) || !aligned16(h0) ||
+        !aligned16(dhT) || !aligned16(dh0))
+        return BDLA_ERR_ALIGN;
+    size_t so;
+    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
+    auto *states = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    {
+        KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
+        BDLA_CUDA(launch_vec_fwd(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, states));
+    }
+    {
+        KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(launch_vec_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, states, dhT, dq,
+                                 dk, dv, da, dh0));
+    }
+    return BDLA_OK;
+}
+
 bdla_status bdla_set_wait_limit_ns(uint64_t ns)
 {
     g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);

@@ -110,7 +110,9 @@ struct BwdSmem {
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
     uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
         mf_done, acc_free, drain, full_z, z_free;
-    uint64_t never;   // nothing arrives here: the wait of the stall test hook
+    uint64_t never;
+    uint64_t wait_ns;     // limit of the pipeline waits
+    int stall_at[3];      // test hook: block at which producer / MMA / epilogue stall (-1: never)   // nothing arrives here: the wait of the stall test hook
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -328,6 +330,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.z_free, 1);
         mbar_init(&sm.never, 1);
         sm.abort_flag = 0;
+        sm.wait_ns = wait_ns;
+        for (int r = 0; r < 3; ++r)
+            sm.stall_at[r] = stall == r + 1 ? stall_blk : -1;
         mbar_fence_init();
     }
     if (kpan == 1) {   // dk = 64: the second dk panel of Q and K stays zero
@@ -359,14 +364,15 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             int last = -1;
             bool ok = true;
             for (int jj = 0; jj < nblk; ++jj) {
-                if (*abort_flag || (stall == BDLA_STALL_PRODUCER && jj == stall_blk &&
-                                    !mbar_wait(&sm.never, 0, wait_ns))) {
+                if (*abort_flag) {
                     ok = false;
                     break;
                 }
                 const int j = nblk - 1 - jj;
                 const int t0 = (int)(d.start + (int64_t)j * BT);
-                if (jj > 0 && !mbar_wait(&sm.free_in, (jj - 1) & 1, wait_ns)) {
+                // (test hook: the stalling producer waits on `never` here instead)
+                const bool sp = jj == sm.stall_at[0];
+                if ((jj > 0 || sp) && !mbar_wait_lim(sp ? &sm.never : &sm.free_in, sp ? 0u : (uint32_t)((jj - 1) & 1), &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -383,7 +389,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 if (st_tma) {
                     // bf16 state before the block, straight into the z tile, once the
                     // previous block's output staging has left z
-                    if (jj > 0 && !mbar_wait(&sm.z_free, (jj - 1) & 1, wait_ns)) {
+                    if (jj > 0 && !mbar_wait_lim(&sm.z_free, (jj - 1) & 1, &sm.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -424,12 +430,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             bool ok = true;
             for (int jj = 0; jj < nblk && ok; ++jj) {
                 const uint32_t par = jj & 1;
-                if (*abort_flag ||
-                    (stall == BDLA_STALL_MMA && jj == stall_blk && !mbar_wait(&sm.never, 0, wait_ns)) ||
-                    !mbar_wait(&sm.full_in, par, wait_ns) ||
+                // (test hook: the stalling MMA warp waits on `never` instead of full_in)
+                const bool sm_ = jj == sm.stall_at[1];
+                if (*abort_flag || !mbar_wait_lim(sm_ ? &sm.never : &sm.full_in, sm_ ? 0u : par, &sm.wait_ns) ||
                     // S_in: straight from its TMA load, or once the epilogue converted it
-                    !mbar_wait(st_tma ? &sm.full_z : &sm.z_ready, par, wait_ns) ||
-                    (jj > 0 && !mbar_wait(&sm.acc_free, (jj - 1) & 1, wait_ns))) {
+                    !mbar_wait_lim(st_tma ? &sm.full_z : &sm.z_ready, par, &sm.wait_ns) ||
+                    (jj > 0 && !mbar_wait_lim(&sm.acc_free, (jj - 1) & 1, &sm.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -441,7 +447,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
                 }
                 umma_commit(&sm.m1_done);
-                if (!mbar_wait(&sm.ea_done, par, wait_ns)) {
+                if (!mbar_wait_lim(&sm.ea_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -451,7 +457,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int ks = 0; ks < DV / 16; ++ks)
                     umma_bf16(t_c1, kmaj(sv, ks), kmaj(sz, ks), id_ve, ks > 0);
                 umma_commit(&sm.mb_done);
-                if (!mbar_wait(&sm.eb_done, par, wait_ns)) {
+                if (!mbar_wait_lim(&sm.eb_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -461,7 +467,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     umma_bf16(t_c3, kmaj(sx, ks), mnmaj(sk, ks), id_dpk, 1);
                 }
                 umma_commit(&sm.md_done);
-                if (!mbar_wait(&sm.ee_done, par, wait_ns)) {
+                if (!mbar_wait_lim(&sm.ee_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -514,7 +520,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         auto finish_block = [&]() -> bool {
             // Eg: outputs of block pend_j once Mf has completed
             const int jj = nblk - 1 - pend_j;
-            if (!epi_all(mbar_wait(&sm.mf_done, jj & 1, wait_ns)) || *abort_flag)
+            if (!epi_all(mbar_wait_lim(&sm.mf_done, jj & 1, &sm.wait_ns)) || *abort_flag)
                 return false;
             tc_fence_after();
             const int64_t t = d.start + (int64_t)pend_j * BT + r;
@@ -711,11 +717,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
-            if (stall == BDLA_STALL_EPILOGUE && jj == stall_blk) {
-                ok = epi_all(mbar_wait(&sm.never, 0, wait_ns));
-                if (!ok)
-                    break;
-            }
             // the decay scalars load overlaps the previous block's output stores
             const float g = valid ? gamma[(int64_t)h * tokens + t0 + r] : 0.0f;
             const float fac = valid ? dfac[(int64_t)h * tokens + t0 + r] : 0.0f;
@@ -756,7 +757,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int bp = (int)par;   // parity of this block's partial sums
             if (st_tma) {
                 // the producer loaded S_in (bf16) into z; <S_in, E> is taken in EA
-                ok = epi_all(mbar_wait(&sm.full_z, par, wait_ns)) && !*abort_flag;
+                ok = epi_all(mbar_wait_lim(&sm.full_z, par, &sm.wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
             } else {
@@ -798,7 +799,11 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // ---- EA (P goes into x: the previous block's output stores are done reading it)
             if (warp == 2 && lane == 0)
                 tma_store_wait_read();
-            ok = epi_all(mbar_wait(&sm.m1_done, par, wait_ns)) && !*abort_flag;
+            {
+                // (test hook: the stalling epilogue waits on `never` instead of m1_done)
+                const bool se = jj == sm.stall_at[2];
+                ok = epi_all(mbar_wait_lim(se ? &sm.never : &sm.m1_done, se ? 0u : par, &sm.wait_ns)) && !*abort_flag;
+            }
             if (!ok)
                 break;
             tc_fence_after();
@@ -807,38 +812,34 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 // P_ts = (q_t . k_s) e^{Gamma_t - Gamma_s}, dP_ts = (dO_t . v_s) e^{Gamma_t - Gamma_s};
                 // each half takes 8 of the row's 16 pairs, reading each 16-byte
                 // chunk of its q and dO rows once
-                float pq[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-                float pd[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
                 const int s0 = 16 * tau + 8 * half;
+                float acc[8];
+                // q_t . k_s first, then dO_t . v_s, so one set of accumulators is live
 #pragma unroll 1
-                for (int p = 0; p < kpan; ++p)
+                for (int which = 0; which < 2; ++which) {
+                    const unsigned char *xa = which == 0 ? sm.q : sm.dO;
+                    const unsigned char *yb = which == 0 ? sm.k : sm.v;
+                    const int npan = which == 0 ? kpan : DV / 64;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 qa = *reinterpret_cast<const uint4 *>(sm.q + p * kPanel + sw128_offset(r, c8));
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint4 kb = *reinterpret_cast<const uint4 *>(sm.k + p * kPanel + sw128_offset(s0 + i, c8));
-                            pq[i] = dot_bf16x8(qa, kb, pq[i]);
-                        }
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        acc[i] = 0.0f;
 #pragma unroll 1
-                for (int p = 0; p < DV / 64; ++p)
+                    for (int p = 0; p < npan; ++p)
+#pragma unroll 2
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint4 xr = *reinterpret_cast<const uint4 *>(xa + p * kPanel + sw128_offset(r, c8));
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 oa = *reinterpret_cast<const uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint4 vb = *reinterpret_cast<const uint4 *>(sm.v + p * kPanel + sw128_offset(s0 + i, c8));
-                            pd[i] = dot_bf16x8(oa, vb, pd[i]);
+                            for (int i = 0; i < 8; ++i) {
+                                const uint4 yr = *reinterpret_cast<const uint4 *>(yb + p * kPanel + sw128_offset(s0 + i, c8));
+                                acc[i] = dot_bf16x8(xr, yr, acc[i]);
+                            }
                         }
-                    }
+                    float (*dst)[kChunk + 1] = which == 0 ? sm.dgp : sm.dgd;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int sc = s0 + i;
-                    const bool live = valid && sc <= r;
-                    const float e = live ? expf(g - sm.gq[sc]) : 0.0f;
-                    sm.dgp[r][8 * half + i] = pq[i] * e;
-                    sm.dgd[r][8 * half + i] = pd[i] * e;
+                    for (int i = 0; i < 8; ++i) {
+                        const int sc = s0 + i;
+                        dst[r][8 * half + i] = (valid && sc <= r) ? acc[i] * expf(g - sm.gq[sc]) : 0.0f;
+                    }
                 }
                 epi_sync();   // all raw V rows read before any row is rescaled below
             }
@@ -984,7 +985,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
             // ---- Eb: C1 <- w_s o C1 (the inter-block part of dk), k . dk_inter,
             //      then dP -> smem
-            ok = epi_all(mbar_wait(&sm.mb_done, par, wait_ns)) && !*abort_flag;
+            ok = epi_all(mbar_wait_lim(&sm.mb_done, par, &sm.wait_ns)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
@@ -1068,7 +1069,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
             } else {
                 // ---- Ee: K -> K o w_s in place once Md has read K
-                ok = epi_all(mbar_wait(&sm.md_done, par, wait_ns)) && !*abort_flag;
+                ok = epi_all(mbar_wait_lim(&sm.md_done, par, &sm.wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
                 tc_fence_after();

@@ -39,13 +39,14 @@ __device__ __forceinline__ float log_decay(float a, float b, int mode)
     return -(fmaxf(a, 0.0f) + log1pf(expf(-fabsf(a))));
 }
 
-// d lambda / d a
+// d lambda / d a.  sigma'(a) = sigma(a) (1 - sigma(a)) is taken as
+// sigma(a) sigma(-a): equal in exact arithmetic, and it keeps its relative
+// accuracy for saturated logits, where 1 - sigma(a) in fp32 rounds to 0.
 __device__ __forceinline__ float log_decay_deriv(float a, float b, int mode)
 {
-    float s = sigmoidf_(a);
     if (mode == BDLA_DECAY_BOUNDED_SIGMOID)
-        return b * s * (1.0f - s);
-    return -s;
+        return b * sigmoidf_(a) * sigmoidf_(-a);
+    return -sigmoidf_(a);
 }
 
 // Document [start, end) of document n: packed offsets or fixed length T.

@@ -64,7 +64,9 @@ struct FwdSmem {
     uint32_t abl_pair[BT][4];   // ablation: one half's 8 position-pair values of a row (bf16 pairs)
     uint64_t full_qk[2], empty_qk[2], score_full[2];
     uint64_t full_v, empty_v, p_ready, o_full, p_free, drain;
-    uint64_t never;   // nothing arrives here: the wait of the stall test hook
+    uint64_t never;
+    uint64_t wait_ns;     // limit of the pipeline waits
+    int stall_at[3];      // test hook: block at which producer / MMA / epilogue stall (-1: never)   // nothing arrives here: the wait of the stall test hook
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -168,6 +170,9 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.drain, 1);
         mbar_init(&sm.never, 1);
         sm.abort_flag = 0;
+        sm.wait_ns = wait_ns;
+        for (int r = 0; r < 3; ++r)
+            sm.stall_at[r] = stall == r + 1 ? stall_blk : -1;
         mbar_fence_init();
     }
     if (kpan == 1) {   // dk = 64: the second dk panel of Q and K stays zero
@@ -198,13 +203,9 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int j = 0; j < nblk; ++j) {
                 if (*abort_flag)
                     break;
-                if (stall == BDLA_STALL_PRODUCER && j == stall_blk && !mbar_wait(&sm.never, 0, wait_ns)) {
-                    consumed = false;
-                    break;
-                }
                 const int s = j & 1;
                 const int t0 = (int)(d.start + (int64_t)j * BT);
-                if (j >= 2 && !mbar_wait(&sm.empty_qk[s], ((j >> 1) - 1) & 1, wait_ns)) {
+                if (j >= 2 && !mbar_wait_lim(&sm.empty_qk[s], ((j >> 1) - 1) & 1, &sm.wait_ns)) {
                     consumed = false;
                     break;
                 }
@@ -215,7 +216,9 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tma_load_3d(sm.k[s] + p * kPanel, &tk, &sm.full_qk[s], p * 64, h, t0);
                 }
                 last_qk[s] = j;
-                if (j >= 1 && !mbar_wait(&sm.empty_v, (j - 1) & 1, wait_ns)) {
+                // (test hook: the stalling producer waits on `never` here instead)
+                const bool sp = j == sm.stall_at[0];
+                if ((j >= 1 || sp) && !mbar_wait_lim(sp ? &sm.never : &sm.empty_v, sp ? 0u : (uint32_t)((j - 1) & 1), &sm.wait_ns)) {
                     consumed = false;
                     break;
                 }
@@ -247,10 +250,10 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             bool ok = true;
             auto issue_qk = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(&sm.full_qk[s], (j >> 1) & 1, wait_ns))
+                if (!mbar_wait_lim(&sm.full_qk[s], (j >> 1) & 1, &sm.wait_ns))
                     return false;
                 // the P of block j - 2 (in this score buffer) has been read by its P V GEMM
-                if (j >= 2 && !mbar_wait(&sm.p_free, j & 1, wait_ns))
+                if (j >= 2 && !mbar_wait_lim(&sm.p_free, j & 1, &sm.wait_ns))
                     return false;
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks) {
@@ -265,14 +268,16 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 ok = issue_qk(0);
             for (int j = 0; ok && j < nblk; ++j) {
                 const int s = j & 1;
-                if (*abort_flag ||
-                    (stall == BDLA_STALL_MMA && j == stall_blk && !mbar_wait(&sm.never, 0, wait_ns))) {
+                if (*abort_flag) {
                     ok = false;
                     break;
                 }
                 if (!STATES && j + 1 < nblk && !(ok = issue_qk(j + 1)))
                     break;
-                if (!mbar_wait(&sm.p_ready, j & 1, wait_ns) || !mbar_wait(&sm.full_v, j & 1, wait_ns)) {
+                // (test hook: the stalling MMA warp waits on `never` here instead)
+                const bool sm_ = j == sm.stall_at[1];
+                if (!mbar_wait_lim(sm_ ? &sm.never : &sm.p_ready, sm_ ? 0u : (uint32_t)(j & 1), &sm.wait_ns) ||
+                    !mbar_wait_lim(&sm.full_v, j & 1, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -394,11 +399,6 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
-            if (stall == BDLA_STALL_EPILOGUE && j == stall_blk) {
-                ok = epi_all(mbar_wait(&sm.never, 0, wait_ns));
-                if (!ok)
-                    break;
-            }
             // ---- decay scalars of this block
             const float g = g_next;
             if (j + 1 < nblk) {
@@ -433,10 +433,11 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float qsc = valid ? expf(lam_r) : 0.0f;
             const float ksc = valid ? expf(lend - lam_r) : 0.0f;
 
-            if (STATES) {
-                ok = epi_all(mbar_wait(&sm.full_qk[s], (j >> 1) & 1, wait_ns)) && !*abort_flag;
-            } else {
-                ok = epi_all(mbar_wait(&sm.score_full[s], (j >> 1) & 1, wait_ns)) && !*abort_flag;
+            {
+                // (test hook: the stalling epilogue waits on `never` here instead)
+                const bool se = j == sm.stall_at[2];
+                uint64_t *bar = se ? &sm.never : (STATES ? &sm.full_qk[s] : &sm.score_full[s]);
+                ok = epi_all(mbar_wait_lim(bar, se ? 0u : (uint32_t)((j >> 1) & 1), &sm.wait_ns)) && !*abort_flag;
             }
             if (!ok)
                 break;
@@ -562,7 +563,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (j > 0) {
                 if (ck_tma && warp == 2 && lane == 0)
                     tma_store_wait_read();   // previous checkpoint store is done with sb
-                ok = epi_all(mbar_wait(&sm.o_full, (j - 1) & 1, wait_ns)) && !*abort_flag;
+                ok = epi_all(mbar_wait_lim(&sm.o_full, (j - 1) & 1, &sm.wait_ns)) && !*abort_flag;
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -637,7 +638,7 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         if (ck_tma && warp == 2 && lane == 0)
             tma_store_wait_read();
         if (ok && nblk > 0) {
-            ok = epi_all(mbar_wait(&sm.o_full, (nblk - 1) & 1, wait_ns)) && !*abort_flag;
+            ok = epi_all(mbar_wait_lim(&sm.o_full, (nblk - 1) & 1, &sm.wait_ns)) && !*abort_flag;
             if (ok) {
                 tc_fence_after();
                 if (!STATES)

@@ -83,6 +83,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     return true;
 }
 
+// Same, with the limit read (from shared memory) only once the phase has
+// not completed after 256 polls, so it occupies no register on the fast path.
+__device__ __forceinline__ bool mbar_wait_lim(uint64_t *bar, uint32_t parity, const uint64_t *limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++n & 255u) == 0u && globaltimer_ns() - t0 > *limit_ns)
+            return false;
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem()
 {

@@ -12,6 +12,8 @@
 //   S_out     = e^{gamma} S_in + sum_s e^{gamma - Gamma_s} k_s v_s^T,
 // gamma = Gamma at the tile's last token; S is written to the checkpoint
 // array at every multiple of the stride.
+#include <mma.h>
+
 #include "bdla_internal.h"
 #include "bdla_sm100.cuh"
 
@@ -160,31 +162,35 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 // kernel fills the states at the block's inner multiples of the stride, one
 // CTA per (64-column slice, head, block), all blocks at once: from the block
 // start S, each 16-token tile c applies
-//   S <- e^{gamma_c} S + sum_{t in tile} e^{gamma_c - Gamma_t} k_t v_t^T
-// (Gamma tile-local, gamma_c its value at the tile's last token; every weight
-// <= 1).  The block's keys and value slice are staged in shared memory once;
-// threads own 4 columns x DK/16 rows of the state (16 column groups x 16 row
-// groups).
+//   S <- e^{gamma_c} S + (K o w)_c^T V_c,   w_t = e^{gamma_c - Gamma_t} <= 1
+// (Gamma tile-local, gamma_c its value at the tile's last token).  The update
+// is one 16-token bf16 warp MMA per 16 x 16 state tile (wmma, fp32
+// accumulate); each warp keeps its state tiles in accumulator fragments, scales
+// them by e^{gamma_c} (the same factor for every element) and stores them to
+// the checkpoint directly.  The block's weighted keys and value slice are
+// staged in shared memory once.
 constexpr int kExpThreads = 256;
+constexpr int kExpWarps = kExpThreads / 32;
 
 template <int DK>
 struct ExpSmem {
-    __nv_bfloat16 k[128][DK];
+    __nv_bfloat16 kw[128][DK];          // k_t o w_t
     __nv_bfloat16 v[128][kDvSlice];
     float w[128];        // e^{gamma_c - Gamma_t} for the token's tile c
     float eg[128 / kChunk];
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kExpThreads, 3)
+__global__ void __launch_bounds__(kExpThreads)
 ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                    const float *__restrict__ gamma, const int32_t *__restrict__ cu, int T,
                    int64_t tokens, int n_docs, int H, int dv, float *__restrict__ ckpt,
                    int ckpt_stride, int64_t n_slots)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    using namespace nvcuda;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     ExpSmem<DK> &sm = *reinterpret_cast<ExpSmem<DK> *>(smem_raw);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int j0 = blockIdx.x * kDvSlice, h = blockIdx.y;
     const SegSpan blk = seg_span(cu, T, tokens, n_docs, blockIdx.z, 1);   // one 128-token block
     if (!blk.valid || blk.len <= kChunk)
@@ -193,17 +199,6 @@ ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__r
     const int64_t off0 = (int64_t)blk.blk_base * 128;   // doc-local first token
     const int ntiles = (int)((blk.len + kChunk - 1) / kChunk);
     const int m = (ntiles - 1) * kChunk;   // tokens feeding the inner states (full tiles)
-    // stage keys, values and weights of the block's first ntiles - 1 tiles
-    for (int e = tid; e < m * (DK / 8); e += kExpThreads) {
-        const int t = e / (DK / 8), c8 = e % (DK / 8);
-        reinterpret_cast<uint4 *>(&sm.k[t][0])[c8] =
-            reinterpret_cast<const uint4 *>(k + ((size_t)(blk.start + t) * H + h) * DK)[c8];
-    }
-    for (int e = tid; e < m * (kDvSlice / 8); e += kExpThreads) {
-        const int t = e / (kDvSlice / 8), c8 = e % (kDvSlice / 8);
-        reinterpret_cast<uint4 *>(&sm.v[t][0])[c8] =
-            reinterpret_cast<const uint4 *>(v + ((size_t)(blk.start + t) * H + h) * dv + j0)[c8];
-    }
     if (tid < m) {
         const float gt = gamma[(int64_t)h * tokens + blk.start + tid];
         const float gend = gamma[(int64_t)h * tokens + blk.start + (tid | (kChunk - 1))];
@@ -211,51 +206,58 @@ ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__r
         if ((tid & (kChunk - 1)) == kChunk - 1)
             sm.eg[tid / kChunk] = expf(gend);
     }
-    const size_t sstride = (size_t)DK * dv;
-    const int cg = tid % 16, rg = tid / 16;
-    const int col = j0 + 4 * cg;
-    constexpr int kRows = DK / 16;
-    float4 S[kRows];
-    {
-        const int64_t slot = ckpt_slot(blk.doc_start, n, off0 / ckpt_stride, ckpt_stride);
-        const float *src = ckpt + ((size_t)h * n_slots + slot) * sstride;
+    __syncthreads();
+    // weighted keys and the value slice of the block's first ntiles - 1 tiles
+    for (int e = tid; e < m * (DK / 8); e += kExpThreads) {
+        const int t = e / (DK / 8), c8 = e % (DK / 8);
+        const uint4 raw = reinterpret_cast<const uint4 *>(k + ((size_t)(blk.start + t) * H + h) * DK)[c8];
+        const float wt = sm.w[t];
+        const uint32_t x[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t y[4];
 #pragma unroll
-        for (int i = 0; i < kRows; ++i)
-            S[i] = *reinterpret_cast<const float4 *>(src + (size_t)(rg + 16 * i) * dv + col);
+        for (int i = 0; i < 4; ++i)
+            y[i] = sm100::pack_bf16(sm100::bf16_lo(x[i]) * wt, sm100::bf16_hi(x[i]) * wt);
+        reinterpret_cast<uint4 *>(&sm.kw[t][0])[c8] = make_uint4(y[0], y[1], y[2], y[3]);
+    }
+    for (int e = tid; e < m * (kDvSlice / 8); e += kExpThreads) {
+        const int t = e / (kDvSlice / 8), c8 = e % (kDvSlice / 8);
+        reinterpret_cast<uint4 *>(&sm.v[t][0])[c8] =
+            reinterpret_cast<const uint4 *>(v + ((size_t)(blk.start + t) * H + h) * dv + j0)[c8];
     }
     __syncthreads();
+    // this warp's 16 x 16 tiles of the DK x 64 state slice
+    constexpr int kTiles = (DK / 16) * (kDvSlice / 16);
+    constexpr int kPerWarp = kTiles / kExpWarps;
+    const size_t sstride = (size_t)DK * dv;
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc[kPerWarp];
+    {
+        const int64_t slot = ckpt_slot(blk.doc_start, n, off0 / ckpt_stride, ckpt_stride);
+        const float *src = ckpt + ((size_t)h * n_slots + slot) * sstride + j0;
+#pragma unroll
+        for (int x = 0; x < kPerWarp; ++x) {
+            const int tile = warp * kPerWarp + x, mi = tile / (kDvSlice / 16), ni = tile % (kDvSlice / 16);
+            wmma::load_matrix_sync(acc[x], src + (size_t)(16 * mi) * dv + 16 * ni, dv, wmma::mem_row_major);
+        }
+    }
     for (int c = 0; c + 1 < ntiles; ++c) {   // the last tile ends the block: not needed here
         const float eg = sm.eg[c];
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-            S[i].x *= eg;
-            S[i].y *= eg;
-            S[i].z *= eg;
-            S[i].w *= eg;
-        }
-#pragma unroll 4
-        for (int tt = 0; tt < kChunk; ++tt) {
-            const int t = c * kChunk + tt;
-            const float wt = sm.w[t];
-            const uint2 vraw = *reinterpret_cast<const uint2 *>(&sm.v[t][4 * cg]);
-            const float v0 = wt * sm100::bf16_lo(vraw.x), v1 = wt * sm100::bf16_hi(vraw.x);
-            const float v2 = wt * sm100::bf16_lo(vraw.y), v3 = wt * sm100::bf16_hi(vraw.y);
-#pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-                const float kk = bf2f(sm.k[t][rg + 16 * i]);
-                S[i].x = fmaf(kk, v0, S[i].x);
-                S[i].y = fmaf(kk, v1, S[i].y);
-                S[i].z = fmaf(kk, v2, S[i].z);
-                S[i].w = fmaf(kk, v3, S[i].w);
-            }
-        }
         const int64_t tl = off0 + (int64_t)(c + 1) * kChunk;   // doc-local token the state precedes
-        if (tl % ckpt_stride == 0) {
-            const int64_t slot = ckpt_slot(blk.doc_start, n, tl / ckpt_stride, ckpt_stride);
-            float *dst = ckpt + ((size_t)h * n_slots + slot) * sstride;
+        const bool wr = tl % ckpt_stride == 0;
+        float *dst = ckpt + ((size_t)h * n_slots + (size_t)ckpt_slot(blk.doc_start, n, tl / ckpt_stride, ckpt_stride)) *
+                                sstride + j0;
 #pragma unroll
-            for (int i = 0; i < kRows; ++i)
-                *reinterpret_cast<float4 *>(dst + (size_t)(rg + 16 * i) * dv + col) = S[i];
+        for (int x = 0; x < kPerWarp; ++x) {
+            const int tile = warp * kPerWarp + x, mi = tile / (kDvSlice / 16), ni = tile % (kDvSlice / 16);
+#pragma unroll
+            for (int e = 0; e < acc[x].num_elements; ++e)
+                acc[x].x[e] *= eg;
+            wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+            wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
+            wmma::load_matrix_sync(fa, &sm.kw[16 * c][16 * mi], DK);          // A[i][t] = kw[t][i]
+            wmma::load_matrix_sync(fb, &sm.v[16 * c][16 * ni], kDvSlice);     // B[t][j] = v[t][j]
+            wmma::mma_sync(acc[x], fa, fb, acc[x]);
+            if (wr)
+                wmma::store_matrix_sync(dst + (size_t)(16 * mi) * dv + 16 * ni, acc[x], dv, wmma::mem_row_major);
         }
     }
 }

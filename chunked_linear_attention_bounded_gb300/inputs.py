@@ -9,7 +9,8 @@ Recipe (one workload per context stage, 8K -> 64K -> 256K -> 1M tokens, from
   q ~ N(0,1) / sqrt(dk)             bf16
   k ~ N(0,1), L2-normalised over dk per (token, head) in fp32, then bf16
   v ~ N(0,1)                        bf16
-  a ~ N(mean, std)                  fp32 decay logits
+  a ~ N(mean, std)                  fp32 decay logits ([B,T,H], or [B,T,H,dk] for
+                                    the per-channel decay)
   dO ~ N(0,1)                       bf16 upstream gradient
   h0 ~ N(0, h0_std) per document    fp32 (absent when h0_std == 0)
 Packed documents: n_docs lengths u_i ~ U[lo, hi], rescaled so they sum to T
@@ -44,6 +45,7 @@ class Workload:
     fwd_only: bool = False
     o_f32: bool = False            # fp32 o (else bf16)
     ckpt_stride: int = 0           # >0: fp32 state checkpoints every ckpt_stride tokens
+    vec: bool = False              # one decay logit per key channel: a [B,T,H,dk]
 
     @property
     def tokens(self) -> int:
@@ -66,6 +68,9 @@ WORKLOADS = {
     # 1M stage, unbounded -softplus decay (the ablation)
     "c1m_ablation": Workload("c1m_ablation", B=1, T=1048576, H=8, dk=128, dv=128, seed=1005,
                              a_mean=2.0, a_std=2.0, mode=1),
+    # per-channel decay (one logit per key channel) on the 64K stage's packed documents
+    "varlen64k_vec": Workload("varlen64k_vec", B=1, T=65536, H=32, dk=128, dv=128, seed=1006,
+                              h0_std=0.1, n_docs=8, doc_lo=1024, doc_hi=16384, vec=True),
 }
 
 
@@ -105,7 +110,7 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None) -> dict:
     k = k32.to(torch.bfloat16)
     del k32
     v = _randn((B, T, H, dv), g).to(torch.bfloat16)
-    a = (_randn((B, T, H), g) * w.a_std + w.a_mean).contiguous()
+    a = (_randn((B, T, H, dk) if w.vec else (B, T, H), g) * w.a_std + w.a_mean).contiguous()
     dO = _randn((B, T, H, dv), g).to(torch.bfloat16) if with_grad else None
     n_seq = (cu.numel() - 1) if cu is not None else B
     h0 = (_randn((n_seq, H, dk, dv), g) * w.h0_std) if w.h0_std > 0 else None
@@ -133,7 +138,7 @@ def make_inputs_on(w: Workload, device, with_grad: bool = True) -> dict:
     k = (k32 / k32.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(torch.bfloat16)
     del k32
     v = rn((B, T, H, dv)).to(torch.bfloat16)
-    a = (rn((B, T, H)) * w.a_std + w.a_mean).contiguous()
+    a = (rn((B, T, H, dk) if w.vec else (B, T, H)) * w.a_std + w.a_mean).contiguous()
     dO = rn((B, T, H, dv)).to(torch.bfloat16) if with_grad else None
     n_seq = (cu.numel() - 1) if cu is not None else B
     h0 = (rn((n_seq, H, dk, dv)) * w.h0_std) if w.h0_std > 0 else None

@@ -216,6 +216,36 @@ bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void *v, const 
  */
 bdla_status bdla_noalloc_read_status(void *stream);
 
+/*
+ * Per-channel (vector) decay: one log-decay per (token, head, key channel),
+ * the variant the first page's "per-position cumulative decay" also admits
+ * ("Engineering Long-Context Training for Trillion-Parameter MoE Models:
+ * Three Key Breakthroughs", sec. 3.1), with its sec. 3.2 parameterisations
+ * applied channel by channel:
+ *     lambda_t[i] = b * sigmoid(a_t[i])   or   -softplus(a_t[i]),
+ *     S_t = diag(exp(lambda_t)) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t.
+ * Row i of the dk x dv state decays by its own factor; the bound keeps each
+ * channel's cumulative log-decay over a 16-token tile in [16 b, 0].
+ * Arguments as for bdla_fwd / bdla_bwd except:
+ *   a, da      fp32 [B, T, H, dk]   (one logit / gradient per key channel)
+ *   cu_seqlens device int32 [n_docs + 1] for packed documents (B = 1), or
+ *              NULL for fixed-length rows
+ *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise); no
+ *   checkpoints.  The backward's workspace holds the bf16 state before
+ *   every 16-token tile (written by its own states pass):
+ *   bdla_workspace_bytes_vec(BDLA_OP_BWD, ...) bytes, status word first.
+ */
+size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs);
+bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const float *a, float b,
+                         int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
+                         void *o, bdla_dtype o_dtype, float *hT, bdla_dims d,
+                         bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
+bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const float *a, float b,
+                         int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
+                         const void *dO, const float *dhT, float *dq, float *dk, float *dv,
+                         float *da, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
+                         size_t ws_bytes, void *stream);
+
 /* Static English description of a status code. */
 const char *bdla_status_string(bdla_status s);
 
