@@ -6,7 +6,8 @@ package imports nothing from it.
 
 The arithmetic lives in ``bdla_oracle.c`` (token-by-token recurrence and its
 reverse mode, see the header there for the reading of the pages; the
-per-channel decay variant is ``fwd_vec`` / ``bwd_vec``).  This module
+per-channel decay variant is ``fwd_vec`` / ``bwd_vec``, the gated delta
+rule ``fwd_delta`` / ``bwd_delta``).  This module
 only compiles it with gcc and marshals numpy float64 arrays through ctypes.
 """
 from __future__ import annotations
@@ -57,6 +58,14 @@ def _load():
             lib.oracle_fwd_vec.restype = ctypes.c_int
             lib.oracle_bwd_vec.argtypes = lib.oracle_bwd.argtypes
             lib.oracle_bwd_vec.restype = ctypes.c_int
+            lib.oracle_fwd_delta.argtypes = [ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             dp, dp, dp, dp, dp, ctypes.c_double, ctypes.c_int, dp, dp, dp,
+                                             ctypes.c_int]
+            lib.oracle_fwd_delta.restype = ctypes.c_int
+            lib.oracle_bwd_delta.argtypes = [ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             dp, dp, dp, dp, dp, ctypes.c_double, ctypes.c_int, dp,
+                                             dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int]
+            lib.oracle_bwd_delta.restype = ctypes.c_int
             lib.oracle_log_decay.argtypes = [ctypes.c_int64, dp, ctypes.c_double, ctypes.c_int, dp]
             lib.oracle_log_decay.restype = ctypes.c_int
             _lib = lib
@@ -167,6 +176,48 @@ def bwd_vec(q, k, v, a, dO, b=-5.0, mode=BOUNDED, h0=None, dhT=None, cu_seqlens=
                            _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(da),
                            _ptr(dh0), int(window), int(nthreads))
     return dq, dkk, dvv, da, dh0
+
+
+def fwd_delta(q, k, v, a, beta, b=-5.0, mode=BOUNDED, h0=None, cu_seqlens=None, nthreads=0):
+    """Gated delta rule with the bounded log-decay:
+    S_t = g_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t.
+    beta [T,H] (write strengths, given); otherwise as ``fwd``.  Returns
+    (o, hT), float64."""
+    q, k, v, a, beta, h0 = _f64(q), _f64(k), _f64(v), _f64(a), _f64(beta), _f64(h0)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    assert a.shape == (T, H) and beta.shape == (T, H)
+    cu = _cu(cu_seqlens, T)
+    N = cu.size - 1
+    assert cu[0] == 0 and cu[-1] == T
+    o = np.zeros((T, H, dv))
+    hT = np.zeros((N, H, dk, dv))
+    _load().oracle_fwd_delta(N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), H, dk, dv,
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), float(b), int(mode),
+                             _ptr(h0), _ptr(o), _ptr(hT), int(nthreads))
+    return o, hT
+
+
+def bwd_delta(q, k, v, a, beta, dO, b=-5.0, mode=BOUNDED, h0=None, dhT=None, cu_seqlens=None,
+              window=1024, nthreads=0):
+    """Reverse mode of ``fwd_delta`` for the loss <o, dO> + <hT, dhT>.
+    Returns (dq, dk, dv, da, dbeta, dh0), float64."""
+    q, k, v, a, beta, dO, h0, dhT = (_f64(x) for x in (q, k, v, a, beta, dO, h0, dhT))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.size - 1
+    dq = np.zeros_like(q)
+    dkk = np.zeros_like(k)
+    dvv = np.zeros_like(v)
+    da = np.zeros_like(a)
+    dbeta = np.zeros_like(beta)
+    dh0 = np.zeros((N, H, dk, dv))
+    _load().oracle_bwd_delta(N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), H, dk, dv,
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), float(b), int(mode),
+                             _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(da),
+                             _ptr(dbeta), _ptr(dh0), int(window), int(nthreads))
+    return dq, dkk, dvv, da, dbeta, dh0
 
 
 def threads_used(nthreads=0):

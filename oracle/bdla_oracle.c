@@ -30,6 +30,10 @@
  * attention), constant-decay closed form, T = 1 by hand, central finite
  * differences for every gradient, varlen == concatenation, linearity.
  *
+ * The gated delta rule with the same bounded decay (fwd_delta / bwd_delta,
+ * below) is the "Delta Net-style" structure the first page names beside
+ * linear attention ([P1] sec. 3.1; the substitution applies to it unchanged).
+ *
  * Layouts (row-major, feature innermost):
  *   q, k  [Ttot][H][dk]     v, o, dO  [Ttot][H][dv]     a, da  [Ttot][H]
  *   h0, hT, dh0, dhT  [N][H][dk][dv]    cu  [N+1] document offsets
@@ -451,6 +455,240 @@ int oracle_bwd_vec(int N, const int64_t *cu, int H, int dk, int dv,
         }
         free(win);
         free(g);
+        free(D);
+        free(S);
+    }
+    return used;
+}
+
+/*
+ * Gated delta rule with the bounded log-decay: the "Delta Net-style"
+ * structure [P1] sec. 3.1 names beside linear attention, to which the same
+ * parameterisation substitution applies.  The rule itself is the published
+ * one ("Gated Delta Networks: Improving Mamba2 with Delta Rule", Yang, Kautz
+ * and Hatamizadeh, 2024), written for a dk x dv state read by o = S^T q:
+ *     g_t = exp(lambda_t),  lambda_t = b * sigmoid(a_t) or -softplus(a_t)
+ *     S_t = g_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,  S_0 = h0
+ *     o_t = S_t^T q_t,                                             hT = S_L
+ * with one write strength beta_t per (token, head), given as an input
+ * (beta [Ttot][H]; the caller maps its own logits into (0, 1)).  Computed as
+ *     r_t = S_{t-1}^T k_t,   e_t = v_t - g_t r_t,   S_t = g_t S_{t-1} + beta_t k_t e_t^T,
+ * which is the same update with the projection multiplied out.
+ */
+int oracle_fwd_delta(int N, const int64_t *cu, int H, int dk, int dv,
+                     const double *q, const double *k, const double *v,
+                     const double *a, const double *beta, double b, int mode,
+                     const double *h0, double *o, double *hT, int nthreads)
+{
+    int used = set_threads(nthreads);
+    const int64_t units = (int64_t)N * H;
+    const size_t ssz = (size_t)dk * dv;
+
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(ssz * sizeof(double));
+        double *e = (double *)malloc((size_t)dv * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < units; ++u) {
+            const int n = (int)(u / H), h = (int)(u % H);
+            if (h0)
+                memcpy(S, h0 + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(S, 0, ssz * sizeof(double));
+            for (int64_t t = cu[n]; t < cu[n + 1]; ++t) {
+                const double g = exp(log_decay(a[t * H + h], b, mode));
+                const double bt = beta[t * H + h];
+                const double *qt = q + ((size_t)t * H + h) * dk;
+                const double *kt = k + ((size_t)t * H + h) * dk;
+                const double *vt = v + ((size_t)t * H + h) * dv;
+                double *ot = o + ((size_t)t * H + h) * dv;
+                /* e = v_t - g_t S_{t-1}^T k_t */
+                for (int j = 0; j < dv; ++j) {
+                    double r = 0.0;
+                    for (int i = 0; i < dk; ++i)
+                        r += S[(size_t)i * dv + j] * kt[i];
+                    e[j] = vt[j] - g * r;
+                }
+                /* S_t = g_t S_{t-1} + beta_t k_t e^T */
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + bt * kt[i] * e[j];
+                /* o_t = S_t^T q_t */
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; ++i)
+                        acc += S[(size_t)i * dv + j] * qt[i];
+                    ot[j] = acc;
+                }
+            }
+            if (hT)
+                memcpy(hT + (size_t)u * ssz, S, ssz * sizeof(double));
+        }
+        free(e);
+        free(S);
+    }
+    return used;
+}
+
+/*
+ * Reverse mode of oracle_fwd_delta for the loss <o, dO> + <hT, dhT>.  With D
+ * the adjoint of S_t and r, e as in the forward:
+ *   D += q_t dO_t^T;          dq_t = S_t dO_t
+ *   de = beta_t D^T k_t;      dv_t = de;            dr = -g_t de
+ *   dk_t = beta_t D e + S_{t-1} dr
+ *   dbeta_t = k_t^T D e
+ *   dlambda_t = g_t (<D, S_{t-1}> - r . de);        da_t = dlambda_t dlambda/da
+ *   D <- g_t D + k_t dr^T      (adjoint of S_{t-1})
+ * and dh0 = D at the end.  S_{t-1} comes from fp64 checkpoints every
+ * `window` tokens, recomputed forward inside each window.
+ */
+static void delta_step(int dk, int dv, double *S, const double *kt, const double *vt, double g, double bt,
+                       double *e)
+{
+    for (int j = 0; j < dv; ++j) {
+        double r = 0.0;
+        for (int i = 0; i < dk; ++i)
+            r += S[(size_t)i * dv + j] * kt[i];
+        e[j] = vt[j] - g * r;
+    }
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + bt * kt[i] * e[j];
+}
+
+int oracle_bwd_delta(int N, const int64_t *cu, int H, int dk, int dv,
+                     const double *q, const double *k, const double *v,
+                     const double *a, const double *beta, double b, int mode,
+                     const double *h0, const double *dO, const double *dhT,
+                     double *dq, double *dkk, double *dvv, double *da, double *dbeta,
+                     double *dh0, int window, int nthreads)
+{
+    int used = set_threads(nthreads);
+    const int64_t units = (int64_t)N * H;
+    const size_t ssz = (size_t)dk * dv;
+    if (window <= 0)
+        window = 1024;
+
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(ssz * sizeof(double));
+        double *D = (double *)malloc(ssz * sizeof(double));
+        double *e = (double *)malloc((size_t)dv * sizeof(double));
+        double *r = (double *)malloc((size_t)dv * sizeof(double));
+        double *de = (double *)malloc((size_t)dv * sizeof(double));
+        double *dr = (double *)malloc((size_t)dv * sizeof(double));
+        double *win = (double *)malloc((size_t)window * ssz * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < units; ++u) {
+            const int n = (int)(u / H), h = (int)(u % H);
+            const int64_t t0 = cu[n], L = cu[n + 1] - cu[n];
+            const int64_t nwin = (L + window - 1) / window;
+            double *ck = (double *)malloc((size_t)(nwin > 0 ? nwin : 1) * ssz * sizeof(double));
+
+            /* forward sweep: checkpoint S before each window */
+            if (h0)
+                memcpy(S, h0 + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(S, 0, ssz * sizeof(double));
+            for (int64_t t = 0; t < L; ++t) {
+                if (t % window == 0)
+                    memcpy(ck + (size_t)(t / window) * ssz, S, ssz * sizeof(double));
+                const int64_t tt = t0 + t;
+                delta_step(dk, dv, S, k + ((size_t)tt * H + h) * dk, v + ((size_t)tt * H + h) * dv,
+                           exp(log_decay(a[tt * H + h], b, mode)), beta[tt * H + h], e);
+            }
+
+            if (dhT)
+                memcpy(D, dhT + (size_t)u * ssz, ssz * sizeof(double));
+            else
+                memset(D, 0, ssz * sizeof(double));
+
+            for (int64_t w = nwin - 1; w >= 0; --w) {
+                const int64_t ws = w * window;
+                const int64_t we = (ws + window < L) ? ws + window : L;
+                memcpy(S, ck + (size_t)w * ssz, ssz * sizeof(double));
+                for (int64_t t = ws; t < we; ++t) {
+                    memcpy(win + (size_t)(t - ws) * ssz, S, ssz * sizeof(double));
+                    const int64_t tt = t0 + t;
+                    delta_step(dk, dv, S, k + ((size_t)tt * H + h) * dk, v + ((size_t)tt * H + h) * dv,
+                               exp(log_decay(a[tt * H + h], b, mode)), beta[tt * H + h], e);
+                }
+                for (int64_t t = we - 1; t >= ws; --t) {
+                    const int64_t tt = t0 + t;
+                    const double at = a[tt * H + h];
+                    const double g = exp(log_decay(at, b, mode));
+                    const double bt = beta[tt * H + h];
+                    const double *qt = q + ((size_t)tt * H + h) * dk;
+                    const double *kt = k + ((size_t)tt * H + h) * dk;
+                    const double *vt = v + ((size_t)tt * H + h) * dv;
+                    const double *gt = dO + ((size_t)tt * H + h) * dv;
+                    double *dqt = dq + ((size_t)tt * H + h) * dk;
+                    double *dkt = dkk + ((size_t)tt * H + h) * dk;
+                    double *dvt = dvv + ((size_t)tt * H + h) * dv;
+                    const double *Sp = win + (size_t)(t - ws) * ssz; /* S_{t-1} */
+                    /* r = S_{t-1}^T k_t,  e = v_t - g r */
+                    for (int j = 0; j < dv; ++j) {
+                        double acc = 0.0;
+                        for (int i = 0; i < dk; ++i)
+                            acc += Sp[(size_t)i * dv + j] * kt[i];
+                        r[j] = acc;
+                        e[j] = vt[j] - g * acc;
+                    }
+                    /* D += q_t dO_t^T  (adjoint of S_t) */
+                    for (int i = 0; i < dk; ++i)
+                        for (int j = 0; j < dv; ++j)
+                            D[(size_t)i * dv + j] += qt[i] * gt[j];
+                    /* dq_t = S_t dO_t with S_t = g S_{t-1} + beta k e^T */
+                    for (int i = 0; i < dk; ++i) {
+                        double acc = 0.0;
+                        for (int j = 0; j < dv; ++j)
+                            acc += (g * Sp[(size_t)i * dv + j] + bt * kt[i] * e[j]) * gt[j];
+                        dqt[i] = acc;
+                    }
+                    /* de = beta D^T k;  dv_t = de;  dr = -g de */
+                    for (int j = 0; j < dv; ++j) {
+                        double acc = 0.0;
+                        for (int i = 0; i < dk; ++i)
+                            acc += D[(size_t)i * dv + j] * kt[i];
+                        de[j] = bt * acc;
+                        dvt[j] = de[j];
+                        dr[j] = -g * de[j];
+                    }
+                    /* dk_t = beta D e + S_{t-1} dr;  dbeta_t = k^T D e */
+                    double db = 0.0;
+                    for (int i = 0; i < dk; ++i) {
+                        double De = 0.0, Sdr = 0.0;
+                        for (int j = 0; j < dv; ++j) {
+                            De += D[(size_t)i * dv + j] * e[j];
+                            Sdr += Sp[(size_t)i * dv + j] * dr[j];
+                        }
+                        dkt[i] = bt * De + Sdr;
+                        db += kt[i] * De;
+                    }
+                    dbeta[tt * H + h] = db;
+                    /* dlambda_t = g (<D, S_{t-1}> - r . de) */
+                    double dot = 0.0;
+                    for (size_t x = 0; x < ssz; ++x)
+                        dot += D[x] * Sp[x];
+                    double rde = 0.0;
+                    for (int j = 0; j < dv; ++j)
+                        rde += r[j] * de[j];
+                    da[tt * H + h] = g * (dot - rde) * log_decay_deriv(at, b, mode);
+                    /* adjoint of S_{t-1}: D <- g D + k dr^T */
+                    for (int i = 0; i < dk; ++i)
+                        for (int j = 0; j < dv; ++j)
+                            D[(size_t)i * dv + j] = g * D[(size_t)i * dv + j] + kt[i] * dr[j];
+                }
+            }
+            if (dh0)
+                memcpy(dh0 + (size_t)u * ssz, D, ssz * sizeof(double));
+            free(ck);
+        }
+        free(win);
+        free(dr);
+        free(de);
+        free(r);
+        free(e);
         free(D);
         free(S);
     }

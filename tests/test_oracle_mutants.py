@@ -6,7 +6,8 @@ a wrong operand, the decay applied after instead of before the update, a wrong
 gate derivative, an adjoint that is not decayed, a checkpoint window read from
 the wrong place, an ignored initial state), and runs the pins of the function
 it lives in (``test_oracle_pins.py`` for the scalar decay,
-``test_oracle_vec_pins.py`` for the per-channel decay) against the copy in a
+``test_oracle_vec_pins.py`` for the per-channel decay,
+``test_oracle_delta_pins.py`` for the gated delta rule) against the copy in a
 fresh interpreter.  The pins pass on an unmodified copy and fail on every
 mutant.  The committed oracle is never modified.
 """
@@ -20,6 +21,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
 VEC_PINS = os.path.join(ROOT, "tests", "test_oracle_vec_pins.py")
+DELTA_PINS = os.path.join(ROOT, "tests", "test_oracle_delta_pins.py")
 
 # (name, text in bdla_oracle.c, replacement[, occurrence]): the text occurs
 # exactly once, or, where the scalar and per-channel functions share a line,
@@ -75,6 +77,23 @@ VEC_MUTANTS = [
 ]
 
 
+# the gated delta rule (fwd_delta / bwd_delta), checked by its own pins
+DELTA_MUTANTS = [
+    ("delta retrieval not decayed", "e[j] = vt[j] - g * r;", "e[j] = vt[j] - r;", 1),
+    ("delta projection built from q", "r += S[(size_t)i * dv + j] * kt[i];", "r += S[(size_t)i * dv + j] * qt[i];", 1),
+    ("delta write strength applied twice", "S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + bt * kt[i] * e[j];",
+     "S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + bt * bt * kt[i] * e[j];", 1),
+    ("delta backward: retrieval adjoint without the gate", "dr[j] = -g * de[j];", "dr[j] = -de[j];"),
+    ("delta backward: state adjoint misses the projection", "D[(size_t)i * dv + j] = g * D[(size_t)i * dv + j] + kt[i] * dr[j];",
+     "D[(size_t)i * dv + j] = g * D[(size_t)i * dv + j];"),
+    ("delta backward: dbeta from v instead of e", "De += D[(size_t)i * dv + j] * e[j];",
+     "De += D[(size_t)i * dv + j] * vt[j];"),
+    ("delta backward: decay gradient misses the retrieval term", "g * (dot - rde) * log_decay_deriv",
+     "g * dot * log_decay_deriv"),
+    ("delta backward: dk misses S dr", "dkt[i] = bt * De + Sdr;", "dkt[i] = bt * De;"),
+]
+
+
 def _copy_oracle(dst, mutation=None):
     pkg = os.path.join(dst, "oracle")
     os.makedirs(pkg)
@@ -110,12 +129,13 @@ def test_unmodified_copy_passes_the_pins(tmp_path):
     where = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__)"], cwd=str(tmp_path),
                            capture_output=True, text=True, timeout=120)
     assert where.stdout.strip().startswith(str(tmp_path)), where.stdout + where.stderr
-    for pins in (PINS, VEC_PINS):
+    for pins in (PINS, VEC_PINS, DELTA_PINS):
         r = _run_pins(str(tmp_path), pins)
         assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
-CASES = [(m, PINS) for m in MUTANTS] + [(m, VEC_PINS) for m in VEC_MUTANTS]
+CASES = ([(m, PINS) for m in MUTANTS] + [(m, VEC_PINS) for m in VEC_MUTANTS] +
+         [(m, DELTA_PINS) for m in DELTA_MUTANTS])
 
 
 @pytest.mark.parametrize("mutant,pins", CASES, ids=[c[0][0] for c in CASES])
