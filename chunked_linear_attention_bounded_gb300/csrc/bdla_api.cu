@@ -206,7 +206,7 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     // 128-token block, or (fp32) block starts of strides dividing it
     const bool fused_ckpt = ckpt && ckpt_stride % kBlock == 0;
     const bool split_ckpt = ckpt && !fused_ckpt && kBlock % ckpt_stride == 0 && ckpt_dtype == BDLA_F32 &&
-                            (int64_t)total_tokens(d) / kBlock + (varlen ? n_docs : d.B) < 65535;
+                            (int64_t)total_tokens(d) / kBlock + (varlen ? n_docs : d.B) <= INT32_MAX;
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     {
         KernelMark mark_(BDLA_KERNEL_DECAY, p.stream);

@@ -44,7 +44,7 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                 float *__restrict__ hT, float *__restrict__ ckpt, int ckpt_stride,
                 int64_t n_slots, int n_docs, int seg_blk, const float *__restrict__ seg_init)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
     const int tid = threadIdx.x;
     const int j0 = blockIdx.x * kDvSlice;
@@ -160,45 +160,66 @@ fwd_tile_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 // Checkpoints inside the 128-token blocks.  The tensor-core forward has
 // written the state at every block start (fp32, same slot layout); this
 // kernel fills the states at the block's inner multiples of the stride, one
-// CTA per (64-column slice, head, block), all blocks at once: from the block
-// start S, each 16-token tile c applies
+// CTA per (block, head), all blocks at once: from the block start S, each
+// 16-token tile c applies
 //   S <- e^{gamma_c} S + (K o w)_c^T V_c,   w_t = e^{gamma_c - Gamma_t} <= 1
 // (Gamma tile-local, gamma_c its value at the tile's last token).  The update
 // is one 16-token bf16 warp MMA per 16 x 16 state tile (wmma, fp32
-// accumulate); each warp keeps its state tiles in accumulator fragments, scales
-// them by e^{gamma_c} (the same factor for every element) and stores them to
-// the checkpoint directly.  The block's weighted keys and value slice are
-// staged in shared memory once.
+// accumulate).  Warp w keeps rows 16 (w mod DK/16) .. +15 of the state over
+// its share of the columns in accumulator fragments, scales them by
+// e^{gamma_c} (one factor for every element), and writes each inner state
+// through a staging panel in shared memory with bulk async copies, one per
+// row.  The work is all output bandwidth: the CTA reads k, v and the
+// block-start state once (bulk async copies onto one mbarrier, k weighted in
+// place afterwards) and writes up to seven states of DK x DV fp32.  Rows in
+// shared memory are padded by 16 bytes so that the fragment loads and stores
+// of consecutive rows fall in different banks.
 constexpr int kExpThreads = 256;
 constexpr int kExpWarps = kExpThreads / 32;
+constexpr int kExpRows = 128 - kChunk;   // tokens feeding the inner states (the last tile feeds none)
 
-template <int DK>
+template <int DK, int DV>
 struct ExpSmem {
-    __nv_bfloat16 kw[128][DK];          // k_t o w_t
-    __nv_bfloat16 v[128][kDvSlice];
-    float w[128];        // e^{gamma_c - Gamma_t} for the token's tile c
+    static constexpr int kRG = DK / 16;                 // row groups
+    static constexpr int kNC = DV * kRG / kExpWarps;    // columns per warp
+    static constexpr int kLdS = kNC + 4;                // padded panel row (floats)
+    static constexpr int kLdK = DK + 8, kLdV = DV + 8;  // padded bf16 rows
+    float stage[kExpWarps][16 * kLdS];                  // one panel per warp
+    __nv_bfloat16 kw[kExpRows][kLdK];                   // k_t o w_t
+    __nv_bfloat16 v[kExpRows][kLdV];
+    float w[kExpRows];   // e^{gamma_c - Gamma_t} for the token's tile c
     float eg[128 / kChunk];
+    alignas(8) uint64_t bar;   // the block's loads
 };
+static_assert(sizeof(ExpSmem<128, 256>) <= 227 * 1024, "expansion tile exceeds shared memory");
 
-template <int DK>
-__global__ void __launch_bounds__(kExpThreads)
+template <int DK, int DV>
+__global__ void __launch_bounds__(kExpThreads, 1)
 ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                    const float *__restrict__ gamma, const int32_t *__restrict__ cu, int T,
-                   int64_t tokens, int n_docs, int H, int dv, float *__restrict__ ckpt,
-                   int ckpt_stride, int64_t n_slots)
+                   int64_t tokens, int n_docs, int H, float *__restrict__ ckpt, int ckpt_stride,
+                   int64_t n_slots, uint64_t wait_ns, DeviceStatus *st)
 {
     using namespace nvcuda;
+    using Sm = ExpSmem<DK, DV>;
+    constexpr int RG = Sm::kRG, NC = Sm::kNC, NF = NC / 16, LDS = Sm::kLdS;
+    static_assert(NC % 16 == 0 && kExpWarps % RG == 0, "warp split");
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    ExpSmem<DK> &sm = *reinterpret_cast<ExpSmem<DK> *>(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int j0 = blockIdx.x * kDvSlice, h = blockIdx.y;
-    const SegSpan blk = seg_span(cu, T, tokens, n_docs, blockIdx.z, 1);   // one 128-token block
+    Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y;
+    const SegSpan blk = seg_span(cu, T, tokens, n_docs, (int)blockIdx.x, 1);   // one 128-token block
     if (!blk.valid || blk.len <= kChunk)
         return;   // no tile boundary inside the block
     const int n = blk.n;
     const int64_t off0 = (int64_t)blk.blk_base * 128;   // doc-local first token
     const int ntiles = (int)((blk.len + kChunk - 1) / kChunk);
     const int m = (ntiles - 1) * kChunk;   // tokens feeding the inner states (full tiles)
+    constexpr uint32_t kPanelBytes = 16u * NC * 4u;   // bytes of one warp's panel
+    if (tid == 0) {
+        sm100::mbar_init(&sm.bar, 1);
+        sm100::mbar_fence_init();
+    }
     if (tid < m) {
         const float gt = gamma[(int64_t)h * tokens + blk.start + tid];
         const float gend = gamma[(int64_t)h * tokens + blk.start + (tid | (kChunk - 1))];
@@ -207,59 +228,83 @@ ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__r
             sm.eg[tid / kChunk] = expf(gend);
     }
     __syncthreads();
-    // weighted keys and the value slice of the block's first ntiles - 1 tiles
+    if (tid == 0)
+        sm100::mbar_arrive_expect_tx(&sm.bar, (uint32_t)m * (DK + DV) * 2u + kExpWarps * kPanelBytes);
+    __syncthreads();   // the expected bytes are posted before any copy can complete
+    // keys and values of the block's first ntiles - 1 tiles, one row per thread
+    if (tid < m) {
+        sm100::bulk_load(&sm.kw[tid][0], k + ((size_t)(blk.start + tid) * H + h) * DK, DK * 2u, &sm.bar);   // row stride padded
+        sm100::bulk_load(&sm.v[tid][0], v + ((size_t)(blk.start + tid) * H + h) * DV, DV * 2u, &sm.bar);
+    }
+    // this warp's panel of the block-start state: rows r0 .. r0 + 15, columns c0 .. c0 + NC - 1
+    const int r0 = 16 * (warp % RG), c0 = (warp / RG) * NC;
+    const size_t sstride = (size_t)DK * DV;
+    float *stg = sm.stage[warp];
+    if (lane < 16) {   // one panel row per lane
+        const int64_t slot = ckpt_slot(blk.doc_start, n, off0 / ckpt_stride, ckpt_stride);
+        const float *src = ckpt + ((size_t)h * n_slots + slot) * sstride + (size_t)r0 * DV + c0;
+        sm100::bulk_load(stg + lane * LDS, src + (size_t)lane * DV, NC * 4u, &sm.bar);
+    }
+    const bool ok = sm100::mbar_wait(&sm.bar, 0, wait_ns);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0)
+            set_status(st, BDLA_ERR_TIMEOUT, (unsigned)blockIdx.x);
+        if (!ok)
+            sm100::mbar_wait(&sm.bar, 0, wait_ns);   // let the copies land before the CTA leaves
+        return;
+    }
+    // weight the keys in place: k_t o w_t
     for (int e = tid; e < m * (DK / 8); e += kExpThreads) {
         const int t = e / (DK / 8), c8 = e % (DK / 8);
-        const uint4 raw = reinterpret_cast<const uint4 *>(k + ((size_t)(blk.start + t) * H + h) * DK)[c8];
+        uint4 *p = reinterpret_cast<uint4 *>(&sm.kw[t][0]) + c8;
+        const uint4 raw = *p;
         const float wt = sm.w[t];
         const uint32_t x[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t y[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             y[i] = sm100::pack_bf16(sm100::bf16_lo(x[i]) * wt, sm100::bf16_hi(x[i]) * wt);
-        reinterpret_cast<uint4 *>(&sm.kw[t][0])[c8] = make_uint4(y[0], y[1], y[2], y[3]);
+        *p = make_uint4(y[0], y[1], y[2], y[3]);
     }
-    for (int e = tid; e < m * (kDvSlice / 8); e += kExpThreads) {
-        const int t = e / (kDvSlice / 8), c8 = e % (kDvSlice / 8);
-        reinterpret_cast<uint4 *>(&sm.v[t][0])[c8] =
-            reinterpret_cast<const uint4 *>(v + ((size_t)(blk.start + t) * H + h) * dv + j0)[c8];
-    }
-    __syncthreads();
-    // this warp's 16 x 16 tiles of the DK x 64 state slice
-    constexpr int kTiles = (DK / 16) * (kDvSlice / 16);
-    constexpr int kPerWarp = kTiles / kExpWarps;
-    const size_t sstride = (size_t)DK * dv;
-    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc[kPerWarp];
-    {
-        const int64_t slot = ckpt_slot(blk.doc_start, n, off0 / ckpt_stride, ckpt_stride);
-        const float *src = ckpt + ((size_t)h * n_slots + slot) * sstride + j0;
+    __syncthreads();   // kw weighted
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc[NF];
 #pragma unroll
-        for (int x = 0; x < kPerWarp; ++x) {
-            const int tile = warp * kPerWarp + x, mi = tile / (kDvSlice / 16), ni = tile % (kDvSlice / 16);
-            wmma::load_matrix_sync(acc[x], src + (size_t)(16 * mi) * dv + 16 * ni, dv, wmma::mem_row_major);
-        }
-    }
+    for (int f = 0; f < NF; ++f)
+        wmma::load_matrix_sync(acc[f], stg + 16 * f, LDS, wmma::mem_row_major);
+    __syncwarp();
     for (int c = 0; c + 1 < ntiles; ++c) {   // the last tile ends the block: not needed here
         const float eg = sm.eg[c];
-        const int64_t tl = off0 + (int64_t)(c + 1) * kChunk;   // doc-local token the state precedes
-        const bool wr = tl % ckpt_stride == 0;
-        float *dst = ckpt + ((size_t)h * n_slots + (size_t)ckpt_slot(blk.doc_start, n, tl / ckpt_stride, ckpt_stride)) *
-                                sstride + j0;
+        wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+        wmma::load_matrix_sync(fa, &sm.kw[16 * c][r0], Sm::kLdK);            // A[i][t] = kw[t][r0 + i]
 #pragma unroll
-        for (int x = 0; x < kPerWarp; ++x) {
-            const int tile = warp * kPerWarp + x, mi = tile / (kDvSlice / 16), ni = tile % (kDvSlice / 16);
+        for (int f = 0; f < NF; ++f) {
 #pragma unroll
-            for (int e = 0; e < acc[x].num_elements; ++e)
-                acc[x].x[e] *= eg;
-            wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+            for (int e = 0; e < acc[f].num_elements; ++e)
+                acc[f].x[e] *= eg;
             wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-            wmma::load_matrix_sync(fa, &sm.kw[16 * c][16 * mi], DK);          // A[i][t] = kw[t][i]
-            wmma::load_matrix_sync(fb, &sm.v[16 * c][16 * ni], kDvSlice);     // B[t][j] = v[t][j]
-            wmma::mma_sync(acc[x], fa, fb, acc[x]);
-            if (wr)
-                wmma::store_matrix_sync(dst + (size_t)(16 * mi) * dv + 16 * ni, acc[x], dv, wmma::mem_row_major);
+            wmma::load_matrix_sync(fb, &sm.v[16 * c][c0 + 16 * f], Sm::kLdV);  // B[t][j] = v[t][c0 + j]
+            wmma::mma_sync(acc[f], fa, fb, acc[f]);
+        }
+        const int64_t tl = off0 + (int64_t)(c + 1) * kChunk;   // doc-local token the state precedes
+        if (tl % ckpt_stride != 0)
+            continue;
+        if (lane < 16)
+            sm100::tma_store_wait_read();   // the previous panel has left the staging buffer
+        __syncwarp();
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            wmma::store_matrix_sync(stg + 16 * f, acc[f], LDS, wmma::mem_row_major);
+        sm100::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane < 16) {   // one panel row per lane
+            float *dst = ckpt + ((size_t)h * n_slots + (size_t)ckpt_slot(blk.doc_start, n, tl / ckpt_stride, ckpt_stride)) *
+                                    sstride + (size_t)(r0 + lane) * DV + c0;
+            sm100::bulk_store(dst, stg + lane * LDS, NC * 4u);
+            sm100::tma_store_commit();
         }
     }
+    if (lane < 16)
+        sm100::tma_store_wait_read();   // shared memory stays valid until the copies have read it
 }
 
 template <typename K>
@@ -304,25 +349,35 @@ cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const _
         return cudaSuccess;
     const int64_t n_slots = ckpt_slots(p, ckpt_stride);
     const int64_t blocks = (p.tokens + 127) / 128 + p.n_docs;   // block slots (seg_span with 1-block segments)
-    if (blocks > 65535)
+    if (blocks > INT32_MAX || p.H > 65535)
         return cudaErrorInvalidValue;
-    dim3 grid(p.dv / kDvSlice, p.H, (unsigned)blocks);
+    dim3 grid((unsigned)blocks, p.H);
+    const WaitCfg wc = wait_cfg(BDLA_KERNEL_STATES);
     cudaError_t err;
+#define BDLA_EXPAND(DK_, DV_)                                                                       \
+    do {                                                                                            \
+        auto kern = ckpt_expand_kernel<DK_, DV_>;                                                   \
+        if ((err = set_smem(kern, sizeof(ExpSmem<DK_, DV_>))) != cudaSuccess)                       \
+            return err;                                                                             \
+        kern<<<grid, kExpThreads, sizeof(ExpSmem<DK_, DV_>), p.stream>>>(                           \
+            k, v, gamma, p.cu, p.T, p.tokens, p.n_docs, p.H, ckpt, ckpt_stride, n_slots, wc.ns, p.st); \
+    } while (0)
     if (p.dk == 64) {
-        auto kern = ckpt_expand_kernel<64>;
-        if ((err = set_smem(kern, sizeof(ExpSmem<64>))) != cudaSuccess)
-            return err;
-        kern<<<grid, kExpThreads, sizeof(ExpSmem<64>), p.stream>>>(k, v, gamma, p.cu, p.T, p.tokens,
-                                                                  p.n_docs, p.H, p.dv, ckpt, ckpt_stride,
-                                                                  n_slots);
+        if (p.dv == 64)
+            BDLA_EXPAND(64, 64);
+        else if (p.dv == 128)
+            BDLA_EXPAND(64, 128);
+        else
+            BDLA_EXPAND(64, 256);
     } else {
-        auto kern = ckpt_expand_kernel<128>;
-        if ((err = set_smem(kern, sizeof(ExpSmem<128>))) != cudaSuccess)
-            return err;
-        kern<<<grid, kExpThreads, sizeof(ExpSmem<128>), p.stream>>>(k, v, gamma, p.cu, p.T, p.tokens,
-                                                                   p.n_docs, p.H, p.dv, ckpt, ckpt_stride,
-                                                                   n_slots);
+        if (p.dv == 64)
+            BDLA_EXPAND(128, 64);
+        else if (p.dv == 128)
+            BDLA_EXPAND(128, 128);
+        else
+            BDLA_EXPAND(128, 256);
     }
+#undef BDLA_EXPAND
     return cudaGetLastError();
 }
 
