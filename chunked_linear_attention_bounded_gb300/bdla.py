@@ -36,7 +36,8 @@ EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", 
            "bdla_bwd_varlen", "bdla_read_device_status", "bdla_status_string", "bdla_version",
            "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
            "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall",
-           "bdla_workspace_bytes_vec", "bdla_fwd_vec", "bdla_bwd_vec")
+           "bdla_workspace_bytes_vec", "bdla_fwd_vec", "bdla_bwd_vec", "bdla_workspace_bytes_delta",
+           "bdla_fwd_delta")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 STALL_NONE, STALL_PRODUCER, STALL_MMA, STALL_EPILOGUE = 0, 1, 2, 3
 
@@ -102,6 +103,10 @@ def lib():
         L.bdla_bwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, Dims,
                                    ci, vp, sz, vp]
         L.bdla_bwd_vec.restype = ci
+        L.bdla_workspace_bytes_delta.argtypes = [ci, Dims, ci]
+        L.bdla_workspace_bytes_delta.restype = sz
+        L.bdla_fwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, Dims, ci, vp, sz, vp]
+        L.bdla_fwd_delta.restype = ci
         del i32
         _lib = L
     return _lib
@@ -450,3 +455,51 @@ def bwd_vec(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None,
     if st:
         raise BdlaError(st, "bdla_bwd_vec")
     return dq, dk_, dv_, da, dh0
+
+
+# ---------------------------------------------------------------- gated delta rule
+def _delta_checks(q, k, v, a, beta, cu_seqlens, h0):
+    _check(q, "q", torch.bfloat16, 4)
+    _check(k, "k", torch.bfloat16, 4)
+    _check(v, "v", torch.bfloat16, 4)
+    _check(a, "a", torch.float32, 3)
+    _check(beta, "beta", torch.float32, 3)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or a.shape != q.shape[:3] or beta.shape != a.shape:
+        raise ValueError("q, k, v, a, beta shapes disagree")
+    n_docs = 0
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, 1)
+        n_docs = cu_seqlens.numel() - 1
+    n_seq = n_docs if n_docs else B
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, 4)
+        if tuple(h0.shape) != (n_seq, H, dk, dv):
+            raise ValueError("h0 must be [n_docs, H, dk, dv]")
+    return B, T, H, dk, dv, n_docs, n_seq
+
+
+def _ws_delta(op, q, v, n_docs, ws):
+    B, T, H, dk = q.shape
+    need = int(lib().bdla_workspace_bytes_delta(op, Dims(B, T, H, dk, v.shape[-1]), n_docs))
+    if need == 0:
+        raise BdlaError(ERR_UNSUPPORTED, "bdla_workspace_bytes_delta")
+    if ws is None:
+        return Workspace(need, q.device)
+    return ws.ensure(need)
+
+
+def fwd_delta(q, k, v, a, beta, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUNDED,
+              o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, out=None, hT_out=None, stream=None):
+    """Gated delta rule forward (a, beta [B, T, H]).  Returns (o, hT)."""
+    B, T, H, dk, dv, n_docs, n_seq = _delta_checks(q, k, v, a, beta, cu_seqlens, h0)
+    o = out if out is not None else torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    hT = hT_out if hT_out is not None else torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _ws_delta(OP_FWD, q, v, n_docs, ws)
+    st = lib().bdla_fwd_delta(_p(q), _p(k), _p(v), _p(a), _p(beta), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0),
+                              _p(o), _dtype_code(o.dtype), _p(hT), _dims(q, v), mode, ws.ptr, ws.nbytes,
+                              _stream_handle(stream))
+    if st:
+        raise BdlaError(st, "bdla_fwd_delta")
+    return o, hT

@@ -553,6 +553,57 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
     return BDLA_OK;
 }
 
+// ---------------------------------------------------------------- gated delta rule
+namespace {
+
+size_t delta_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off)
+{
+    size_t off = round_up(kStatusBytes);
+    *states_off = off;
+    if (op == BDLA_OP_BWD) {
+        Problem p{};
+        p.tokens = total_tokens(d);
+        p.n_docs = n_docs;
+        off += round_up((size_t)d.H * delta_state_slots(p) * d.dk * d.dv * 2);
+    }
+    return off;
+}
+
+}  // namespace
+
+size_t bdla_workspace_bytes_delta(int op, bdla_dims d, int n_docs)
+{
+    const bool varlen = n_docs > 0;
+    if (check_vec(d, varlen ? reinterpret_cast<const int32_t *>(1) : nullptr, n_docs) != BDLA_OK)
+        return 0;
+    size_t so;
+    return delta_layout(op, d, varlen ? n_docs : d.B, &so);
+}
+
+bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const float *a, const float *beta,
+                           float b, int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0, void *o,
+                           bdla_dtype o_dtype, float *hT, bdla_dims d, bdla_decay_mode mode, void *ws,
+                           size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    if (total_tokens(d) > 0 && (!q || !k || !v || !a || !beta || !o))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
+        !aligned16(hT) || !aligned16(a) || !aligned16(beta))
+        return BDLA_ERR_ALIGN;
+    if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
+        return BDLA_ERR_DTYPE;
+    size_t so;
+    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
+    KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
+    BDLA_CUDA(launch_delta_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                               static_cast<const __nv_bfloat16 *>(v), a, beta, h0, o, o_dtype == BDLA_F32, hT,
+                               nullptr));
+    return BDLA_OK;
+}
+
 bdla_status bdla_set_wait_limit_ns(uint64_t ns)
 {
     g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);

@@ -1,0 +1,350 @@
+// Gated delta rule with the bounded log-decay: the "Delta Net-style"
+// structure that "Engineering Long-Context Training for Trillion-Parameter MoE
+// Models: Three Key Breakthroughs" (sec. 3.1) names beside linear attention,
+// with the same decay parameterisation (sec. 3.2).  The rule is the published
+// gated delta rule ("Gated Delta Networks: Improving Mamba2 with Delta Rule",
+// 2024) for a dk x dv state read by o = S^T q:
+//     S_t = g_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   g_t = e^{lambda_t}.
+//
+// Multiplying out the projection gives gated linear attention with the
+// pseudo-values delta_t = beta_t (v_t - g_t S_{t-1}^T k_t).  Inside a 16-token
+// tile (Gamma the tile-local cumsum of lambda, gamma its total, S_0 the state
+// before the tile) they solve one unit lower-triangular system (the WY / UT
+// form of the rule):
+//   L     = diag(beta) strict_tril((K K^T) o E),   E_ts = e^{Gamma_t - Gamma_s} <= 1
+//   T     = (I + L)^{-1} diag(beta)
+//   Delta = T V - (T diag(e^{Gamma}) K) S_0
+//   O     = diag(e^{Gamma}) Q S_0 + tril((Q K^T) o E) Delta
+//   S_C   = e^{gamma} S_0 + K^T (diag(e^{gamma - Gamma}) Delta)
+// Every decay factor is at most 1.  The 16 x 16 products Q K^T and K K^T are
+// taken from the exact bf16 inputs and the pair factors applied to their fp32
+// values; the solve, T V, T diag(e^Gamma) K and the causal product with Delta
+// run in fp32 on CUDA cores (all contractions of length 16); the three
+// products with the state (Q S_0, W S_0, K^T Delta) are bf16 warp MMAs (wmma
+// 16x16x16, fp32 accumulate) against a bf16 copy of the fp32 state.  Folding
+// e^{-Gamma} into bf16 key operands, as the linear-attention kernels do, is
+// legal under the bound here too, but the rounding then passes through the
+// triangular solve into every output (about 3e-3 relative error on o in an
+// fp32 simulation, against 1e-4 this way).
+#include <mma.h>
+
+#include "bdla_internal.h"
+
+namespace bdla {
+
+namespace {
+
+using namespace nvcuda;
+
+constexpr int kT = kChunk;       // 16-token tile
+constexpr int kDT = 128;         // threads (4 warps)
+constexpr int kDvs = 64;         // value columns per forward CTA
+
+template <int DK>
+struct DeltaFwdSmem {
+    static constexpr int LK = DK + 8;     // padded rows (bf16), so consecutive rows change banks
+    static constexpr int LV = kDvs + 8;
+    static constexpr int LF = kDvs + 4;   // padded rows (fp32)
+    static constexpr int LS = kT + 4;     // 16 x 16 fp32 tiles
+    float S32[DK * LF];                   // fp32 state (this CTA's value columns)
+    __nv_bfloat16 S16[DK * LV];           // its bf16 copy (MMA operand)
+    __nv_bfloat16 Q[kT * LK], K[kT * LK], Wb[kT * LK];
+    __nv_bfloat16 V[kT * LV], Dh[kT * LV];
+    float QK[kT * LS], KK[kT * LS], Tm[kT * LS];
+    float QS[kT * LF], WS[kT * LF], Dl[kT * LF];
+    float G[kT], eG[kT], beta[kT];
+};
+
+// Rows [t0, t0 + nv) of a token-major bf16 tensor [tokens][H][d] (columns
+// [c0, c0 + w)) into a [16][ld] tile; rows past nv are zero.  w % 8 == 0.
+__device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv_bfloat16 *src, int64_t t0, int nv,
+                                          int H, int h, int d, int c0, int w)
+{
+    const int chunks = kT * w / 8;
+    for (int e = threadIdx.x; e < chunks; e += kDT) {
+        const int t = e / (w / 8), c = (e % (w / 8)) * 8;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (t < nv)
+            val = *reinterpret_cast<const uint4 *>(src + ((t0 + t) * H + h) * (int64_t)d + c0 + c);
+        *reinterpret_cast<uint4 *>(dst + t * ld + c) = val;
+    }
+}
+
+// C[16][16] (ld LS) = A B^T for two [16][DK] bf16 tiles (ld LK); one warp.
+template <int DK, int LK, int LS>
+__device__ __forceinline__ void gram16(float *C, const __nv_bfloat16 *A, const __nv_bfloat16 *B)
+{
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+    wmma::fill_fragment(acc, 0.0f);
+#pragma unroll
+    for (int kk = 0; kk < DK / 16; ++kk) {
+        wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
+        wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
+        wmma::load_matrix_sync(fa, A + 16 * kk, LK);
+        wmma::load_matrix_sync(fb, B + 16 * kk, LK);   // B^T[kk][s] = B[s][kk]
+        wmma::mma_sync(acc, fa, fb, acc);
+    }
+    wmma::store_matrix_sync(C, acc, LS, wmma::mem_row_major);
+}
+
+// C[16][16 ni .. +15] (ld LF) = A S for A [16][DK] bf16 (ld LK) and the bf16
+// state S [DK][kDvs] (ld LV); one warp, one 16-column panel.
+template <int DK, int LK, int LV, int LF>
+__device__ __forceinline__ void times_state(float *C, const __nv_bfloat16 *A, const __nv_bfloat16 *S, int ni)
+{
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+    wmma::fill_fragment(acc, 0.0f);
+#pragma unroll
+    for (int kk = 0; kk < DK / 16; ++kk) {
+        wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
+        wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
+        wmma::load_matrix_sync(fa, A + 16 * kk, LK);
+        wmma::load_matrix_sync(fb, S + 16 * kk * LV + 16 * ni, LV);
+        wmma::mma_sync(acc, fa, fb, acc);
+    }
+    wmma::store_matrix_sync(C + 16 * ni, acc, LF, wmma::mem_row_major);
+}
+
+// One CTA per (64-column value slice, head, document), tiles in order.
+// STATES: no q and no output; the bf16 state before every tile goes to
+// `states` ([H][slots][DK][dv], slot = floor(doc_start / 16) + n + tile).
+template <int DK, bool STATES>
+__global__ void __launch_bounds__(kDT)
+delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
+                 const float *__restrict__ beta, float b, int mode, const int32_t *__restrict__ cu, int T,
+                 int64_t tokens, int H, int dv, const float *__restrict__ h0, void *__restrict__ o, int o_f32,
+                 float *__restrict__ hT, __nv_bfloat16 *__restrict__ states, int64_t n_slots, DeviceStatus *st)
+{
+    using Sm = DeltaFwdSmem<DK>;
+    constexpr int LK = Sm::LK, LV = Sm::LV, LF = Sm::LF, LS = Sm::LS;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = blockIdx.x * kDvs, h = blockIdx.y, n = blockIdx.z;
+    const DocSpan d = doc_span(cu, n, T);
+    if (!doc_valid(d, tokens)) {
+        if (tid == 0)
+            set_status(st, BDLA_ERR_DEVICE, (unsigned)n);
+        return;
+    }
+    const int64_t unit = (int64_t)n * H + h;
+    const size_t sstride = (size_t)DK * dv;
+    for (int e = tid; e < DK * kDvs; e += kDT) {
+        const int i = e / kDvs, j = e % kDvs;
+        const float x = h0 != nullptr ? h0[unit * sstride + (size_t)i * dv + j0 + j] : 0.0f;
+        sm.S32[i * LF + j] = x;
+        sm.S16[i * LV + j] = __float2bfloat16_rn(x);
+    }
+    __syncthreads();
+    const int ntile = (int)((d.len + kT - 1) / kT);
+    for (int c = 0; c < ntile; ++c) {
+        const int64_t t0 = d.start + (int64_t)c * kT;
+        const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
+        // ---- the tile's inputs, the decay cumsum and the write strengths
+        if (STATES) {
+            __nv_bfloat16 *dst = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride + j0;
+            for (int e = tid; e < DK * kDvs / 8; e += kDT) {
+                const int row = e / (kDvs / 8), col = (e % (kDvs / 8)) * 8;
+                *reinterpret_cast<uint4 *>(dst + (size_t)row * dv + col) =
+                    *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
+            }
+        } else {
+            load_rows(sm.Q, LK, q, t0, nv, H, h, DK, 0, DK);
+        }
+        load_rows(sm.K, LK, k, t0, nv, H, h, DK, 0, DK);
+        load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, kDvs);
+        if (warp == 0) {
+            const bool in = lane < nv;
+            float x = in ? log_decay(a[(t0 + lane) * H + h], b, mode) : 0.0f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {   // inclusive scan over the tile
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off)
+                    x += y;
+            }
+            if (lane < kT) {
+                sm.G[lane] = x;
+                sm.eG[lane] = expf(x);
+                sm.beta[lane] = in ? beta[(t0 + lane) * H + h] : 0.0f;
+            }
+        }
+        __syncthreads();
+        // ---- products from the exact inputs: K K^T, Q K^T, Q S_0
+        if (warp == 0) {
+            gram16<DK, LK, LS>(sm.KK, sm.K, sm.K);
+        } else if (!STATES) {
+            if (warp == 1)
+                gram16<DK, LK, LS>(sm.QK, sm.Q, sm.K);
+            for (int ni = warp - 2; ni < kDvs / 16; ni += 2)
+                if (ni >= 0)
+                    times_state<DK, LK, LV, LF>(sm.QS, sm.Q, sm.S16, ni);
+        }
+        __syncthreads();
+        // ---- pair factors: L = beta_t (k_t.k_s) E_ts (s < t), P = (q_t.k_s) E_ts (s <= t)
+        for (int e = tid; e < kT * kT; e += kDT) {
+            const int t = e / kT, s = e % kT;
+            const float E = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.0f;
+            sm.KK[t * LS + s] = s < t ? sm.beta[t] * sm.KK[t * LS + s] * E : 0.0f;
+            if (!STATES)
+                sm.QK[t * LS + s] *= E;
+        }
+        __syncthreads();
+        // ---- T = (I + L)^{-1} diag(beta): lane j solves column j by forward substitution
+        if (warp == 0 && lane < kT) {
+            const int j = lane;
+            float x[kT];
+#pragma unroll
+            for (int t = 0; t < kT; ++t) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int s = 0; s < t; ++s)
+                    acc += sm.KK[t * LS + s] * x[s];
+                x[t] = t < j ? 0.0f : (t == j ? sm.beta[j] : -acc);
+                sm.Tm[t * LS + j] = x[t];
+            }
+        }
+        __syncthreads();
+        // ---- W = T diag(e^{Gamma}) K (bf16 operand), U = T V (fp32, into Dl)
+        for (int e = tid; e < kT * DK; e += kDT) {
+            const int t = e / DK, i = e % DK;
+            float acc = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kT; ++s)
+                acc += sm.Tm[t * LS + s] * sm.eG[s] * __bfloat162float(sm.K[s * LK + i]);
+            sm.Wb[t * LK + i] = __float2bfloat16_rn(acc);
+        }
+        for (int e = tid; e < kT * kDvs; e += kDT) {
+            const int t = e / kDvs, j = e % kDvs;
+            float acc = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kT; ++s)
+                acc += sm.Tm[t * LS + s] * __bfloat162float(sm.V[s * LV + j]);
+            sm.Dl[t * LF + j] = acc;
+        }
+        __syncthreads();
+        // ---- W S_0
+        times_state<DK, LK, LV, LF>(sm.WS, sm.Wb, sm.S16, warp);
+        __syncthreads();
+        // ---- Delta = U - W S_0 and its state-update operand diag(e^{gamma - Gamma}) Delta
+        const float gam = sm.G[kT - 1];
+        {
+            const int t = tid >> 3, c8 = (tid & 7) * 8;   // one row segment of 8 per thread
+            const float w = expf(gam - sm.G[t]);
+            __align__(16) __nv_bfloat16 h8[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float dl = sm.Dl[t * LF + c8 + x] - sm.WS[t * LF + c8 + x];
+                sm.Dl[t * LF + c8 + x] = dl;
+                h8[x] = __float2bfloat16_rn(w * dl);
+            }
+            *reinterpret_cast<uint4 *>(sm.Dh + t * LV + c8) = *reinterpret_cast<const uint4 *>(h8);
+        }
+        __syncthreads();
+        // ---- O = diag(e^{Gamma}) Q S_0 + P Delta (rows t < nv)
+        if (!STATES) {
+            const int t = tid >> 3, c8 = (tid & 7) * 8;
+            float out[8];
+            const float eg = sm.eG[t];
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                out[x] = eg * sm.QS[t * LF + c8 + x];
+            for (int s = 0; s <= t; ++s) {
+                const float p = sm.QK[t * LS + s];
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    out[x] += p * sm.Dl[s * LF + c8 + x];
+            }
+            if (t < nv) {
+                const size_t off = ((size_t)(t0 + t) * H + h) * dv + j0 + c8;
+                if (o_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(o) + off);
+                    dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+                    dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+                } else {
+                    __align__(16) __nv_bfloat16 w8[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        w8[x] = __float2bfloat16_rn(out[x]);
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + off) =
+                        *reinterpret_cast<const uint4 *>(w8);
+                }
+            }
+        }
+        // ---- S <- e^{gamma} S + K^T (diag(e^{gamma - Gamma}) Delta)
+        {
+            const float eg = expf(gam);
+            for (int tile = warp; tile < (DK / 16) * (kDvs / 16); tile += kDT / 32) {
+                const int mi = tile / (kDvs / 16), ni = tile % (kDvs / 16);
+                wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+                wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+                wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
+                wmma::load_matrix_sync(acc, sm.S32 + 16 * mi * LF + 16 * ni, LF, wmma::mem_row_major);
+#pragma unroll
+                for (int x = 0; x < acc.num_elements; ++x)
+                    acc.x[x] *= eg;
+                wmma::load_matrix_sync(fa, sm.K + 16 * mi, LK);     // A[i][t] = K[t][16 mi + i]
+                wmma::load_matrix_sync(fb, sm.Dh + 16 * ni, LV);    // B[t][j] = Dh[t][16 ni + j]
+                wmma::mma_sync(acc, fa, fb, acc);
+                wmma::store_matrix_sync(sm.S32 + 16 * mi * LF + 16 * ni, acc, LF, wmma::mem_row_major);
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < DK * kDvs; e += kDT) {
+            const int i = e / kDvs, j = e % kDvs;
+            sm.S16[i * LV + j] = __float2bfloat16_rn(sm.S32[i * LF + j]);
+        }
+        __syncthreads();
+    }
+    if (hT != nullptr)
+        for (int e = tid; e < DK * kDvs; e += kDT) {
+            const int i = e / kDvs, j = e % kDvs;
+            hT[unit * sstride + (size_t)i * dv + j0 + j] = sm.S32[i * LF + j];
+        }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+int64_t delta_state_slots(const Problem &p) { return p.tokens / kT + p.n_docs + 1; }
+
+cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const float *a, const float *beta, const float *h0, void *o,
+                             int o_f32, float *hT, __nv_bfloat16 *states)
+{
+    if (p.n_docs <= 0)
+        return cudaSuccess;
+    dim3 grid(p.dv / kDvs, p.H, p.n_docs);
+    const int64_t slots = delta_state_slots(p);
+    cudaError_t err;
+#define BDLA_DELTA_FWD(DK_, ST_)                                                                    \
+    do {                                                                                            \
+        auto kern = delta_fwd_kernel<DK_, ST_>;                                                     \
+        if ((err = set_smem(kern, sizeof(DeltaFwdSmem<DK_>))) != cudaSuccess)                       \
+            return err;                                                                             \
+        kern<<<grid, kDT, sizeof(DeltaFwdSmem<DK_>), p.stream>>>(q, k, v, a, beta, p.b, p.mode, p.cu, p.T,   \
+                                                                 p.tokens, p.H, p.dv, h0, o, o_f32, hT,     \
+                                                                 states, slots, p.st);                      \
+    } while (0)
+    const bool st = states != nullptr;
+    if (p.dk == 64) {
+        if (st)
+            BDLA_DELTA_FWD(64, true);
+        else
+            BDLA_DELTA_FWD(64, false);
+    } else {
+        if (st)
+            BDLA_DELTA_FWD(128, true);
+        else
+            BDLA_DELTA_FWD(128, false);
+    }
+#undef BDLA_DELTA_FWD
+    return cudaGetLastError();
+}
+
+}  // namespace bdla

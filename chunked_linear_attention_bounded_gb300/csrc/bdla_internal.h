@@ -182,4 +182,12 @@ cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
                            const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
                            float *da, float *dh0);
 
+// Gated delta rule (a, beta: [tokens][H] fp32).  Forward: o, hT; with
+// `states` non-null it runs the states pass instead (no q, no o): the bf16
+// state before every 16-token tile into states [H][delta_state_slots][dk][dv].
+int64_t delta_state_slots(const Problem &p);
+cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const float *a, const float *beta, const float *h0, void *o,
+                             int o_f32, float *hT, __nv_bfloat16 *states);
+
 }  // namespace bdla

@@ -13,6 +13,8 @@ Recipe (one workload per context stage, 8K -> 64K -> 256K -> 1M tokens, from
                                     the per-channel decay)
   dO ~ N(0,1)                       bf16 upstream gradient
   h0 ~ N(0, h0_std) per document    fp32 (absent when h0_std == 0)
+  beta = sigmoid(N(0,1))            fp32 [B,T,H] write strengths (gated delta rule
+                                    workloads only; drawn after everything above)
 Packed documents: n_docs lengths u_i ~ U[lo, hi], rescaled so they sum to T
 (floor, remainder added to the last document).
 """
@@ -46,6 +48,7 @@ class Workload:
     o_f32: bool = False            # fp32 o (else bf16)
     ckpt_stride: int = 0           # >0: fp32 state checkpoints every ckpt_stride tokens
     vec: bool = False              # one decay logit per key channel: a [B,T,H,dk]
+    delta: bool = False            # gated delta rule: write strengths beta [B,T,H]
 
     @property
     def tokens(self) -> int:
@@ -71,6 +74,9 @@ WORKLOADS = {
     # per-channel decay (one logit per key channel) on the 64K stage's packed documents
     "varlen64k_vec": Workload("varlen64k_vec", B=1, T=65536, H=32, dk=128, dv=128, seed=1006,
                               h0_std=0.1, n_docs=8, doc_lo=1024, doc_hi=16384, vec=True),
+    # gated delta rule with the bounded decay on the 64K stage's packed documents
+    "varlen64k_delta": Workload("varlen64k_delta", B=1, T=65536, H=32, dk=128, dv=128, seed=1007,
+                                h0_std=0.1, n_docs=8, doc_lo=1024, doc_hi=16384, delta=True),
 }
 
 
@@ -93,7 +99,8 @@ def _randn(shape, g, chunk_rows=1 << 18):
 def make_inputs(w: Workload, with_grad: Optional[bool] = None) -> dict:
     """Returns CPU tensors: q,k [B,T,H,dk] bf16, v [B,T,H,dv] bf16, a [B,T,H]
     fp32, dO [B,T,H,dv] bf16 (unless forward-only), h0 [N,H,dk,dv] fp32 or None,
-    cu_seqlens int32 [N+1] (packed workloads) or None."""
+    cu_seqlens int32 [N+1] (packed workloads) or None, beta [B,T,H] fp32
+    (gated delta rule workloads) or None."""
     if with_grad is None:
         with_grad = not w.fwd_only
     g = torch.Generator(device="cpu")
@@ -114,7 +121,8 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None) -> dict:
     dO = _randn((B, T, H, dv), g).to(torch.bfloat16) if with_grad else None
     n_seq = (cu.numel() - 1) if cu is not None else B
     h0 = (_randn((n_seq, H, dk, dv), g) * w.h0_std) if w.h0_std > 0 else None
-    return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu)
+    beta = torch.sigmoid(_randn((B, T, H), g)).contiguous() if w.delta else None
+    return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu, beta=beta)
 
 
 def make_inputs_on(w: Workload, device, with_grad: bool = True) -> dict:
@@ -142,7 +150,8 @@ def make_inputs_on(w: Workload, device, with_grad: bool = True) -> dict:
     dO = rn((B, T, H, dv)).to(torch.bfloat16) if with_grad else None
     n_seq = (cu.numel() - 1) if cu is not None else B
     h0 = (rn((n_seq, H, dk, dv)) * w.h0_std) if w.h0_std > 0 else None
-    return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu)
+    beta = torch.sigmoid(rn((B, T, H))).contiguous() if w.delta else None
+    return dict(q=q, k=k, v=v, a=a, dO=dO, h0=h0, cu_seqlens=cu, beta=beta)
 
 
 def small_variant(w: Workload, T: int, H: Optional[int] = None, n_docs: Optional[int] = None,

@@ -246,6 +246,32 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
                          float *da, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
                          size_t ws_bytes, void *stream);
 
+/*
+ * Gated delta rule with the bounded log-decay: the "Delta Net-style"
+ * structure the first page names beside linear attention ("Engineering
+ * Long-Context Training for Trillion-Parameter MoE Models: Three Key
+ * Breakthroughs", sec. 3.1), with the sec. 3.2 decay in its gate.  The rule
+ * is the published gated delta rule ("Gated Delta Networks: Improving Mamba2
+ * with Delta Rule", 2024) for a dk x dv state read by o = S^T q:
+ *     S_t = g_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+ *     g_t = exp(lambda_t),  o_t = S_t^T q_t.
+ * Arguments as for bdla_fwd_vec / bdla_bwd_vec except:
+ *   a, da        fp32 [B, T, H]   (one decay logit per token and head)
+ *   beta, dbeta  fp32 [B, T, H]   write strengths beta_t (the caller maps its
+ *                own logits into [0, 1]; keys are expected L2-normalised) and
+ *                their gradient
+ *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise).  The
+ *   backward's workspace holds the bf16 state before every 16-token tile
+ *   (its own states pass): bdla_workspace_bytes_delta(BDLA_OP_BWD, ...)
+ *   bytes, status word first.
+ */
+size_t bdla_workspace_bytes_delta(int op, bdla_dims d, int n_docs);
+bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const float *a,
+                           const float *beta, float b, int chunk, const int32_t *cu_seqlens,
+                           int n_docs, const float *h0, void *o, bdla_dtype o_dtype, float *hT,
+                           bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
+                           void *stream);
+
 /* Static English description of a status code. */
 const char *bdla_status_string(bdla_status s);
 
