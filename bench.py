@@ -538,12 +538,15 @@ def ablation_leg(dev, steps: int = 5, warmup: int = 3):
             "ablation_over_bounded": res["c1m_ablation"] / res["c1m"], "steps": steps}
 
 
-def vec_arm(args, w, inp):
-    """Per-channel decay (bdla_fwd_vec / bdla_bwd_vec): one fwd+bwd step on
-    the packed 64K-stage documents with one decay logit per key channel.
-    Single GPU; one JSON line.  The roofline numerator counts the bytes the
-    method must move: q, k, v (bf16), a (fp32, dk per token-head), o (bf16);
-    backward q, k, v, dO, a in and dq, dk, dv, da (fp32) out."""
+def variant_arm(args, w, inp):
+    """Per-channel decay (bdla_fwd_vec / bdla_bwd_vec) or the gated delta rule
+    (bdla_fwd_delta / bdla_bwd_delta): one fwd+bwd step on the packed
+    64K-stage documents.  Single GPU; one JSON line.  The roofline numerator
+    counts the bytes the method must move: q, k, v (bf16), a (fp32: dk per
+    token-head for the per-channel decay, one otherwise), beta (fp32, delta
+    rule), o (bf16); backward q, k, v, dO, a, beta in and dq, dk, dv, da,
+    dbeta (fp32) out.  The bf16 states the backward's states pass writes are
+    not algorithmic bytes."""
     import torch
 
     from chunked_linear_attention_bounded_gb300 import bdla as B
@@ -552,19 +555,28 @@ def vec_arm(args, w, inp):
     n_seq = (g["cu_seqlens"].numel() - 1) if g["cu_seqlens"] is not None else w.B
     nd = n_seq if g["cu_seqlens"] is not None else 0
     Dm = B.Dims(w.B, w.T, w.H, w.dk, w.dv)
-    ws_f = B.Workspace(B.lib().bdla_workspace_bytes_vec(B.OP_FWD, Dm, nd), dev)
-    ws_b = B.Workspace(B.lib().bdla_workspace_bytes_vec(B.OP_BWD, Dm, nd), dev)
-    outs = (torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
+    wsb = B.lib().bdla_workspace_bytes_delta if w.delta else B.lib().bdla_workspace_bytes_vec
+    ws_f = B.Workspace(wsb(B.OP_FWD, Dm, nd), dev)
+    ws_b = B.Workspace(wsb(B.OP_BWD, Dm, nd), dev)
+    outs = [torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
             torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
             torch.empty(g["v"].shape, dtype=torch.float32, device=dev),
-            torch.empty(g["a"].shape, dtype=torch.float32, device=dev))
+            torch.empty(g["a"].shape, dtype=torch.float32, device=dev)]
+    if w.delta:
+        outs.append(torch.empty(g["beta"].shape, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream()
 
     def step():
+        if w.delta:
+            B.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                        mode=w.mode, ws=ws_f)
+            B.bwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], g["dO"], w.b, h0=g["h0"],
+                        cu_seqlens=g["cu_seqlens"], mode=w.mode, ws=ws_b, outs=tuple(outs))
+            return
         B.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"], mode=w.mode,
                   ws=ws_f)
         B.bwd_vec(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
-                  mode=w.mode, ws=ws_b, outs=outs)
+                  mode=w.mode, ws=ws_b, outs=tuple(outs))
     kernels = {"fwd": B.KERNEL_FWD, "states": B.KERNEL_STATES, "bwd": B.KERNEL_BWD}
     for _ in range(max(3, args.warmup)):
         step()
@@ -595,13 +607,16 @@ def vec_arm(args, w, inp):
     kernel_ms = {n: sum(a_.elapsed_time(b_) for a_, b_ in kev[n]) / K for n in kernels}
     th = w.B * w.T * w.H
     st = w.dk * w.dv * 4 * n_seq * w.H
-    ab = {"fwd": th * (2 * w.dk * 2 + 2 * w.dv + 4 * w.dk + 2 * w.dv) + 2 * st,
-          "bwd": th * (2 * w.dk * 2 + 2 * w.dv * 2 + 4 * w.dk + 4 * w.dk * 2 + 4 * w.dv + 4 * w.dk) + st}
+    a_b = 4 * w.dk if w.vec else 4            # decay logits per token-head
+    x_b = 4 if w.delta else 0                 # write strengths per token-head
+    ab = {"fwd": th * (2 * w.dk * 2 + 2 * w.dv + a_b + x_b + 2 * w.dv) + 2 * st,
+          "bwd": th * (2 * w.dk * 2 + 2 * w.dv * 2 + a_b + x_b + 4 * w.dk * 2 + 4 * w.dv + a_b + x_b) + st}
     hbm, hbm_src = peaks()
     dom = max(("fwd", "bwd"), key=lambda n: kernel_ms[n])
     achieved = ab[dom] / (kernel_ms[dom] / 1000.0) / 1e9
     tokens = w.B * w.T
-    out = {"metric": "tokens/s fwd+bwd, per-channel decay (T=64K packed, H=32, d=128, bf16)",
+    what = "gated delta rule" if w.delta else "per-channel decay"
+    out = {"metric": f"tokens/s fwd+bwd, {what} (T=64K packed, H=32, d=128, bf16)",
            "value": tokens / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": K,
            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, 1),
@@ -682,12 +697,13 @@ def main():
         return
     inp = make_inputs(w, with_grad=True)
     if args.impl == "reference":
-        if w.vec:
-            print(json.dumps({"impl": "reference", "unavailable": "the per-channel mode has no oracle timing arm"}))
+        if w.vec or w.delta:
+            print(json.dumps({"impl": "reference",
+                              "unavailable": "the per-channel and delta-rule modes have no oracle timing arm"}))
             return
         reference_arm(args, w, inp)
-    elif w.vec:
-        vec_arm(args, w, inp)
+    elif w.vec or w.delta:
+        variant_arm(args, w, inp)
     else:
         ours_arm(args, w, inp)
 

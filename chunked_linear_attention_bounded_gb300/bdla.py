@@ -37,7 +37,7 @@ EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", 
            "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
            "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall",
            "bdla_workspace_bytes_vec", "bdla_fwd_vec", "bdla_bwd_vec", "bdla_workspace_bytes_delta",
-           "bdla_fwd_delta")
+           "bdla_fwd_delta", "bdla_bwd_delta")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 STALL_NONE, STALL_PRODUCER, STALL_MMA, STALL_EPILOGUE = 0, 1, 2, 3
 
@@ -107,6 +107,9 @@ def lib():
         L.bdla_workspace_bytes_delta.restype = sz
         L.bdla_fwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, Dims, ci, vp, sz, vp]
         L.bdla_fwd_delta.restype = ci
+        L.bdla_bwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     Dims, ci, vp, sz, vp]
+        L.bdla_bwd_delta.restype = ci
         del i32
         _lib = L
     return _lib
@@ -503,3 +506,31 @@ def fwd_delta(q, k, v, a, beta, b: float = -5.0, h0=None, cu_seqlens=None, mode:
     if st:
         raise BdlaError(st, "bdla_fwd_delta")
     return o, hT
+
+
+def bwd_delta(q, k, v, a, beta, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, mode: int = BOUNDED,
+              want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, stream=None):
+    """Gated delta rule backward.  Returns (dq, dk, dv, da, dbeta, dh0);
+    dh0 is None unless asked for."""
+    B, T, H, dk, dv, n_docs, n_seq = _delta_checks(q, k, v, a, beta, cu_seqlens, h0)
+    _check(dO, "dO", torch.bfloat16, 4)
+    if dO.shape != v.shape:
+        raise ValueError("dO must match v")
+    if dhT is not None:
+        _check(dhT, "dhT", torch.float32, 4)
+    dev = q.device
+    if outs is None:
+        outs = (torch.empty(q.shape, dtype=torch.float32, device=dev),
+                torch.empty(k.shape, dtype=torch.float32, device=dev),
+                torch.empty(v.shape, dtype=torch.float32, device=dev),
+                torch.empty(a.shape, dtype=torch.float32, device=dev),
+                torch.empty(beta.shape, dtype=torch.float32, device=dev))
+    dq, dk_, dv_, da, dbeta = outs
+    dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
+    ws = _ws_delta(OP_BWD, q, v, n_docs, ws)
+    st = lib().bdla_bwd_delta(_p(q), _p(k), _p(v), _p(a), _p(beta), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0),
+                              _p(dO), _p(dhT), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dbeta), _p(dh0), _dims(q, v),
+                              mode, ws.ptr, ws.nbytes, _stream_handle(stream))
+    if st:
+        raise BdlaError(st, "bdla_bwd_delta")
+    return dq, dk_, dv_, da, dbeta, dh0

@@ -604,6 +604,39 @@ bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const fl
     return BDLA_OK;
 }
 
+bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const float *a, const float *beta,
+                           float b, int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
+                           const void *dO, const float *dhT, float *dq, float *dk, float *dv, float *da,
+                           float *dbeta, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
+                           size_t ws_bytes, void *stream)
+{
+    BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
+    BDLA_TRY(check_decay(b, chunk, mode));
+    if (total_tokens(d) > 0 && (!q || !k || !v || !a || !beta || !dO || !dq || !dk || !dv || !da || !dbeta))
+        return BDLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(a) ||
+        !aligned16(beta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(da) ||
+        !aligned16(dbeta) || !aligned16(h0) || !aligned16(dhT) || !aligned16(dh0))
+        return BDLA_ERR_ALIGN;
+    size_t so;
+    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
+    auto *states = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    {
+        KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
+        BDLA_CUDA(launch_delta_fwd(p, qb, kb, vb, a, beta, h0, nullptr, 0, nullptr, states));
+    }
+    {
+        KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(launch_delta_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, beta, states, dhT,
+                                   dq, dk, dv, da, dbeta, dh0));
+    }
+    return BDLA_OK;
+}
+
 bdla_status bdla_set_wait_limit_ns(uint64_t ns)
 {
     g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);

@@ -303,6 +303,453 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         }
 }
 
+// ---------------------------------------------------------------- backward
+// Reverse walk over a document's tiles, one CTA per (head, document) holding
+// all value columns, with the adjoint D of the state at the tile end kept in
+// accumulator fragments (warp w owns the 16 x 16 tiles w, w + 8, ...).  Per
+// tile, with S_0 the bf16 state before it (states pass), the forward
+// quantities are recomputed (E, P, L, T, W, U, Delta) and then
+//   dDelta = P^T dO + diag(w) K D                     (w_t = e^{gamma - Gamma_t})
+//   dP     = tril(dO Delta^T),  dW = -dDelta S_0^T,  dT = dDelta V^T + dW (diag(e^Gamma) K)^T
+//   dv     = T^T dDelta,        dM = T^T dW
+//   X      = (I + L)^{-T} dT,   dL = -strict_tril(X T^T),  dbeta_t = X_tt + sum_s dL_ts (K K^T o E)_ts
+//   dq     = diag(e^Gamma) dO S_0^T + (dP o E) K
+//   dk     = (dP o E)^T Q + (diag(w) Delta) D^T + diag(e^Gamma) dM + (dA + dA^T) K,
+//            dA = diag(beta) (dL o E)
+//   D     <- e^{gamma} D + Q^T diag(e^Gamma) dO - W^T dDelta
+// and the decay gradient as sums that never subtract large equal terms: over
+// the pairs s < r <= t of the pair terms dP o P + dL o L, suffix sums of the
+// terms through e^{Gamma_t}, prefix sums of the terms through w_t, and the
+// state term e^{gamma} <S_0, D>.  Products with the state or the adjoint are
+// bf16 warp MMAs; the 16-long contractions are fp32 on CUDA cores.
+constexpr int kBT = 256;   // backward threads (8 warps)
+
+template <int DK, int DV>
+struct DeltaBwdSmem {
+    static constexpr int LK = DK + 8, LV = DV + 8;
+    static constexpr int LW = (DK > DV ? DK : DV) + 4;   // 16-row fp32 buffers
+    static constexpr int LS = kT + 4;
+    __nv_bfloat16 S16[DK * LV];   // state before the tile
+    __nv_bfloat16 D16[DK * LV];   // bf16 copy of the adjoint at the tile end
+    __nv_bfloat16 Q[kT * LK], K[kT * LK], Wb[kT * LK];
+    __nv_bfloat16 V[kT * LV], dO[kT * LV], nDb[kT * LV], Dhb[kT * LV], eGdO[kT * LV];
+    float B1[kT * LW];   // U, then Delta
+    float B2[kT * LW];   // W S_0, then dO S_0^T
+    float B3[kT * LW];   // Q S_0, then dW, then dM
+    float B4[kT * LW];   // K D, then dDelta
+    float B5[kT * LW];   // (diag(w) Delta) D^T
+    float E[kT * LS], P[kT * LS], KE[kT * LS], Lm[kT * LS], Tm[kT * LS], dP[kT * LS], X[kT * LS], dL[kT * LS];
+    float stage[kBT / 32][256];   // per-warp 16 x 16 fp32 staging
+    float G[kT], eG[kT], w[kT], beta[kT], sq[kT], sm_[kT], wdw[kT], red[kBT / 32];
+};
+static_assert(sizeof(DeltaBwdSmem<128, 128>) <= 227 * 1024, "delta backward tile exceeds shared memory");
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kBT, 1)
+delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                 const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ dO,
+                 const float *__restrict__ a, const float *__restrict__ beta, float b, int mode,
+                 const int32_t *__restrict__ cu, int T, int64_t tokens, int H,
+                 const __nv_bfloat16 *__restrict__ states, int64_t n_slots, const float *__restrict__ dhT,
+                 float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, float *__restrict__ da,
+                 float *__restrict__ dbeta, float *__restrict__ dh0, DeviceStatus *st)
+{
+    using Sm = DeltaBwdSmem<DK, DV>;
+    constexpr int LK = Sm::LK, LV = Sm::LV, LW = Sm::LW, LS = Sm::LS;
+    constexpr int NW = kBT / 32;
+    constexpr int NFD = (DK / 16) * (DV / 16) / NW;   // adjoint fragments per warp
+    static_assert(NFD >= 1 && (DK / 16) * (DV / 16) % NW == 0, "adjoint split");
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, n = blockIdx.y;
+    const DocSpan d = doc_span(cu, n, T);
+    if (!doc_valid(d, tokens)) {
+        if (tid == 0)
+            set_status(st, BDLA_ERR_DEVICE, (unsigned)n);
+        return;
+    }
+    const int64_t unit = (int64_t)n * H + h;
+    const size_t sstride = (size_t)DK * DV;
+    float *stg = sm.stage[warp];
+    // ---- the adjoint at the document end: fragments and bf16 copy
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> Df[NFD];
+#pragma unroll
+    for (int x = 0; x < NFD; ++x) {
+        const int tile = warp + NW * x, mi = tile / (DV / 16), ni = tile % (DV / 16);
+        for (int e = lane; e < 256; e += 32) {
+            const int r = e >> 4, c2 = e & 15;
+            stg[e] = dhT != nullptr ? dhT[unit * sstride + (size_t)(16 * mi + r) * DV + 16 * ni + c2] : 0.0f;
+        }
+        __syncwarp();
+        wmma::load_matrix_sync(Df[x], stg, 16, wmma::mem_row_major);
+        for (int e = lane; e < 256; e += 32)
+            sm.D16[(16 * mi + (e >> 4)) * LV + 16 * ni + (e & 15)] = __float2bfloat16_rn(stg[e]);
+        __syncwarp();
+    }
+    const int ntile = (int)((d.len + kT - 1) / kT);
+    for (int c = ntile - 1; c >= 0; --c) {
+        const int64_t t0 = d.start + (int64_t)c * kT;
+        const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
+        // ---- P0: inputs, the state before the tile, decay scalars
+        {
+            const int rows_k = DK / 8, rows_v = DV / 8;
+            for (int e = tid; e < kT * rows_k; e += kBT) {
+                const int t = e / rows_k, c8 = (e % rows_k) * 8;
+                uint4 qv = make_uint4(0, 0, 0, 0), kv = qv;
+                if (t < nv) {
+                    const size_t off = ((size_t)(t0 + t) * H + h) * DK + c8;
+                    qv = *reinterpret_cast<const uint4 *>(q + off);
+                    kv = *reinterpret_cast<const uint4 *>(k + off);
+                }
+                *reinterpret_cast<uint4 *>(sm.Q + t * LK + c8) = qv;
+                *reinterpret_cast<uint4 *>(sm.K + t * LK + c8) = kv;
+            }
+            for (int e = tid; e < kT * rows_v; e += kBT) {
+                const int t = e / rows_v, c8 = (e % rows_v) * 8;
+                uint4 vv = make_uint4(0, 0, 0, 0), gv = vv;
+                if (t < nv) {
+                    const size_t off = ((size_t)(t0 + t) * H + h) * DV + c8;
+                    vv = *reinterpret_cast<const uint4 *>(v + off);
+                    gv = *reinterpret_cast<const uint4 *>(dO + off);
+                }
+                *reinterpret_cast<uint4 *>(sm.V + t * LV + c8) = vv;
+                *reinterpret_cast<uint4 *>(sm.dO + t * LV + c8) = gv;
+            }
+            const __nv_bfloat16 *src = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride;
+            for (int e = tid; e < DK * rows_v; e += kBT) {
+                const int row = e / rows_v, c8 = (e % rows_v) * 8;
+                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) =
+                    *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            }
+            if (warp == 0) {
+                const bool in = lane < nv;
+                float x = in ? log_decay(a[(t0 + lane) * H + h], b, mode) : 0.0f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off)
+                        x += y;
+                }
+                const float gam = __shfl_sync(0xffffffffu, x, kT - 1);
+                if (lane < kT) {
+                    sm.G[lane] = x;
+                    sm.eG[lane] = expf(x);
+                    sm.w[lane] = expf(gam - x);
+                    sm.beta[lane] = in ? beta[(t0 + lane) * H + h] : 0.0f;
+                }
+            }
+        }
+        __syncthreads();
+        const float gam = sm.G[kT - 1];
+        // ---- P1: K K^T, Q K^T, Q S_0, K D (MMAs); the state term <S_0, D>
+        {
+            constexpr int J = 2 + 2 * (DV / 16);
+            for (int job = warp; job < J; job += NW) {
+                if (job == 0)
+                    gram16<DK, LK, LS>(sm.KE, sm.K, sm.K);
+                else if (job == 1)
+                    gram16<DK, LK, LS>(sm.P, sm.Q, sm.K);
+                else if (job < 2 + DV / 16)
+                    times_state<DK, LK, LV, LW>(sm.B3, sm.Q, sm.S16, job - 2);
+                else
+                    times_state<DK, LK, LV, LW>(sm.B4, sm.K, sm.D16, job - 2 - DV / 16);
+            }
+            float part = 0.0f;
+#pragma unroll
+            for (int x = 0; x < NFD; ++x) {
+                const int tile = warp + NW * x, mi = tile / (DV / 16), ni = tile % (DV / 16);
+                wmma::store_matrix_sync(stg, Df[x], 16, wmma::mem_row_major);
+                __syncwarp();
+                for (int e = lane; e < 256; e += 32)
+                    part += stg[e] * __bfloat162float(sm.S16[(16 * mi + (e >> 4)) * LV + 16 * ni + (e & 15)]);
+                __syncwarp();
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (lane == 0)
+                sm.red[warp] = part;
+        }
+        __syncthreads();
+        // ---- P2: pair factors; row sums (Q S_0) . dO
+        for (int e = tid; e < kT * kT; e += kBT) {
+            const int t = e / kT, s = e % kT;
+            const float E = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.0f;
+            sm.E[t * LS + s] = E;
+            sm.P[t * LS + s] *= E;
+            const float ke = s < t ? sm.KE[t * LS + s] * E : 0.0f;
+            sm.KE[t * LS + s] = ke;
+            sm.Lm[t * LS + s] = sm.beta[t] * ke;
+        }
+        for (int t = warp; t < kT; t += NW) {
+            float part = 0.0f;
+            for (int j = lane; j < DV; j += 32)
+                part += sm.B3[t * LW + j] * __bfloat162float(sm.dO[t * LV + j]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (lane == 0)
+                sm.sq[t] = part;
+        }
+        __syncthreads();
+        // ---- P3: T = (I + L)^{-1} diag(beta); bf16 e^{Gamma} o dO
+        if (warp == 0 && lane < kT) {
+            const int j = lane;
+            float x[kT];
+#pragma unroll
+            for (int t = 0; t < kT; ++t) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int s = 0; s < t; ++s)
+                    acc += sm.Lm[t * LS + s] * x[s];
+                x[t] = t < j ? 0.0f : (t == j ? sm.beta[j] : -acc);
+                sm.Tm[t * LS + j] = x[t];
+            }
+        }
+        for (int e = tid; e < kT * DV; e += kBT) {
+            const int t = e / DV, j = e % DV;
+            sm.eGdO[t * LV + j] = __float2bfloat16_rn(sm.eG[t] * __bfloat162float(sm.dO[t * LV + j]));
+        }
+        __syncthreads();
+        // ---- P4: W = T diag(e^Gamma) K (bf16), U = T V (fp32)
+        for (int e = tid; e < kT * DK; e += kBT) {
+            const int t = e / DK, i = e % DK;
+            float acc = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kT; ++s)
+                acc += sm.Tm[t * LS + s] * sm.eG[s] * __bfloat162float(sm.K[s * LK + i]);
+            sm.Wb[t * LK + i] = __float2bfloat16_rn(acc);
+        }
+        for (int e = tid; e < kT * DV; e += kBT) {
+            const int t = e / DV, j = e % DV;
+            float acc = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kT; ++s)
+                acc += sm.Tm[t * LS + s] * __bfloat162float(sm.V[s * LV + j]);
+            sm.B1[t * LW + j] = acc;
+        }
+        __syncthreads();
+        // ---- P5: W S_0
+        for (int ni = warp; ni < DV / 16; ni += NW)
+            times_state<DK, LK, LV, LW>(sm.B2, sm.Wb, sm.S16, ni);
+        __syncthreads();
+        // ---- P6: Delta, diag(w) Delta (bf16), dDelta = P^T dO + diag(w) K D, -dDelta (bf16)
+        for (int e = tid; e < kT * DV; e += kBT) {
+            const int t = e / DV, j = e % DV;
+            const float dl = sm.B1[t * LW + j] - sm.B2[t * LW + j];
+            sm.B1[t * LW + j] = dl;
+            sm.Dhb[t * LV + j] = __float2bfloat16_rn(sm.w[t] * dl);
+            float acc = sm.w[t] * sm.B4[t * LW + j];
+            for (int s2 = t; s2 < kT; ++s2)
+                acc += sm.P[s2 * LS + t] * __bfloat162float(sm.dO[s2 * LV + j]);
+            sm.B4[t * LW + j] = acc;
+            sm.nDb[t * LV + j] = __float2bfloat16_rn(-acc);
+        }
+        __syncthreads();
+        // ---- P7: dW = (-dDelta) S_0^T, dO S_0^T, (diag(w) Delta) D^T  (N = DK panels)
+        for (int job = warp; job < 3 * (DK / 16); job += NW) {
+            const int kind = job / (DK / 16), ni = job % (DK / 16);
+            const __nv_bfloat16 *A = kind == 0 ? sm.nDb : (kind == 1 ? sm.dO : sm.Dhb);
+            const __nv_bfloat16 *Bm = kind == 2 ? sm.D16 : sm.S16;
+            float *C = kind == 0 ? sm.B3 : (kind == 1 ? sm.B2 : sm.B5);
+            wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+            wmma::fill_fragment(acc, 0.0f);
+#pragma unroll
+            for (int kk = 0; kk < DV / 16; ++kk) {
+                wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
+                wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
+                wmma::load_matrix_sync(fa, A + 16 * kk, LV);
+                wmma::load_matrix_sync(fb, Bm + 16 * ni * LV + 16 * kk, LV);   // B[j][i] = M[16 ni + i][j]
+                wmma::mma_sync(acc, fa, fb, acc);
+            }
+            wmma::store_matrix_sync(C + 16 * ni, acc, LW, wmma::mem_row_major);
+        }
+        __syncthreads();
+        // ---- P8: dP, dT, dv
+        for (int e = tid; e < kT * kT; e += kBT) {
+            const int t = e / kT, s = e % kT;
+            float acc = 0.0f;
+            if (s <= t)
+                for (int j = 0; j < DV; ++j)
+                    acc += __bfloat162float(sm.dO[t * LV + j]) * sm.B1[s * LW + j];
+            sm.dP[t * LS + s] = acc;
+            float dt = 0.0f;
+            for (int j = 0; j < DV; ++j)
+                dt += sm.B4[t * LW + j] * __bfloat162float(sm.V[s * LV + j]);
+            float dw = 0.0f;
+            for (int i = 0; i < DK; ++i)
+                dw += sm.B3[t * LW + i] * __bfloat162float(sm.K[s * LK + i]);
+            sm.X[t * LS + s] = dt + sm.eG[s] * dw;
+        }
+        for (int e = tid; e < kT * DV; e += kBT) {
+            const int t = e / DV, j = e % DV;
+            float acc = 0.0f;
+            for (int s = t; s < kT; ++s)
+                acc += sm.Tm[s * LS + t] * sm.B4[s * LW + j];
+            if (t < nv)
+                dv[((size_t)(t0 + t) * H + h) * DV + j] = acc;
+        }
+        __syncthreads();
+        // ---- P9: dM = T^T dW in place (thread = column); X = (I + L)^{-T} dT (lane = column)
+        if (tid < DK) {
+            const int i = tid;
+            float col[kT];
+#pragma unroll
+            for (int s = 0; s < kT; ++s)
+                col[s] = sm.B3[s * LW + i];
+#pragma unroll
+            for (int t = 0; t < kT; ++t) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int s = t; s < kT; ++s)
+                    acc += sm.Tm[s * LS + t] * col[s];
+                sm.B3[t * LW + i] = acc;
+            }
+        } else if (tid >= kBT - 32 && lane < kT) {
+            const int j = lane;
+            float x[kT];
+#pragma unroll
+            for (int t = kT - 1; t >= 0; --t) {
+                float acc = sm.X[t * LS + j];
+#pragma unroll
+                for (int s = t + 1; s < kT; ++s)
+                    acc -= sm.Lm[s * LS + t] * x[s];
+                x[t] = acc;
+            }
+            __syncwarp(0x0000ffffu);
+#pragma unroll
+            for (int t = 0; t < kT; ++t)
+                sm.X[t * LS + j] = x[t];
+        }
+        __syncthreads();
+        // ---- P10: dL = -strict_tril(X T^T)
+        for (int e = tid; e < kT * kT; e += kBT) {
+            const int t = e / kT, s = e % kT;
+            float acc = 0.0f;
+            if (s < t)
+                for (int u = 0; u <= s; ++u)   // T is lower-triangular: T_su = 0 for u > s
+                    acc -= sm.X[t * LS + u] * sm.Tm[s * LS + u];
+            sm.dL[t * LS + s] = acc;
+        }
+        __syncthreads();
+        // ---- P11: dq, dk; per-row sums for the decay gradient
+        {
+            constexpr int IPR = DK / 8;   // items per row, contiguous lanes
+            for (int e = tid; e < kT * IPR; e += kBT) {
+                const int t = e / IPR, c8 = (e % IPR) * 8;
+                float gq[8], gk[8];
+                const float eg = sm.eG[t];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    gq[x] = eg * sm.B2[t * LW + c8 + x];
+                    gk[x] = sm.B5[t * LW + c8 + x] + eg * sm.B3[t * LW + c8 + x];
+                }
+                for (int s = 0; s < kT; ++s) {
+                    const float dpe_ts = s <= t ? sm.dP[t * LS + s] * sm.E[t * LS + s] : 0.0f;   // as (t, s)
+                    const float dpe_st = t <= s ? sm.dP[s * LS + t] * sm.E[s * LS + t] : 0.0f;   // as (s, t)
+                    const float da_ts = s < t ? sm.beta[t] * sm.dL[t * LS + s] * sm.E[t * LS + s] : 0.0f;
+                    const float da_st = t < s ? sm.beta[s] * sm.dL[s * LS + t] * sm.E[s * LS + t] : 0.0f;
+                    const float ck = da_ts + da_st;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const float ks = __bfloat162float(sm.K[s * LK + c8 + x]);
+                        gq[x] += dpe_ts * ks;
+                        gk[x] += dpe_st * __bfloat162float(sm.Q[s * LK + c8 + x]) + ck * ks;
+                    }
+                }
+                float pm = 0.0f, pw = 0.0f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float kt = __bfloat162float(sm.K[t * LK + c8 + x]);
+                    pm += sm.B3[t * LW + c8 + x] * kt;
+                    pw += sm.B5[t * LW + c8 + x] * kt;
+                }
+#pragma unroll
+                for (int off = 1; off < IPR; off <<= 1) {
+                    pm += __shfl_xor_sync(0xffffffffu, pm, off);
+                    pw += __shfl_xor_sync(0xffffffffu, pw, off);
+                }
+                if (e % IPR == 0) {
+                    sm.sm_[t] = pm;
+                    sm.wdw[t] = pw;
+                }
+                if (t < nv) {
+                    const size_t off = ((size_t)(t0 + t) * H + h) * DK + c8;
+                    float4 *pq = reinterpret_cast<float4 *>(dq + off);
+                    float4 *pk = reinterpret_cast<float4 *>(dk + off);
+                    pq[0] = make_float4(gq[0], gq[1], gq[2], gq[3]);
+                    pq[1] = make_float4(gq[4], gq[5], gq[6], gq[7]);
+                    pk[0] = make_float4(gk[0], gk[1], gk[2], gk[3]);
+                    pk[1] = make_float4(gk[4], gk[5], gk[6], gk[7]);
+                }
+            }
+        }
+        __syncthreads();
+        // ---- P12: decay and write-strength gradients; D <- e^gamma D + Q^T (e^Gamma o dO) - W^T dDelta
+        if (warp == 0 && lane < kT) {
+            const int r = lane;
+            float cross = 0.0f;
+            for (int t = r; t < kT; ++t)
+                for (int s = 0; s < r; ++s)
+                    cross += sm.dP[t * LS + s] * sm.P[t * LS + s] + sm.dL[t * LS + s] * sm.Lm[t * LS + s];
+            float suffix = 0.0f, prefix = 0.0f;
+            for (int t = r; t < kT; ++t)
+                suffix += sm.eG[t] * (sm.sq[t] + sm.sm_[t]);
+            for (int t = 0; t < r; ++t)
+                prefix += sm.wdw[t];
+            float state = 0.0f;
+#pragma unroll
+            for (int x = 0; x < NW; ++x)
+                state += sm.red[x];
+            float db = sm.X[r * LS + r];
+            for (int s = 0; s < r; ++s)
+                db += sm.dL[r * LS + s] * sm.KE[r * LS + s];
+            if (r < nv) {
+                const size_t off = (size_t)(t0 + r) * H + h;
+                const float dl = cross + suffix + prefix + expf(gam) * state;
+                da[off] = dl * log_decay_deriv(a[off], b, mode);
+                dbeta[off] = db;
+            }
+        }
+        {
+            const float eg = expf(gam);
+#pragma unroll
+            for (int x = 0; x < NFD; ++x) {
+                const int tile = warp + NW * x, mi = tile / (DV / 16), ni = tile % (DV / 16);
+#pragma unroll
+                for (int e = 0; e < Df[x].num_elements; ++e)
+                    Df[x].x[e] *= eg;
+                wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+                wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
+                wmma::load_matrix_sync(fa, sm.Q + 16 * mi, LK);      // A[i][t] = Q[t][16 mi + i]
+                wmma::load_matrix_sync(fb, sm.eGdO + 16 * ni, LV);
+                wmma::mma_sync(Df[x], fa, fb, Df[x]);
+                wmma::load_matrix_sync(fa, sm.Wb + 16 * mi, LK);     // A[i][t] = W[t][16 mi + i]
+                wmma::load_matrix_sync(fb, sm.nDb + 16 * ni, LV);
+                wmma::mma_sync(Df[x], fa, fb, Df[x]);
+                wmma::store_matrix_sync(stg, Df[x], 16, wmma::mem_row_major);
+                __syncwarp();
+                for (int e = lane; e < 256; e += 32)
+                    sm.D16[(16 * mi + (e >> 4)) * LV + 16 * ni + (e & 15)] = __float2bfloat16_rn(stg[e]);
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+    }
+    if (dh0 != nullptr) {
+#pragma unroll
+        for (int x = 0; x < NFD; ++x) {
+            const int tile = warp + NW * x, mi = tile / (DV / 16), ni = tile % (DV / 16);
+            wmma::store_matrix_sync(stg, Df[x], 16, wmma::mem_row_major);
+            __syncwarp();
+            for (int e = lane; e < 256; e += 32)
+                dh0[unit * sstride + (size_t)(16 * mi + (e >> 4)) * DV + 16 * ni + (e & 15)] = stg[e];
+            __syncwarp();
+        }
+    }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes)
 {
@@ -344,6 +791,37 @@ cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __n
             BDLA_DELTA_FWD(128, false);
     }
 #undef BDLA_DELTA_FWD
+    return cudaGetLastError();
+}
+
+cudaError_t launch_delta_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a, const float *beta,
+                             const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
+                             float *da, float *dbeta, float *dh0)
+{
+    if (p.n_docs <= 0)
+        return cudaSuccess;
+    dim3 grid(p.H, p.n_docs);
+    const int64_t slots = delta_state_slots(p);
+    cudaError_t err;
+#define BDLA_DELTA_BWD(DK_, DV_)                                                                    \
+    do {                                                                                            \
+        auto kern = delta_bwd_kernel<DK_, DV_>;                                                     \
+        if ((err = set_smem(kern, sizeof(DeltaBwdSmem<DK_, DV_>))) != cudaSuccess)                  \
+            return err;                                                                             \
+        kern<<<grid, kBT, sizeof(DeltaBwdSmem<DK_, DV_>), p.stream>>>(                              \
+            q, k, v, dO, a, beta, p.b, p.mode, p.cu, p.T, p.tokens, p.H, states, slots, dhT, dq, dk, dv, da, \
+            dbeta, dh0, p.st);                                                                      \
+    } while (0)
+    if (p.dk == 64 && p.dv == 64)
+        BDLA_DELTA_BWD(64, 64);
+    else if (p.dk == 64)
+        BDLA_DELTA_BWD(64, 128);
+    else if (p.dv == 64)
+        BDLA_DELTA_BWD(128, 64);
+    else
+        BDLA_DELTA_BWD(128, 128);
+#undef BDLA_DELTA_BWD
     return cudaGetLastError();
 }
 

@@ -189,5 +189,9 @@ int64_t delta_state_slots(const Problem &p);
 cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *a, const float *beta, const float *h0, void *o,
                              int o_f32, float *hT, __nv_bfloat16 *states);
+cudaError_t launch_delta_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                             const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a, const float *beta,
+                             const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
+                             float *da, float *dbeta, float *dh0);
 
 }  // namespace bdla

@@ -271,6 +271,12 @@ bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const fl
                            int n_docs, const float *h0, void *o, bdla_dtype o_dtype, float *hT,
                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
                            void *stream);
+bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const float *a,
+                           const float *beta, float b, int chunk, const int32_t *cu_seqlens,
+                           int n_docs, const float *h0, const void *dO, const float *dhT,
+                           float *dq, float *dk, float *dv, float *da, float *dbeta, float *dh0,
+                           bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
+                           void *stream);
 
 /* Static English description of a status code. */
 const char *bdla_status_string(bdla_status s);

@@ -1,6 +1,7 @@
-"""GPU parity of the gated delta rule path (bdla_fwd_delta, through the C ABI)
-against the fp64 gated-delta oracle on the same seeded bytes.  Bar per
-tensor: relative L2 <= 5e-3 and max-abs <= 2e-2 * max|ref|."""
+"""GPU parity of the gated delta rule path (bdla_fwd_delta / bdla_bwd_delta,
+through the C ABI) against the fp64 gated-delta oracle on the same seeded
+bytes.  Bar per tensor: relative L2 <= 5e-3 and max-abs <= 2e-2 * max|ref|
+(o, hT, dq, dk, dv, da, dbeta, dh0)."""
 import dataclasses
 
 import numpy as np
@@ -21,30 +22,43 @@ def _delta_case(name, T, H=2, n_docs=None, **kw):
     return dataclasses.replace(w, delta=True, vec=False, **kw)
 
 
-def _run(w, inp, o_dtype=torch.bfloat16):
+def _run(w, inp, o_dtype=torch.bfloat16, with_grad=False, dhT=None):
     g = to_device(inp)
     ws = bdla.Workspace(256, "cuda")
     o, hT = bdla.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, h0=g.get("h0"),
                            cu_seqlens=g.get("cu_seqlens"), mode=w.mode, o_dtype=o_dtype, ws=ws)
+    out = dict(o=o, hT=hT)
+    if with_grad:
+        dq, dk, dv, da, dbeta, dh0 = bdla.bwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], g["dO"], w.b,
+                                                    h0=g.get("h0"), dhT=None if dhT is None else dhT.cuda(),
+                                                    cu_seqlens=g.get("cu_seqlens"), mode=w.mode, want_dh0=True,
+                                                    ws=ws)
+        out.update(dq=dq, dk=dk, dv=dv, da=da, dbeta=dbeta, dh0=dh0)
     torch.cuda.synchronize()
     assert ws.read_device_status() == 0
-    return dict(o=o, hT=hT)
+    return out
 
 
-def _oracle(inp, b, mode, heads=None):
+def _oracle(inp, b, mode, heads=None, with_grad=False, dhT=None):
     q = inp["q"]
     B, T = q.shape[0], q.shape[1]
     cu = cu_of(inp, B, T)
     args = [flat64(inp[x], heads) for x in ("q", "k", "v", "a", "beta")]
     h0 = heads64(inp.get("h0"), heads)
     o, hT = oracle.fwd_delta(*args, b, mode, h0=h0, cu_seqlens=cu)
-    return dict(o=o, hT=hT)
+    out = dict(o=o, hT=hT)
+    if with_grad:
+        dhT64 = None if dhT is None else heads64(dhT, heads)
+        dq, dk, dv, da, dbeta, dh0 = oracle.bwd_delta(*args, flat64(inp["dO"], heads), b, mode, h0=h0, dhT=dhT64,
+                                                      cu_seqlens=cu)
+        out.update(dq=dq, dk=dk, dv=dv, da=da, dbeta=dbeta, dh0=dh0)
+    return out
 
 
 def _compare(gpu, ref, heads=None):
     for n, r in ref.items():
         x = gpu[n]
-        if n == "hT":
+        if n in ("hT", "dh0"):
             x = x if heads is None else x[:, heads]
             got = x.double().cpu().numpy()
         else:
@@ -65,21 +79,23 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-T{c[1]}-dk{c[4]}-dv{c[5]}")
 @pytest.mark.parametrize("mode", [bdla.BOUNDED, bdla.SOFTPLUS])
-def test_delta_fwd_small(case, mode):
+def test_delta_fwd_bwd_small(case, mode):
     name, T, H, nd, dk, dv = case
     kw = dict(dk=dk, dv=dv, mode=mode, fwd_only=False)
     if mode == bdla.SOFTPLUS:
         kw.update(a_mean=2.0, a_std=2.0)
     w = _delta_case(name, T, H, nd, **kw)
-    inp = make_inputs(w, with_grad=False)
-    _compare(_run(w, inp), _oracle(inp, w.b, mode))
+    inp = make_inputs(w, with_grad=True)
+    n_seq = (inp["cu_seqlens"].numel() - 1) if inp["cu_seqlens"] is not None else w.B
+    dhT = torch.randn((n_seq, H, dk, dv), generator=torch.Generator().manual_seed(9)) * 0.1
+    _compare(_run(w, inp, with_grad=True, dhT=dhT), _oracle(inp, w.b, mode, with_grad=True, dhT=dhT))
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 33])
 def test_delta_edge_lengths(T):
     w = dataclasses.replace(_delta_case("c8k", T, H=2, dk=64, dv=64, h0_std=0.3), B=2)
-    inp = make_inputs(w, with_grad=False)
-    _compare(_run(w, inp, o_dtype=torch.float32), _oracle(inp, w.b, w.mode))
+    inp = make_inputs(w, with_grad=True)
+    _compare(_run(w, inp, o_dtype=torch.float32, with_grad=True), _oracle(inp, w.b, w.mode, with_grad=True))
 
 
 def test_delta_full_write_retrieves_the_value():
@@ -96,10 +112,12 @@ def test_delta_full_write_retrieves_the_value():
     np.testing.assert_allclose(gpu["o"].cpu().numpy(), v, rtol=0, atol=0.05)
 
 
+@pytest.mark.slow
 def test_delta_full_size_workload_sampled_heads():
-    """The 64K stage's packed documents at full size on the GPU; the oracle
-    checks two heads (every document, every token)."""
+    """The 64K stage's packed documents at full size on the GPU, forward and
+    backward; the oracle checks two heads (every document, every token)."""
     w = WORKLOADS["varlen64k_delta"]
-    inp = make_inputs(w, with_grad=False)
+    inp = make_inputs(w, with_grad=True)
     heads = [0, 21]
-    _compare(_run(w, inp), _oracle(inp, w.b, w.mode, heads=heads), heads=heads)
+    gpu = _run(w, inp, with_grad=True)
+    _compare(gpu, _oracle(inp, w.b, w.mode, heads=heads, with_grad=True), heads=heads)

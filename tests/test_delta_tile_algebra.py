@@ -126,6 +126,53 @@ def tile_bwd(q, k, v, a, beta, dO, h0, dhT, b, mode):
     return dq, dk, dv, da, dbeta, D
 
 
+def tile_bwd_one_pairs(q, k, v, lam, beta, S0, dO, D):
+    """The same reverse mode in the order the backward kernel takes it: the
+    16 x 16 products from the raw inputs with the pair factors E_ts =
+    e^{Gamma_t - Gamma_s} applied separately, and the decay gradient as
+    sums that never cancel: over the token pairs (s < r <= t) that cross r
+    for the pair terms of P and L, suffix sums of the terms through
+    e^{Gamma_t}, prefix sums of the terms through e^{gamma - Gamma_t}, and
+    the state term e^{gamma} <S_0, D>."""
+    G = np.cumsum(lam)
+    gam = G[-1]
+    n = len(q)
+    eG = np.exp(G)
+    w = np.exp(gam - G)
+    E = np.tril(np.exp(G[:, None] - G[None, :]))
+    A = k @ k.T
+    L = beta[:, None] * np.tril(A * E, -1)
+    P = np.tril((q @ k.T) * E)
+    T = np.linalg.solve(np.eye(n) + L, np.diag(beta))
+    M = eG[:, None] * k
+    W = T @ M
+    Delta = T @ v - W @ S0
+    QS = q @ S0
+    # adjoints
+    dDelta = P.T @ dO + w[:, None] * (k @ D)
+    dS0 = q.T @ (eG[:, None] * dO) + np.exp(gam) * D - W.T @ dDelta
+    dP = np.tril(dO @ Delta.T)
+    dW = -dDelta @ S0.T
+    dT = dDelta @ v.T + dW @ M.T
+    dv = T.T @ dDelta
+    dMm = T.T @ dW
+    X = np.linalg.solve((np.eye(n) + L).T, dT)
+    dL = -np.tril(X @ T.T, -1)
+    dbeta = np.diag(X) + np.sum(dL * np.tril(A * E, -1), axis=1)
+    dA = beta[:, None] * dL * E
+    dPE = dP * E
+    dq = eG[:, None] * (dO @ S0.T) + dPE @ k
+    dk = dPE.T @ q + (w[:, None] * Delta) @ D.T + eG[:, None] * dMm + (dA + dA.T) @ k
+    # decay gradient
+    pair = dP * P + dL * L                       # per pair (t, s): d/dGamma_t, minus d/dGamma_s
+    cross = np.array([pair[r:, :r].sum() for r in range(n)])
+    single_suffix = eG * np.sum(QS * dO, axis=1) + eG * np.sum(dMm * k, axis=1)
+    dw = np.sum(k * (Delta @ D.T), axis=1)       # d loss / d w_t
+    before = np.cumsum(w * dw) - w * dw          # sum over t < r
+    dlam = cross + np.cumsum(single_suffix[::-1])[::-1] + before + np.exp(gam) * np.sum(S0 * D)
+    return dq, dk, dv, dlam, dbeta, dS0
+
+
 def _case(rng, L, dk=6, dv=5, mode=oracle.BOUNDED):
     q = rng.standard_normal((L, 1, dk)) * 0.5
     k = rng.standard_normal((L, 1, dk))
@@ -167,3 +214,17 @@ def test_unit_lower_solve_is_the_nilpotent_product():
     L8 = L4 @ L4
     prod = (I - L) @ (I + L2) @ (I + L4) @ (I + L8)
     np.testing.assert_allclose(prod, np.linalg.inv(I + L), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [oracle.BOUNDED, oracle.SOFTPLUS])
+@pytest.mark.parametrize("L", [1, 9, 16])
+def test_delta_pair_form_of_the_tile_backward(mode, L):
+    """The kernel's evaluation order of one tile's reverse mode (raw-input
+    products, separate pair factors, non-cancelling decay-gradient sums)
+    equals the reverse mode of the tile's forward."""
+    rng = np.random.default_rng(400 + L)
+    q, k, v, a, beta, h0, dO, dhT = _case(rng, L, mode=mode)
+    lam = _lam(a[:, 0], -5.0, mode)
+    args = (q[:, 0], k[:, 0], v[:, 0], lam, beta[:, 0], h0[0, 0], dO[:, 0], dhT[0, 0])
+    for name, x, y in zip(("dq", "dk", "dv", "dlam", "dbeta", "dS0"), tile_bwd_one_pairs(*args), tile_bwd_one(*args)):
+        np.testing.assert_allclose(x, y, rtol=1e-9, atol=1e-11, err_msg=name)
