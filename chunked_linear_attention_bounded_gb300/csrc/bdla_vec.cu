@@ -47,9 +47,14 @@ using namespace nvcuda;
 constexpr int kT = kChunk;       // 16-token tile
 constexpr int kVecThreads = 128; // 4 warps
 
+// Row strides in shared memory, padded by 16 bytes so that the 16 rows a
+// warp MMA fragment touches fall in different banks.
+constexpr int padb(int d) { return d + 8; }   // bf16 rows
+constexpr int padf(int d) { return d + 4; }   // fp32 rows
+
 // Rows [t0, t0 + nv) of a token-major bf16 tensor [tokens][H][d] (columns
-// [c0, c0 + w)) into a [16][w] tile; rows past nv are zero.  w % 8 == 0.
-__device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int64_t t0, int nv,
+// [c0, c0 + w)) into a [16][ld] tile; rows past nv are zero.  w % 8 == 0.
+__device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv_bfloat16 *src, int64_t t0, int nv,
                                           int H, int h, int d, int c0, int w)
 {
     const int chunks = kT * w / 8;
@@ -58,7 +63,7 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, const __nv_bfloat1
         uint4 val = make_uint4(0, 0, 0, 0);
         if (t < nv)
             val = *reinterpret_cast<const uint4 *>(src + ((t0 + t) * H + h) * (int64_t)d + c0 + c);
-        *reinterpret_cast<uint4 *>(dst + t * w + c) = val;
+        *reinterpret_cast<uint4 *>(dst + t * ld + c) = val;
     }
 }
 
@@ -71,6 +76,7 @@ __device__ __forceinline__ void channel_pass(const float *__restrict__ a, int64_
                                              int mode, __nv_bfloat16 *Qt, __nv_bfloat16 *Kt, __nv_bfloat16 *Kh,
                                              float *gam_out, float *g)
 {
+    constexpr int LK = padb(DK);
     const int i = threadIdx.x;
     if (i >= DK)
         return;
@@ -85,11 +91,11 @@ __device__ __forceinline__ void channel_pass(const float *__restrict__ a, int64_
     const float gam = run;
 #pragma unroll
     for (int t = 0; t < kT; ++t) {
-        const float kr = __bfloat162float(Kt[t * DK + i]);
+        const float kr = __bfloat162float(Kt[t * LK + i]);
         if (Qt != nullptr)
-            Qt[t * DK + i] = __float2bfloat16_rn(__bfloat162float(Qt[t * DK + i]) * expf(G[t]));
-        Kt[t * DK + i] = __float2bfloat16_rn(kr * expf(-G[t]));
-        Kh[t * DK + i] = __float2bfloat16_rn(kr * expf(gam - G[t]));
+            Qt[t * LK + i] = __float2bfloat16_rn(__bfloat162float(Qt[t * LK + i]) * expf(G[t]));
+        Kt[t * LK + i] = __float2bfloat16_rn(kr * expf(-G[t]));
+        Kh[t * LK + i] = __float2bfloat16_rn(kr * expf(gam - G[t]));
         if (gam_out != nullptr)
             gam_out[t * DK + i] = G[t];
     }
@@ -101,36 +107,40 @@ template <int DK, int DV>
 __device__ __forceinline__ void state_update(float *S32, __nv_bfloat16 *S16, const __nv_bfloat16 *Kh,
                                              const __nv_bfloat16 *V, const float *g)
 {
-    for (int e = threadIdx.x; e < DK * DV; e += kVecThreads)
-        S32[e] *= g[e / DV];
-    __syncthreads();
+    constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV);
     const int warp = threadIdx.x >> 5;
     for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecThreads / 32) {
         const int mi = tile / (DV / 16), ni = tile % (DV / 16);
         wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
         wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
         wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-        wmma::load_matrix_sync(acc, S32 + 16 * mi * DV + 16 * ni, DV, wmma::mem_row_major);
-        wmma::load_matrix_sync(fa, Kh + 16 * mi, DK);          // A[m][t] = Kh[t][16 mi + m]
-        wmma::load_matrix_sync(fb, V + 16 * ni, DV);           // B[t][n] = V[t][16 ni + n]
+        // rows of one fragment: 16 * mi + r, each decayed by its own channel's factor
+        for (int e = threadIdx.x & 31; e < 256; e += 32)
+            S32[(16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15)] *= g[16 * mi + (e >> 4)];
+        __syncwarp();
+        wmma::load_matrix_sync(acc, S32 + 16 * mi * LF + 16 * ni, LF, wmma::mem_row_major);
+        wmma::load_matrix_sync(fa, Kh + 16 * mi, LK);          // A[m][t] = Kh[t][16 mi + m]
+        wmma::load_matrix_sync(fb, V + 16 * ni, LV);           // B[t][n] = V[t][16 ni + n]
         wmma::mma_sync(acc, fa, fb, acc);
-        wmma::store_matrix_sync(S32 + 16 * mi * DV + 16 * ni, acc, DV, wmma::mem_row_major);
+        wmma::store_matrix_sync(S32 + 16 * mi * LF + 16 * ni, acc, LF, wmma::mem_row_major);
+        __syncwarp();
+        for (int e = threadIdx.x & 31; e < 256; e += 32) {
+            const int x = (16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15);
+            S16[(16 * mi + (e >> 4)) * LV + 16 * ni + (e & 15)] = __float2bfloat16_rn(S32[x]);
+        }
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < DK * DV; e += kVecThreads)
-        S16[e] = __float2bfloat16_rn(S32[e]);
     __syncthreads();
 }
 
 template <int DK, int DV>
 struct VecFwdSmem {
-    float S32[DK * DV];
-    __nv_bfloat16 S16[DK * DV];
-    __nv_bfloat16 Qt[kT * DK], Kt[kT * DK], Kh[kT * DK];
-    __nv_bfloat16 V[kT * DV];
+    float S32[DK * padf(DV)];
+    __nv_bfloat16 S16[DK * padb(DV)];
+    __nv_bfloat16 Qt[kT * padb(DK)], Kt[kT * padb(DK)], Kh[kT * padb(DK)];
+    __nv_bfloat16 V[kT * padb(DV)];
     __nv_bfloat16 P[kT * kT];
     float A[kT * kT];
-    float O[kT * DV];
+    float O[kT * padf(DV)];
     float g[DK];
 };
 
@@ -147,6 +157,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     VecFwdSmem<DK, DV> &sm = *reinterpret_cast<VecFwdSmem<DK, DV> *>(smem_raw);
+    constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int j0 = blockIdx.x * DV, h = blockIdx.y, n = blockIdx.z;
     const DocSpan d = doc_span(cu, n, T);
@@ -158,9 +169,10 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     const int64_t unit = (int64_t)n * H + h;
     const size_t sstride = (size_t)DK * dv;
     for (int e = tid; e < DK * DV; e += kVecThreads) {
-        const float x = h0 != nullptr ? h0[unit * sstride + (size_t)(e / DV) * dv + j0 + e % DV] : 0.0f;
-        sm.S32[e] = x;
-        sm.S16[e] = __float2bfloat16_rn(x);
+        const int i = e / DV, j = e % DV;
+        const float x = h0 != nullptr ? h0[unit * sstride + (size_t)i * dv + j0 + j] : 0.0f;
+        sm.S32[i * LF + j] = x;
+        sm.S16[i * LV + j] = __float2bfloat16_rn(x);
     }
     __syncthreads();
     const int ntile = (int)((d.len + kT - 1) / kT);
@@ -173,13 +185,13 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             for (int e = tid; e < DK * DV / 8; e += kVecThreads) {
                 const int row = e / (DV / 8), col = (e % (DV / 8)) * 8;
                 *reinterpret_cast<uint4 *>(dst + (size_t)row * dv + col) =
-                    *reinterpret_cast<const uint4 *>(sm.S16 + row * DV + col);
+                    *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
             }
         } else {
-            load_rows(sm.Qt, q, t0, nv, H, h, DK, 0, DK);
+            load_rows(sm.Qt, LK, q, t0, nv, H, h, DK, 0, DK);
         }
-        load_rows(sm.Kt, k, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.V, v, t0, nv, H, h, dv, j0, DV);
+        load_rows(sm.Kt, LK, k, t0, nv, H, h, DK, 0, DK);
+        load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, DV);
         __syncthreads();
         channel_pass<DK>(a, t0, nv, H, h, b, mode, STATES ? nullptr : sm.Qt, sm.Kt, sm.Kh, nullptr, sm.g);
         __syncthreads();
@@ -191,8 +203,8 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                     wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
-                    wmma::load_matrix_sync(fa, sm.Qt + 16 * kk, DK);
-                    wmma::load_matrix_sync(fb, sm.Kt + 16 * kk, DK);   // B[kk][s] = Kt[s][kk]
+                    wmma::load_matrix_sync(fa, sm.Qt + 16 * kk, LK);
+                    wmma::load_matrix_sync(fb, sm.Kt + 16 * kk, LK);   // B[kk][s] = Kt[s][kk]
                     wmma::mma_sync(acc, fa, fb, acc);
                 }
                 wmma::store_matrix_sync(sm.A, acc, kT, wmma::mem_row_major);
@@ -211,16 +223,16 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                     wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-                    wmma::load_matrix_sync(fa, sm.Qt + 16 * kk, DK);
-                    wmma::load_matrix_sync(fb, sm.S16 + 16 * kk * DV + 16 * ni, DV);
+                    wmma::load_matrix_sync(fa, sm.Qt + 16 * kk, LK);
+                    wmma::load_matrix_sync(fb, sm.S16 + 16 * kk * LV + 16 * ni, LV);
                     wmma::mma_sync(acc, fa, fb, acc);
                 }
                 wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fp;
                 wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fv;
                 wmma::load_matrix_sync(fp, sm.P, kT);
-                wmma::load_matrix_sync(fv, sm.V + 16 * ni, DV);
+                wmma::load_matrix_sync(fv, sm.V + 16 * ni, LV);
                 wmma::mma_sync(acc, fp, fv, acc);
-                wmma::store_matrix_sync(sm.O + 16 * ni, acc, DV, wmma::mem_row_major);
+                wmma::store_matrix_sync(sm.O + 16 * ni, acc, LF, wmma::mem_row_major);
             }
             __syncthreads();
             // rows t < nv of o
@@ -228,7 +240,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 const int t = e / (DV / 8), col = (e % (DV / 8)) * 8;
                 if (t >= nv)
                     continue;
-                const float *src = sm.O + t * DV + col;
+                const float *src = sm.O + t * LF + col;
                 const size_t off = ((size_t)(t0 + t) * H + h) * dv + j0 + col;
                 if (o_f32) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(o) + off);
@@ -248,25 +260,25 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     }
     if (hT != nullptr)
         for (int e = tid; e < DK * DV; e += kVecThreads)
-            hT[unit * sstride + (size_t)(e / DV) * dv + j0 + e % DV] = sm.S32[e];
+            hT[unit * sstride + (size_t)(e / DV) * dv + j0 + e % DV] = sm.S32[(e / DV) * LF + e % DV];
 }
 
 template <int DK, int DV>
 struct VecBwdSmem {
-    float D32[DK * DV];
-    __nv_bfloat16 D16[DK * DV];
-    __nv_bfloat16 S16[DK * DV];   // state before the tile
-    __nv_bfloat16 Qr[kT * DK], Kr[kT * DK];   // raw q, k
-    __nv_bfloat16 Qt[kT * DK], Kt[kT * DK], Kh[kT * DK];
-    __nv_bfloat16 V[kT * DV], dO[kT * DV];
+    float D32[DK * padf(DV)];
+    __nv_bfloat16 D16[DK * padb(DV)];
+    __nv_bfloat16 S16[DK * padb(DV)];   // state before the tile
+    __nv_bfloat16 Qr[kT * padb(DK)], Kr[kT * padb(DK)];   // raw q, k
+    __nv_bfloat16 Qt[kT * padb(DK)], Kt[kT * padb(DK)], Kh[kT * padb(DK)];
+    __nv_bfloat16 V[kT * padb(DV)], dO[kT * padb(DV)];
     __nv_bfloat16 P[kT * kT], dP[kT * kT];
     float A[kT * kT], dA[kT * kT];
     float Gm[kT * DK];     // tile-local Gamma
-    float X1[kT * DK];     // dO S_in^T (inter dq, unscaled)
-    float X2[kT * DK];     // dP^T Qt (intra dk, unscaled), then the pair terms X
-    float X3[kT * DK];     // V D^T (inter dk, unscaled), then the terms Y
-    float X4[kT * DK];     // dP Kt (intra dq, unscaled)
-    float Y[kT * DV];      // dv
+    float X1[kT * padf(DK)];   // dO S_in^T (inter dq, unscaled)
+    float X2[kT * padf(DK)];   // dP^T Qt (intra dk, unscaled), then the pair terms X
+    float X3[kT * padf(DK)];   // V D^T (inter dk, unscaled), then the terms Y
+    float X4[kT * padf(DK)];   // dP Kt (intra dq, unscaled)
+    float Y[kT * padf(DV)];    // dv
     float g[DK], gam[DK], cst[DK];
 };
 static_assert(sizeof(VecBwdSmem<128, 128>) <= 227 * 1024, "per-channel backward tile exceeds shared memory");
@@ -286,6 +298,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     VecBwdSmem<DK, DV> &sm = *reinterpret_cast<VecBwdSmem<DK, DV> *>(smem_raw);
+    constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV), LX = padf(DK);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, n = blockIdx.y;
     const DocSpan d = doc_span(cu, n, T);
@@ -297,9 +310,10 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     const int64_t unit = (int64_t)n * H + h;
     const size_t sstride = (size_t)DK * DV;
     for (int e = tid; e < DK * DV; e += kVecThreads) {
+        const int i = e / DV, j = e % DV;
         const float x = dhT != nullptr ? dhT[unit * sstride + e] : 0.0f;
-        sm.D32[e] = x;
-        sm.D16[e] = __float2bfloat16_rn(x);
+        sm.D32[i * LF + j] = x;
+        sm.D16[i * LV + j] = __float2bfloat16_rn(x);
     }
     const int ntile = (int)((d.len + kT - 1) / kT);
     for (int c = ntile - 1; c >= 0; --c) {
@@ -308,17 +322,21 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         // ---- loads
         {
             const __nv_bfloat16 *src = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride;
-            for (int e = tid; e < DK * DV / 8; e += kVecThreads)
-                reinterpret_cast<uint4 *>(sm.S16)[e] = reinterpret_cast<const uint4 *>(src)[e];
+            for (int e = tid; e < DK * DV / 8; e += kVecThreads) {
+                const int row = e / (DV / 8), c8 = (e % (DV / 8)) * 8;
+                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) =
+                    *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            }
         }
-        load_rows(sm.Qr, q, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.Kr, k, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.V, v, t0, nv, H, h, DV, 0, DV);
-        load_rows(sm.dO, dO, t0, nv, H, h, DV, 0, DV);
+        load_rows(sm.Qr, LK, q, t0, nv, H, h, DK, 0, DK);
+        load_rows(sm.Kr, LK, k, t0, nv, H, h, DK, 0, DK);
+        load_rows(sm.V, LV, v, t0, nv, H, h, DV, 0, DV);
+        load_rows(sm.dO, LV, dO, t0, nv, H, h, DV, 0, DV);
         __syncthreads();
         for (int e = tid; e < kT * DK; e += kVecThreads) {
-            sm.Qt[e] = sm.Qr[e];
-            sm.Kt[e] = sm.Kr[e];
+            const int x = (e / DK) * LK + e % DK;
+            sm.Qt[x] = sm.Qr[x];
+            sm.Kt[x] = sm.Kr[x];
         }
         __syncthreads();
         channel_pass<DK>(a, t0, nv, H, h, b, mode, sm.Qt, sm.Kt, sm.Kh, sm.Gm, sm.g);
@@ -332,11 +350,12 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             const __nv_bfloat16 *xa = warp == 0 ? sm.Qt : sm.dO;
             const __nv_bfloat16 *xb = warp == 0 ? sm.Kt : sm.V;
             const int kd = warp == 0 ? DK : DV;
+            const int ld = warp == 0 ? LK : LV;
             for (int kk = 0; kk < kd / 16; ++kk) {
                 wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                 wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
-                wmma::load_matrix_sync(fa, xa + 16 * kk, kd);
-                wmma::load_matrix_sync(fb, xb + 16 * kk, kd);
+                wmma::load_matrix_sync(fa, xa + 16 * kk, ld);
+                wmma::load_matrix_sync(fb, xb + 16 * kk, ld);
                 wmma::mma_sync(acc, fa, fb, acc);
             }
             wmma::store_matrix_sync(warp == 0 ? sm.A : sm.dA, acc, kT, wmma::mem_row_major);
@@ -357,34 +376,34 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 for (int kk = 0; kk < DV / 16; ++kk) {
                     wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                     wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
-                    wmma::load_matrix_sync(fa, sm.dO + 16 * kk, DV);
-                    wmma::load_matrix_sync(fb, sm.S16 + 16 * ni * DV + 16 * kk, DV);   // B[j][i] = S[i][j]
+                    wmma::load_matrix_sync(fa, sm.dO + 16 * kk, LV);
+                    wmma::load_matrix_sync(fb, sm.S16 + 16 * ni * LV + 16 * kk, LV);   // B[j][i] = S[i][j]
                     wmma::mma_sync(acc, fa, fb, acc);
                 }
-                wmma::store_matrix_sync(sm.X1 + 16 * ni, acc, DK, wmma::mem_row_major);
+                wmma::store_matrix_sync(sm.X1 + 16 * ni, acc, LX, wmma::mem_row_major);
             } else if (kind == 3) {
                 wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fp;
                 wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fk;
                 wmma::load_matrix_sync(fp, sm.dP, kT);
-                wmma::load_matrix_sync(fk, sm.Kt + 16 * ni, DK);
+                wmma::load_matrix_sync(fk, sm.Kt + 16 * ni, LK);
                 wmma::mma_sync(acc, fp, fk, acc);
-                wmma::store_matrix_sync(sm.X4 + 16 * ni, acc, DK, wmma::mem_row_major);
+                wmma::store_matrix_sync(sm.X4 + 16 * ni, acc, LX, wmma::mem_row_major);
             } else if (kind == 1) {
                 wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fp;
                 wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fq;
                 wmma::load_matrix_sync(fp, sm.dP, kT);   // A[s][t] = dP[t][s]
-                wmma::load_matrix_sync(fq, sm.Qt + 16 * ni, DK);
+                wmma::load_matrix_sync(fq, sm.Qt + 16 * ni, LK);
                 wmma::mma_sync(acc, fp, fq, acc);
-                wmma::store_matrix_sync(sm.X2 + 16 * ni, acc, DK, wmma::mem_row_major);
+                wmma::store_matrix_sync(sm.X2 + 16 * ni, acc, LX, wmma::mem_row_major);
             } else {   // kind 2
                 for (int kk = 0; kk < DV / 16; ++kk) {
                     wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                     wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
-                    wmma::load_matrix_sync(fa, sm.V + 16 * kk, DV);
-                    wmma::load_matrix_sync(fb, sm.D16 + 16 * ni * DV + 16 * kk, DV);   // B[j][i] = D[i][j]
+                    wmma::load_matrix_sync(fa, sm.V + 16 * kk, LV);
+                    wmma::load_matrix_sync(fb, sm.D16 + 16 * ni * LV + 16 * kk, LV);   // B[j][i] = D[i][j]
                     wmma::mma_sync(acc, fa, fb, acc);
                 }
-                wmma::store_matrix_sync(sm.X3 + 16 * ni, acc, DK, wmma::mem_row_major);
+                wmma::store_matrix_sync(sm.X3 + 16 * ni, acc, LX, wmma::mem_row_major);
             }
         }
         // ---- dv = P^T dO + Kh D  (N = DV panels)
@@ -394,30 +413,31 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fp;
             wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fo;
             wmma::load_matrix_sync(fp, sm.P, kT);   // A[s][t] = P[t][s]
-            wmma::load_matrix_sync(fo, sm.dO + 16 * ni, DV);
+            wmma::load_matrix_sync(fo, sm.dO + 16 * ni, LV);
             wmma::mma_sync(acc, fp, fo, acc);
             for (int kk = 0; kk < DK / 16; ++kk) {
                 wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
                 wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-                wmma::load_matrix_sync(fa, sm.Kh + 16 * kk, DK);
-                wmma::load_matrix_sync(fb, sm.D16 + 16 * kk * DV + 16 * ni, DV);
+                wmma::load_matrix_sync(fa, sm.Kh + 16 * kk, LK);
+                wmma::load_matrix_sync(fb, sm.D16 + 16 * kk * LV + 16 * ni, LV);
                 wmma::mma_sync(acc, fa, fb, acc);
             }
-            wmma::store_matrix_sync(sm.Y + 16 * ni, acc, DV, wmma::mem_row_major);
+            wmma::store_matrix_sync(sm.Y + 16 * ni, acc, LF, wmma::mem_row_major);
         }
         __syncthreads();
         // ---- gradients of q, k, v (rows t < nv); the pair terms X (into X2) and Y (into X3)
         for (int e = tid; e < kT * DK; e += kVecThreads) {
             const int t = e / DK, i = e % DK;
+            const int x = t * LX + i, xb = t * LK + i;   // fp32 / bf16 rows
             const float G = sm.Gm[e];
             const float eG = expf(G);
-            const float qinter = eG * sm.X1[e];
-            const float dqv = qinter + eG * sm.X4[e];
-            const float kinter = expf(sm.gam[i] - G) * sm.X3[e];
-            const float dkv = expf(-G) * sm.X2[e] + kinter;
-            const float kr = __bfloat162float(sm.Kr[e]);
-            sm.X2[e] = __bfloat162float(sm.Kt[e]) * sm.X2[e] - __bfloat162float(sm.Qt[e]) * sm.X4[e] + kr * kinter;
-            sm.X3[e] = __bfloat162float(sm.Qr[e]) * qinter;
+            const float qinter = eG * sm.X1[x];
+            const float dqv = qinter + eG * sm.X4[x];
+            const float kinter = expf(sm.gam[i] - G) * sm.X3[x];
+            const float dkv = expf(-G) * sm.X2[x] + kinter;
+            const float kr = __bfloat162float(sm.Kr[xb]);
+            sm.X2[x] = __bfloat162float(sm.Kt[xb]) * sm.X2[x] - __bfloat162float(sm.Qt[xb]) * sm.X4[x] + kr * kinter;
+            sm.X3[x] = __bfloat162float(sm.Qr[xb]) * qinter;
             if (t < nv) {
                 const size_t off = ((size_t)(t0 + t) * H + h) * DK + i;
                 dq[off] = dqv;
@@ -427,13 +447,13 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         for (int e = tid; e < kT * DV; e += kVecThreads) {
             const int t = e / DV, j = e % DV;
             if (t < nv)
-                dv[((size_t)(t0 + t) * H + h) * DV + j] = sm.Y[e];
+                dv[((size_t)(t0 + t) * H + h) * DV + j] = sm.Y[t * LF + j];
         }
         // pairs across the whole tile: e^{gamma_i} <S_in[i,:], D[i,:]>; one warp per row group
         for (int i = warp; i < DK; i += kVecThreads / 32) {
             float acc = 0.0f;
             for (int j = lane; j < DV; j += 32)
-                acc = fmaf(__bfloat162float(sm.S16[i * DV + j]), sm.D32[i * DV + j], acc);
+                acc = fmaf(__bfloat162float(sm.S16[i * LV + j]), sm.D32[i * LF + j], acc);
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1)
                 acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -447,41 +467,43 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             float ytot = 0.0f;
 #pragma unroll
             for (int t = 0; t < kT; ++t)
-                ytot += sm.X3[t * DK + i];
+                ytot += sm.X3[t * LX + i];
             float xb = 0.0f, yb = 0.0f;   // sums over the tokens before t
             for (int t = 0; t < kT; ++t) {
                 if (t < nv) {
                     const size_t off = ((size_t)(t0 + t) * H + h) * DK + i;
                     da[off] = (xb + (ytot - yb) + sm.cst[i]) * log_decay_deriv(a[off], b, mode);
                 }
-                xb += sm.X2[t * DK + i];
-                yb += sm.X3[t * DK + i];
+                xb += sm.X2[t * LX + i];
+                yb += sm.X3[t * LX + i];
             }
         }
         __syncthreads();
-        // ---- adjoint: D <- diag(g) D + Qt^T dO
-        for (int e = tid; e < DK * DV; e += kVecThreads)
-            sm.D32[e] *= sm.g[e / DV];
-        __syncthreads();
+        // ---- adjoint: D <- diag(g) D + Qt^T dO, tile by tile (each warp owns its tiles)
         for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecThreads / 32) {
             const int mi = tile / (DV / 16), ni = tile % (DV / 16);
+            for (int e = lane; e < 256; e += 32)
+                sm.D32[(16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15)] *= sm.g[16 * mi + (e >> 4)];
+            __syncwarp();
             wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
             wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
             wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-            wmma::load_matrix_sync(acc, sm.D32 + 16 * mi * DV + 16 * ni, DV, wmma::mem_row_major);
-            wmma::load_matrix_sync(fa, sm.Qt + 16 * mi, DK);   // A[i][t] = Qt[t][16 mi + i]
-            wmma::load_matrix_sync(fb, sm.dO + 16 * ni, DV);
+            wmma::load_matrix_sync(acc, sm.D32 + 16 * mi * LF + 16 * ni, LF, wmma::mem_row_major);
+            wmma::load_matrix_sync(fa, sm.Qt + 16 * mi, LK);   // A[i][t] = Qt[t][16 mi + i]
+            wmma::load_matrix_sync(fb, sm.dO + 16 * ni, LV);
             wmma::mma_sync(acc, fa, fb, acc);
-            wmma::store_matrix_sync(sm.D32 + 16 * mi * DV + 16 * ni, acc, DV, wmma::mem_row_major);
+            wmma::store_matrix_sync(sm.D32 + 16 * mi * LF + 16 * ni, acc, LF, wmma::mem_row_major);
+            __syncwarp();
+            for (int e = lane; e < 256; e += 32) {
+                const int r = 16 * mi + (e >> 4), c2 = 16 * ni + (e & 15);
+                sm.D16[r * LV + c2] = __float2bfloat16_rn(sm.D32[r * LF + c2]);
+            }
         }
-        __syncthreads();
-        for (int e = tid; e < DK * DV; e += kVecThreads)
-            sm.D16[e] = __float2bfloat16_rn(sm.D32[e]);
         __syncthreads();
     }
     if (dh0 != nullptr)
         for (int e = tid; e < DK * DV; e += kVecThreads)
-            dh0[unit * sstride + e] = sm.D32[e];
+            dh0[unit * sstride + e] = sm.D32[(e / DV) * LF + e % DV];
 }
 
 template <typename K>
