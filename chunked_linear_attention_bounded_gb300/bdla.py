@@ -37,7 +37,7 @@ EXPORTS = ("bdla_workspace_bytes", "bdla_decay", "bdla_fwd", "bdla_fwd_varlen", 
            "bdla_set_kernel_events", "bdla_fwd_noalloc", "bdla_noalloc_read_status",
            "bdla_set_seq_split", "bdla_decode", "bdla_set_wait_limit_ns", "bdla_set_test_stall",
            "bdla_workspace_bytes_vec", "bdla_fwd_vec", "bdla_bwd_vec", "bdla_workspace_bytes_delta",
-           "bdla_fwd_delta", "bdla_bwd_delta")
+           "bdla_fwd_delta", "bdla_bwd_delta", "bdla_tile_states_bytes")
 KERNEL_DECAY, KERNEL_FWD, KERNEL_BWD, KERNEL_STATES, KERNEL_SEG = 0, 1, 2, 3, 4
 STALL_NONE, STALL_PRODUCER, STALL_MMA, STALL_EPILOGUE = 0, 1, 2, 3
 
@@ -98,17 +98,20 @@ def lib():
         L.bdla_set_test_stall.restype = ci
         L.bdla_workspace_bytes_vec.argtypes = [ci, Dims, ci]
         L.bdla_workspace_bytes_vec.restype = sz
-        L.bdla_fwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, Dims, ci, vp, sz, vp]
+        L.bdla_fwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, vp, Dims, ci, vp, sz, vp]
         L.bdla_fwd_vec.restype = ci
-        L.bdla_bwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, Dims,
+        L.bdla_bwd_vec.argtypes = [vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, Dims,
                                    ci, vp, sz, vp]
         L.bdla_bwd_vec.restype = ci
         L.bdla_workspace_bytes_delta.argtypes = [ci, Dims, ci]
         L.bdla_workspace_bytes_delta.restype = sz
-        L.bdla_fwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, Dims, ci, vp, sz, vp]
+        L.bdla_fwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, ci, vp, vp, Dims, ci, vp, sz,
+                                     vp]
         L.bdla_fwd_delta.restype = ci
-        L.bdla_bwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+        L.bdla_bwd_delta.argtypes = [vp, vp, vp, vp, vp, f32, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      Dims, ci, vp, sz, vp]
+        L.bdla_tile_states_bytes.argtypes = [Dims, ci]
+        L.bdla_tile_states_bytes.restype = sz
         L.bdla_bwd_delta.restype = ci
         del i32
         _lib = L
@@ -417,16 +420,30 @@ def _ws_vec(op, q, v, n_docs, ws):
     return ws.ensure(need)
 
 
+def tile_states(q, v, cu_seqlens=None):
+    """An uninitialised bf16 buffer for the state before every 16-token tile
+    ([H, slots, dk, dv]), the `states` hand-off of the per-channel and
+    delta-rule paths."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n_docs = cu_seqlens.numel() - 1 if cu_seqlens is not None else 0
+    nbytes = int(lib().bdla_tile_states_bytes(Dims(B, T, H, dk, dv), n_docs))
+    if nbytes == 0:
+        raise BdlaError(ERR_UNSUPPORTED, "bdla_tile_states_bytes")
+    return torch.empty((H, nbytes // (2 * H * dk * dv), dk, dv), dtype=torch.bfloat16, device=q.device)
+
+
 def fwd_vec(q, k, v, a, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUNDED,
-            o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, stream=None):
+            o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, states_out=None, stream=None):
     """Forward pass with one log-decay per key channel (a [B, T, H, dk]).
-    Returns (o, hT)."""
+    Returns (o, hT); with `states_out` (from tile_states) it also writes the
+    state before every tile there, for bwd_vec."""
     B, T, H, dk, dv, n_docs, n_seq = _vec_checks(q, k, v, a, cu_seqlens, h0)
     o = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
     hT = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
     ws = _ws_vec(OP_FWD, q, v, n_docs, ws)
     st = lib().bdla_fwd_vec(_p(q), _p(k), _p(v), _p(a), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0), _p(o),
-                            _dtype_code(o.dtype), _p(hT), _dims(q, v), mode, ws.ptr, ws.nbytes,
+                            _dtype_code(o.dtype), _p(hT), _p(states_out), _dims(q, v), mode, ws.ptr, ws.nbytes,
                             _stream_handle(stream))
     if st:
         raise BdlaError(st, "bdla_fwd_vec")
@@ -434,7 +451,7 @@ def fwd_vec(q, k, v, a, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = B
 
 
 def bwd_vec(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, mode: int = BOUNDED,
-            want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, stream=None):
+            want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, states=None, stream=None):
     """Backward pass with one log-decay per key channel.  Returns
     (dq, dk, dv, da, dh0) with da [B, T, H, dk]; dh0 is None unless asked for."""
     B, T, H, dk, dv, n_docs, n_seq = _vec_checks(q, k, v, a, cu_seqlens, h0)
@@ -453,8 +470,8 @@ def bwd_vec(q, k, v, a, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None,
     dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     ws = _ws_vec(OP_BWD, q, v, n_docs, ws)
     st = lib().bdla_bwd_vec(_p(q), _p(k), _p(v), _p(a), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0), _p(dO),
-                            _p(dhT), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dh0), _dims(q, v), mode, ws.ptr,
-                            ws.nbytes, _stream_handle(stream))
+                            _p(dhT), _p(states), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dh0), _dims(q, v), mode,
+                            ws.ptr, ws.nbytes, _stream_handle(stream))
     if st:
         raise BdlaError(st, "bdla_bwd_vec")
     return dq, dk_, dv_, da, dh0
@@ -494,22 +511,25 @@ def _ws_delta(op, q, v, n_docs, ws):
 
 
 def fwd_delta(q, k, v, a, beta, b: float = -5.0, h0=None, cu_seqlens=None, mode: int = BOUNDED,
-              o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, out=None, hT_out=None, stream=None):
-    """Gated delta rule forward (a, beta [B, T, H]).  Returns (o, hT)."""
+              o_dtype=torch.bfloat16, ws: Optional[Workspace] = None, out=None, hT_out=None, states_out=None,
+              stream=None):
+    """Gated delta rule forward (a, beta [B, T, H]).  Returns (o, hT); with
+    `states_out` (from tile_states) it also writes the state before every
+    tile there, for bwd_delta."""
     B, T, H, dk, dv, n_docs, n_seq = _delta_checks(q, k, v, a, beta, cu_seqlens, h0)
     o = out if out is not None else torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
     hT = hT_out if hT_out is not None else torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=q.device)
     ws = _ws_delta(OP_FWD, q, v, n_docs, ws)
     st = lib().bdla_fwd_delta(_p(q), _p(k), _p(v), _p(a), _p(beta), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0),
-                              _p(o), _dtype_code(o.dtype), _p(hT), _dims(q, v), mode, ws.ptr, ws.nbytes,
-                              _stream_handle(stream))
+                              _p(o), _dtype_code(o.dtype), _p(hT), _p(states_out), _dims(q, v), mode, ws.ptr,
+                              ws.nbytes, _stream_handle(stream))
     if st:
         raise BdlaError(st, "bdla_fwd_delta")
     return o, hT
 
 
 def bwd_delta(q, k, v, a, beta, dO, b: float = -5.0, h0=None, dhT=None, cu_seqlens=None, mode: int = BOUNDED,
-              want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, stream=None):
+              want_dh0: bool = False, ws: Optional[Workspace] = None, outs=None, states=None, stream=None):
     """Gated delta rule backward.  Returns (dq, dk, dv, da, dbeta, dh0);
     dh0 is None unless asked for."""
     B, T, H, dk, dv, n_docs, n_seq = _delta_checks(q, k, v, a, beta, cu_seqlens, h0)
@@ -529,8 +549,8 @@ def bwd_delta(q, k, v, a, beta, dO, b: float = -5.0, h0=None, dhT=None, cu_seqle
     dh0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     ws = _ws_delta(OP_BWD, q, v, n_docs, ws)
     st = lib().bdla_bwd_delta(_p(q), _p(k), _p(v), _p(a), _p(beta), b, CHUNK, _p(cu_seqlens), n_docs, _p(h0),
-                              _p(dO), _p(dhT), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dbeta), _p(dh0), _dims(q, v),
-                              mode, ws.ptr, ws.nbytes, _stream_handle(stream))
+                              _p(dO), _p(dhT), _p(states), _p(dq), _p(dk_), _p(dv_), _p(da), _p(dbeta), _p(dh0),
+                              _dims(q, v), mode, ws.ptr, ws.nbytes, _stream_handle(stream))
     if st:
         raise BdlaError(st, "bdla_bwd_delta")
     return dq, dk_, dv_, da, dbeta, dh0

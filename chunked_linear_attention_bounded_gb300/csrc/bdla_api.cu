@@ -489,6 +489,17 @@ size_t vec_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off)
 
 }  // namespace
 
+size_t bdla_tile_states_bytes(bdla_dims d, int n_docs)
+{
+    const bool varlen = n_docs > 0;
+    if (check_vec(d, varlen ? reinterpret_cast<const int32_t *>(1) : nullptr, n_docs) != BDLA_OK)
+        return 0;
+    Problem p{};
+    p.tokens = total_tokens(d);
+    p.n_docs = varlen ? n_docs : d.B;
+    return (size_t)d.H * vec_state_slots(p) * d.dk * d.dv * 2;
+}
+
 size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs)
 {
     const bool varlen = n_docs > 0;
@@ -500,7 +511,7 @@ size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs)
 
 bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const float *a, float b, int chunk,
                          const int32_t *cu_seqlens, int n_docs, const float *h0, void *o,
-                         bdla_dtype o_dtype, float *hT, bdla_dims d, bdla_decay_mode mode, void *ws,
+                         bdla_dtype o_dtype, float *hT, void *states, bdla_dims d, bdla_decay_mode mode, void *ws,
                          size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
@@ -508,7 +519,7 @@ bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const floa
     if (total_tokens(d) > 0 && (!q || !k || !v || !a || !o))
         return BDLA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
-        !aligned16(hT) || !aligned16(a))
+        !aligned16(hT) || !aligned16(a) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
         return BDLA_ERR_DTYPE;
@@ -517,14 +528,15 @@ bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const floa
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
     KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
     BDLA_CUDA(launch_vec_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-                             static_cast<const __nv_bfloat16 *>(v), a, h0, o, o_dtype == BDLA_F32, hT, nullptr));
+                             static_cast<const __nv_bfloat16 *>(v), a, h0, o, o_dtype == BDLA_F32, hT,
+                             static_cast<__nv_bfloat16 *>(states)));
     return BDLA_OK;
 }
 
 bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const float *a, float b, int chunk,
                          const int32_t *cu_seqlens, int n_docs, const float *h0, const void *dO,
-                         const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
-                         bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
+                         const float *dhT, const void *states, float *dq, float *dk, float *dv, float *da,
+                         float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
     BDLA_TRY(check_decay(b, chunk, mode));
@@ -532,22 +544,24 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
         return BDLA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(a) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(da) || !aligned16(h0) ||
-        !aligned16(dhT) || !aligned16(dh0))
+        !aligned16(dhT) || !aligned16(dh0) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
-    auto *states = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
-    {
+    const __nv_bfloat16 *st = static_cast<const __nv_bfloat16 *>(states);
+    if (st == nullptr) {   // no states from the forward: a states pass into the workspace
+        auto *wst = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
         KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_vec_fwd(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, states));
+        BDLA_CUDA(launch_vec_fwd(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, wst));
+        st = wst;
     }
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
-        BDLA_CUDA(launch_vec_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, states, dhT, dq,
+        BDLA_CUDA(launch_vec_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, st, dhT, dq,
                                  dk, dv, da, dh0));
     }
     return BDLA_OK;
@@ -582,7 +596,7 @@ size_t bdla_workspace_bytes_delta(int op, bdla_dims d, int n_docs)
 
 bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const float *a, const float *beta,
                            float b, int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0, void *o,
-                           bdla_dtype o_dtype, float *hT, bdla_dims d, bdla_decay_mode mode, void *ws,
+                           bdla_dtype o_dtype, float *hT, void *states, bdla_dims d, bdla_decay_mode mode, void *ws,
                            size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
@@ -590,7 +604,7 @@ bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const fl
     if (total_tokens(d) > 0 && (!q || !k || !v || !a || !beta || !o))
         return BDLA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) ||
-        !aligned16(hT) || !aligned16(a) || !aligned16(beta))
+        !aligned16(hT) || !aligned16(a) || !aligned16(beta) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
         return BDLA_ERR_DTYPE;
@@ -600,14 +614,14 @@ bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const fl
     KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
     BDLA_CUDA(launch_delta_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
                                static_cast<const __nv_bfloat16 *>(v), a, beta, h0, o, o_dtype == BDLA_F32, hT,
-                               nullptr));
+                               static_cast<__nv_bfloat16 *>(states)));
     return BDLA_OK;
 }
 
 bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const float *a, const float *beta,
                            float b, int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
-                           const void *dO, const float *dhT, float *dq, float *dk, float *dv, float *da,
-                           float *dbeta, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
+                           const void *dO, const float *dhT, const void *states, float *dq, float *dk, float *dv,
+                           float *da, float *dbeta, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
                            size_t ws_bytes, void *stream)
 {
     BDLA_TRY(check_vec(d, cu_seqlens, n_docs));
@@ -616,22 +630,24 @@ bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const fl
         return BDLA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(a) ||
         !aligned16(beta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(da) ||
-        !aligned16(dbeta) || !aligned16(h0) || !aligned16(dhT) || !aligned16(dh0))
+        !aligned16(dbeta) || !aligned16(h0) || !aligned16(dhT) || !aligned16(dh0) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
-    auto *states = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
-    {
+    const __nv_bfloat16 *st = static_cast<const __nv_bfloat16 *>(states);
+    if (st == nullptr) {   // no states from the forward: a states pass into the workspace
+        auto *wst = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
         KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_delta_fwd(p, qb, kb, vb, a, beta, h0, nullptr, 0, nullptr, states));
+        BDLA_CUDA(launch_delta_fwd(p, qb, kb, vb, a, beta, h0, nullptr, 0, nullptr, wst));
+        st = wst;
     }
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
-        BDLA_CUDA(launch_delta_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, beta, states, dhT,
+        BDLA_CUDA(launch_delta_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, beta, st, dhT,
                                    dq, dk, dv, da, dbeta, dh0));
     }
     return BDLA_OK;

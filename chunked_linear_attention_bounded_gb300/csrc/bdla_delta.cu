@@ -106,8 +106,9 @@ __device__ __forceinline__ void times_state(float *C, const __nv_bfloat16 *A, co
 }
 
 // One CTA per (64-column value slice, head, document), tiles in order.
-// STATES: no q and no output; the bf16 state before every tile goes to
-// `states` ([H][slots][DK][dv], slot = floor(doc_start / 16) + n + tile).
+// With `states` given the bf16 state before every tile goes there
+// ([H][slots][DK][dv], slot = floor(doc_start / 16) + n + tile); STATES: no q
+// and no output (the backward's own states pass).
 template <int DK, bool STATES>
 __global__ void __launch_bounds__(kDT)
 delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -142,16 +143,16 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         const int64_t t0 = d.start + (int64_t)c * kT;
         const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
         // ---- the tile's inputs, the decay cumsum and the write strengths
-        if (STATES) {
+        if (states != nullptr) {   // the state before this tile
             __nv_bfloat16 *dst = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride + j0;
             for (int e = tid; e < DK * kDvs / 8; e += kDT) {
                 const int row = e / (kDvs / 8), col = (e % (kDvs / 8)) * 8;
                 *reinterpret_cast<uint4 *>(dst + (size_t)row * dv + col) =
                     *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
             }
-        } else {
-            load_rows(sm.Q, LK, q, t0, nv, H, h, DK, 0, DK);
         }
+        if (!STATES)
+            load_rows(sm.Q, LK, q, t0, nv, H, h, DK, 0, DK);
         load_rows(sm.K, LK, k, t0, nv, H, h, DK, 0, DK);
         load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, kDvs);
         if (warp == 0) {
@@ -778,7 +779,7 @@ cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __n
                                                                  p.tokens, p.H, p.dv, h0, o, o_f32, hT,     \
                                                                  states, slots, p.st);                      \
     } while (0)
-    const bool st = states != nullptr;
+    const bool st = o == nullptr;   // states pass only
     if (p.dk == 64) {
         if (st)
             BDLA_DELTA_FWD(64, true);

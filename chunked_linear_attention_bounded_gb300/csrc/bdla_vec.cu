@@ -144,9 +144,10 @@ struct VecFwdSmem {
     float g[DK];
 };
 
-// One CTA per (dv slice of DV columns, head, document).  STATES: no q, no
-// output; instead the bf16 state before every tile goes to `states`
-// ([H][slots][DK][dv], slot = floor(doc_start / 16) + n + tile).
+// One CTA per (dv slice of DV columns, head, document).  With `states` given
+// the bf16 state before every tile goes there ([H][slots][DK][dv], slot =
+// floor(doc_start / 16) + n + tile); STATES: no q and no output (the
+// backward's own states pass).
 template <int DK, int DV, bool STATES>
 __global__ void __launch_bounds__(kVecThreads)
 vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -179,17 +180,16 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     for (int c = 0; c < ntile; ++c) {
         const int64_t t0 = d.start + (int64_t)c * kT;
         const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
-        if (STATES) {
-            // the state before this tile
+        if (states != nullptr) {   // the state before this tile
             __nv_bfloat16 *dst = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride + j0;
             for (int e = tid; e < DK * DV / 8; e += kVecThreads) {
                 const int row = e / (DV / 8), col = (e % (DV / 8)) * 8;
                 *reinterpret_cast<uint4 *>(dst + (size_t)row * dv + col) =
                     *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
             }
-        } else {
-            load_rows(sm.Qt, LK, q, t0, nv, H, h, DK, 0, DK);
         }
+        if (!STATES)
+            load_rows(sm.Qt, LK, q, t0, nv, H, h, DK, 0, DK);
         load_rows(sm.Kt, LK, k, t0, nv, H, h, DK, 0, DK);
         load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, DV);
         __syncthreads();
@@ -535,7 +535,7 @@ cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
             q, k, v, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, p.dv, h0, o, o_f32, hT, states, slots, \
             p.st);                                                                                  \
     } while (0)
-    const bool st = states != nullptr;
+    const bool st = o == nullptr;   // states pass only
     if (p.dk == 64) {
         if (st)
             BDLA_VEC_FWD(64, true);

@@ -230,21 +230,29 @@ bdla_status bdla_noalloc_read_status(void *stream);
  *   a, da      fp32 [B, T, H, dk]   (one logit / gradient per key channel)
  *   cu_seqlens device int32 [n_docs + 1] for packed documents (B = 1), or
  *              NULL for fixed-length rows
- *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise); no
- *   checkpoints.  The backward's workspace holds the bf16 state before
- *   every 16-token tile (written by its own states pass):
- *   bdla_workspace_bytes_vec(BDLA_OP_BWD, ...) bytes, status word first.
+ *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise).
+ *   states     optional device bf16 [H][slots][dk][dv], slots = tokens / 16 +
+ *              n_docs (B for fixed-length rows) + 1, bdla_tile_states_bytes(d,
+ *              n_docs) bytes, caller-owned: the state before every 16-token
+ *              tile (tile c of document n in slot floor(doc_start / 16) + n + c).
+ *              The forward writes it when non-NULL; the backward reads it when
+ *              non-NULL (the forward's states of the same inputs), else runs
+ *              its own states pass into the workspace.
+ * Workspace: bdla_workspace_bytes_vec(op, ...) bytes, status word first; for
+ * BDLA_OP_BWD it includes room for the backward's own states pass (unused
+ * when the caller passes states).
  */
+size_t bdla_tile_states_bytes(bdla_dims d, int n_docs);
 size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs);
 bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const float *a, float b,
                          int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
-                         void *o, bdla_dtype o_dtype, float *hT, bdla_dims d,
+                         void *o, bdla_dtype o_dtype, float *hT, void *states, bdla_dims d,
                          bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
 bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const float *a, float b,
                          int chunk, const int32_t *cu_seqlens, int n_docs, const float *h0,
-                         const void *dO, const float *dhT, float *dq, float *dk, float *dv,
-                         float *da, float *dh0, bdla_dims d, bdla_decay_mode mode, void *ws,
-                         size_t ws_bytes, void *stream);
+                         const void *dO, const float *dhT, const void *states, float *dq,
+                         float *dk, float *dv, float *da, float *dh0, bdla_dims d,
+                         bdla_decay_mode mode, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Gated delta rule with the bounded log-decay: the "Delta Net-style"
@@ -260,21 +268,23 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
  *   beta, dbeta  fp32 [B, T, H]   write strengths beta_t (the caller maps its
  *                own logits into [0, 1]; keys are expected L2-normalised) and
  *                their gradient
- *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise).  The
- *   backward's workspace holds the bf16 state before every 16-token tile
- *   (its own states pass): bdla_workspace_bytes_delta(BDLA_OP_BWD, ...)
- *   bytes, status word first.
+ *   dk in {64, 128}, dv in {64, 128} (BDLA_ERR_UNSUPPORTED otherwise).
+ *   states       optional, as for bdla_fwd_vec / bdla_bwd_vec (same layout,
+ *                bdla_tile_states_bytes bytes).
+ * Workspace: bdla_workspace_bytes_delta(op, ...) bytes, status word first; for
+ * BDLA_OP_BWD it includes room for the backward's own states pass.
  */
 size_t bdla_workspace_bytes_delta(int op, bdla_dims d, int n_docs);
 bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const float *a,
                            const float *beta, float b, int chunk, const int32_t *cu_seqlens,
                            int n_docs, const float *h0, void *o, bdla_dtype o_dtype, float *hT,
-                           bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
-                           void *stream);
+                           void *states, bdla_dims d, bdla_decay_mode mode, void *ws,
+                           size_t ws_bytes, void *stream);
 bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const float *a,
                            const float *beta, float b, int chunk, const int32_t *cu_seqlens,
                            int n_docs, const float *h0, const void *dO, const float *dhT,
-                           float *dq, float *dk, float *dv, float *da, float *dbeta, float *dh0,
+                           const void *states, float *dq, float *dk, float *dv, float *da,
+                           float *dbeta, float *dh0,
                            bdla_dims d, bdla_decay_mode mode, void *ws, size_t ws_bytes,
                            void *stream);
 

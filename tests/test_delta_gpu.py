@@ -121,3 +121,23 @@ def test_delta_full_size_workload_sampled_heads():
     heads = [0, 21]
     gpu = _run(w, inp, with_grad=True)
     _compare(gpu, _oracle(inp, w.b, w.mode, heads=heads, with_grad=True), heads=heads)
+
+
+def test_delta_states_from_the_forward_equal_the_backwards_own():
+    """The forward's hand-off of the state before every tile (states_out)
+    gives bitwise the same gradients as the backward's own states pass."""
+    w = _delta_case("varlen64k", 900, H=2, n_docs=3, h0_std=0.2)
+    inp = make_inputs(w, with_grad=True)
+    g = to_device(inp)
+    st = bdla.tile_states(g["q"], g["v"], g["cu_seqlens"])
+    fo = bdla.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"], states_out=st)
+    fo_plain = bdla.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"])
+    own = bdla.bwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                     want_dh0=True)
+    handed = bdla.bwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                        want_dh0=True, states=st)
+    torch.cuda.synchronize()
+    for x, y in zip(fo, fo_plain):
+        assert torch.equal(x, y)
+    for x, y in zip(own, handed):
+        assert torch.equal(x, y)

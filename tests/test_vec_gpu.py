@@ -122,3 +122,23 @@ def test_vec_with_equal_channels_matches_the_scalar_path():
     torch.cuda.synchronize()
     assert_close("o", vo.cpu().numpy(), so.cpu().numpy())
     assert_close("hT", vhT.cpu().numpy(), shT.cpu().numpy())
+
+
+def test_vec_states_from_the_forward_equal_the_backwards_own():
+    """The forward's hand-off of the state before every tile (states_out)
+    gives bitwise the same gradients as the backward's own states pass."""
+    w = _vec_case("varlen64k", 900, H=2, n_docs=3, h0_std=0.2)
+    inp = make_inputs(w, with_grad=True)
+    g = to_device(inp)
+    st = bdla.tile_states(g["q"], g["v"], g["cu_seqlens"])
+    fo = bdla.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"], states_out=st)
+    fo_plain = bdla.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"])
+    own = bdla.bwd_vec(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                     want_dh0=True)
+    handed = bdla.bwd_vec(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                        want_dh0=True, states=st)
+    torch.cuda.synchronize()
+    for x, y in zip(fo, fo_plain):
+        assert torch.equal(x, y)
+    for x, y in zip(own, handed):
+        assert torch.equal(x, y)
