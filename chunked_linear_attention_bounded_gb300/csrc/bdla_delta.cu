@@ -37,7 +37,7 @@ namespace {
 using namespace nvcuda;
 
 constexpr int kT = kChunk;       // 16-token tile
-constexpr int kDT = 128;         // threads (4 warps)
+constexpr int kDT = 256;         // forward threads (8 warps)
 constexpr int kDvs = 64;         // value columns per forward CTA
 
 template <int DK>
@@ -177,7 +177,7 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         } else if (!STATES) {
             if (warp == 1)
                 gram16<DK, LK, LS>(sm.QK, sm.Q, sm.K);
-            for (int ni = warp - 2; ni < kDvs / 16; ni += 2)
+            for (int ni = warp - 2; ni < kDvs / 16; ni += kDT / 32 - 2)
                 if (ni >= 0)
                     times_state<DK, LK, LV, LF>(sm.QS, sm.Q, sm.S16, ni);
         }
@@ -225,12 +225,13 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         }
         __syncthreads();
         // ---- W S_0
-        times_state<DK, LK, LV, LF>(sm.WS, sm.Wb, sm.S16, warp);
+        for (int ni = warp; ni < kDvs / 16; ni += kDT / 32)
+            times_state<DK, LK, LV, LF>(sm.WS, sm.Wb, sm.S16, ni);
         __syncthreads();
         // ---- Delta = U - W S_0 and its state-update operand diag(e^{gamma - Gamma}) Delta
         const float gam = sm.G[kT - 1];
-        {
-            const int t = tid >> 3, c8 = (tid & 7) * 8;   // one row segment of 8 per thread
+        for (int e = tid; e < kT * (kDvs / 8); e += kDT) {
+            const int t = e >> 3, c8 = (e & 7) * 8;   // one row segment of 8 per item
             const float w = expf(gam - sm.G[t]);
             __align__(16) __nv_bfloat16 h8[8];
 #pragma unroll
@@ -243,8 +244,8 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         }
         __syncthreads();
         // ---- O = diag(e^{Gamma}) Q S_0 + P Delta (rows t < nv)
-        if (!STATES) {
-            const int t = tid >> 3, c8 = (tid & 7) * 8;
+        for (int e = tid; !STATES && e < kT * (kDvs / 8); e += kDT) {
+            const int t = e >> 3, c8 = (e & 7) * 8;
             float out[8];
             const float eg = sm.eG[t];
 #pragma unroll
@@ -323,7 +324,7 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 // terms through e^{Gamma_t}, prefix sums of the terms through w_t, and the
 // state term e^{gamma} <S_0, D>.  Products with the state or the adjoint are
 // bf16 warp MMAs; the 16-long contractions are fp32 on CUDA cores.
-constexpr int kBT = 256;   // backward threads (8 warps)
+constexpr int kBT = 512;   // backward threads (16 warps)
 
 template <int DK, int DV>
 struct DeltaBwdSmem {

@@ -45,7 +45,8 @@ namespace {
 using namespace nvcuda;
 
 constexpr int kT = kChunk;       // 16-token tile
-constexpr int kVecThreads = 128; // 4 warps
+constexpr int kVecFwdThreads = 256;   // forward: 8 warps
+constexpr int kVecBwdThreads = 512;   // backward: 16 warps (one CTA per SM)
 
 // Row strides in shared memory, padded by 16 bytes so that the 16 rows a
 // warp MMA fragment touches fall in different banks.
@@ -58,7 +59,7 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv
                                           int H, int h, int d, int c0, int w)
 {
     const int chunks = kT * w / 8;
-    for (int e = threadIdx.x; e < chunks; e += kVecThreads) {
+    for (int e = threadIdx.x; e < chunks; e += blockDim.x) {
         const int t = e / (w / 8), c = (e % (w / 8)) * 8;
         uint4 val = make_uint4(0, 0, 0, 0);
         if (t < nv)
@@ -109,7 +110,7 @@ __device__ __forceinline__ void state_update(float *S32, __nv_bfloat16 *S16, con
 {
     constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV);
     const int warp = threadIdx.x >> 5;
-    for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecThreads / 32) {
+    for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += (blockDim.x / 32)) {
         const int mi = tile / (DV / 16), ni = tile % (DV / 16);
         wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
         wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
@@ -149,7 +150,7 @@ struct VecFwdSmem {
 // floor(doc_start / 16) + n + tile); STATES: no q and no output (the
 // backward's own states pass).
 template <int DK, int DV, bool STATES>
-__global__ void __launch_bounds__(kVecThreads)
+__global__ void __launch_bounds__(kVecFwdThreads)
 vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a, float b, int mode,
                const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dv,
@@ -169,7 +170,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     }
     const int64_t unit = (int64_t)n * H + h;
     const size_t sstride = (size_t)DK * dv;
-    for (int e = tid; e < DK * DV; e += kVecThreads) {
+    for (int e = tid; e < DK * DV; e += kVecFwdThreads) {
         const int i = e / DV, j = e % DV;
         const float x = h0 != nullptr ? h0[unit * sstride + (size_t)i * dv + j0 + j] : 0.0f;
         sm.S32[i * LF + j] = x;
@@ -182,7 +183,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
         if (states != nullptr) {   // the state before this tile
             __nv_bfloat16 *dst = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride + j0;
-            for (int e = tid; e < DK * DV / 8; e += kVecThreads) {
+            for (int e = tid; e < DK * DV / 8; e += kVecFwdThreads) {
                 const int row = e / (DV / 8), col = (e % (DV / 8)) * 8;
                 *reinterpret_cast<uint4 *>(dst + (size_t)row * dv + col) =
                     *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
@@ -210,13 +211,13 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 wmma::store_matrix_sync(sm.A, acc, kT, wmma::mem_row_major);
             }
             __syncthreads();
-            for (int e = tid; e < kT * kT; e += kVecThreads) {
+            for (int e = tid; e < kT * kT; e += kVecFwdThreads) {
                 const int t = e / kT, s = e % kT;
                 sm.P[e] = __float2bfloat16_rn(s <= t ? sm.A[e] : 0.0f);
             }
             __syncthreads();
             // O = Qt S_in + P V, one 16-column panel per warp pass
-            for (int ni = warp; ni < DV / 16; ni += kVecThreads / 32) {
+            for (int ni = warp; ni < DV / 16; ni += kVecFwdThreads / 32) {
                 wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
                 wmma::fill_fragment(acc, 0.0f);
 #pragma unroll
@@ -236,7 +237,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             }
             __syncthreads();
             // rows t < nv of o
-            for (int e = tid; e < kT * DV / 8; e += kVecThreads) {
+            for (int e = tid; e < kT * DV / 8; e += kVecFwdThreads) {
                 const int t = e / (DV / 8), col = (e % (DV / 8)) * 8;
                 if (t >= nv)
                     continue;
@@ -259,7 +260,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         state_update<DK, DV>(sm.S32, sm.S16, sm.Kh, sm.V, sm.g);
     }
     if (hT != nullptr)
-        for (int e = tid; e < DK * DV; e += kVecThreads)
+        for (int e = tid; e < DK * DV; e += kVecFwdThreads)
             hT[unit * sstride + (size_t)(e / DV) * dv + j0 + e % DV] = sm.S32[(e / DV) * LF + e % DV];
 }
 
@@ -288,7 +289,7 @@ static_assert(sizeof(VecFwdSmem<128, 64>) <= 227 * 1024, "per-channel forward ti
 // over the document's tiles; the state before each tile comes from the
 // states pass (bf16, [H][slots][DK][dv]).
 template <int DK, int DV>
-__global__ void __launch_bounds__(kVecThreads)
+__global__ void __launch_bounds__(kVecBwdThreads)
 vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ dO,
                const float *__restrict__ a, float b, int mode, const int32_t *__restrict__ cu, int T,
@@ -309,7 +310,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     }
     const int64_t unit = (int64_t)n * H + h;
     const size_t sstride = (size_t)DK * DV;
-    for (int e = tid; e < DK * DV; e += kVecThreads) {
+    for (int e = tid; e < DK * DV; e += kVecBwdThreads) {
         const int i = e / DV, j = e % DV;
         const float x = dhT != nullptr ? dhT[unit * sstride + e] : 0.0f;
         sm.D32[i * LF + j] = x;
@@ -322,7 +323,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         // ---- loads
         {
             const __nv_bfloat16 *src = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride;
-            for (int e = tid; e < DK * DV / 8; e += kVecThreads) {
+            for (int e = tid; e < DK * DV / 8; e += kVecBwdThreads) {
                 const int row = e / (DV / 8), c8 = (e % (DV / 8)) * 8;
                 *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) =
                     *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
@@ -333,7 +334,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         load_rows(sm.V, LV, v, t0, nv, H, h, DV, 0, DV);
         load_rows(sm.dO, LV, dO, t0, nv, H, h, DV, 0, DV);
         __syncthreads();
-        for (int e = tid; e < kT * DK; e += kVecThreads) {
+        for (int e = tid; e < kT * DK; e += kVecBwdThreads) {
             const int x = (e / DK) * LK + e % DK;
             sm.Qt[x] = sm.Qr[x];
             sm.Kt[x] = sm.Kr[x];
@@ -361,14 +362,14 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             wmma::store_matrix_sync(warp == 0 ? sm.A : sm.dA, acc, kT, wmma::mem_row_major);
         }
         __syncthreads();
-        for (int e = tid; e < kT * kT; e += kVecThreads) {
+        for (int e = tid; e < kT * kT; e += kVecBwdThreads) {
             const int t = e / kT, s = e % kT;
             sm.P[e] = __float2bfloat16_rn(s <= t ? sm.A[e] : 0.0f);
             sm.dP[e] = __float2bfloat16_rn(s <= t ? sm.dA[e] : 0.0f);
         }
         __syncthreads();
         // ---- X1 = dO S_in^T;  X2 = dP^T Qt;  X3 = V D^T;  X4 = dP Kt  (N = DK panels)
-        for (int job = warp; job < 4 * (DK / 16); job += kVecThreads / 32) {
+        for (int job = warp; job < 4 * (DK / 16); job += kVecBwdThreads / 32) {
             const int kind = job / (DK / 16), ni = job % (DK / 16);
             wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
             wmma::fill_fragment(acc, 0.0f);
@@ -407,7 +408,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             }
         }
         // ---- dv = P^T dO + Kh D  (N = DV panels)
-        for (int ni = warp; ni < DV / 16; ni += kVecThreads / 32) {
+        for (int ni = warp; ni < DV / 16; ni += kVecBwdThreads / 32) {
             wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
             wmma::fill_fragment(acc, 0.0f);
             wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fp;
@@ -426,7 +427,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         }
         __syncthreads();
         // ---- gradients of q, k, v (rows t < nv); the pair terms X (into X2) and Y (into X3)
-        for (int e = tid; e < kT * DK; e += kVecThreads) {
+        for (int e = tid; e < kT * DK; e += kVecBwdThreads) {
             const int t = e / DK, i = e % DK;
             const int x = t * LX + i, xb = t * LK + i;   // fp32 / bf16 rows
             const float G = sm.Gm[e];
@@ -444,13 +445,13 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 dk[off] = dkv;
             }
         }
-        for (int e = tid; e < kT * DV; e += kVecThreads) {
+        for (int e = tid; e < kT * DV; e += kVecBwdThreads) {
             const int t = e / DV, j = e % DV;
             if (t < nv)
                 dv[((size_t)(t0 + t) * H + h) * DV + j] = sm.Y[t * LF + j];
         }
         // pairs across the whole tile: e^{gamma_i} <S_in[i,:], D[i,:]>; one warp per row group
-        for (int i = warp; i < DK; i += kVecThreads / 32) {
+        for (int i = warp; i < DK; i += kVecBwdThreads / 32) {
             float acc = 0.0f;
             for (int j = lane; j < DV; j += 32)
                 acc = fmaf(__bfloat162float(sm.S16[i * LV + j]), sm.D32[i * LF + j], acc);
@@ -480,7 +481,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         }
         __syncthreads();
         // ---- adjoint: D <- diag(g) D + Qt^T dO, tile by tile (each warp owns its tiles)
-        for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecThreads / 32) {
+        for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecBwdThreads / 32) {
             const int mi = tile / (DV / 16), ni = tile % (DV / 16);
             for (int e = lane; e < 256; e += 32)
                 sm.D32[(16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15)] *= sm.g[16 * mi + (e >> 4)];
@@ -502,7 +503,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         __syncthreads();
     }
     if (dh0 != nullptr)
-        for (int e = tid; e < DK * DV; e += kVecThreads)
+        for (int e = tid; e < DK * DV; e += kVecBwdThreads)
             dh0[unit * sstride + e] = sm.D32[(e / DV) * LF + e % DV];
 }
 
@@ -531,7 +532,7 @@ cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
         auto kern = vec_fwd_kernel<DK_, DVS, ST_>;                                                  \
         if ((err = set_smem(kern, sizeof(VecFwdSmem<DK_, DVS>))) != cudaSuccess)                    \
             return err;                                                                             \
-        kern<<<grid, kVecThreads, sizeof(VecFwdSmem<DK_, DVS>), p.stream>>>(                        \
+        kern<<<grid, kVecFwdThreads, sizeof(VecFwdSmem<DK_, DVS>), p.stream>>>(                        \
             q, k, v, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, p.dv, h0, o, o_f32, hT, states, slots, \
             p.st);                                                                                  \
     } while (0)
@@ -566,7 +567,7 @@ cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
         auto kern = vec_bwd_kernel<DK_, DV_>;                                                       \
         if ((err = set_smem(kern, sizeof(VecBwdSmem<DK_, DV_>))) != cudaSuccess)                    \
             return err;                                                                             \
-        kern<<<grid, kVecThreads, sizeof(VecBwdSmem<DK_, DV_>), p.stream>>>(                        \
+        kern<<<grid, kVecBwdThreads, sizeof(VecBwdSmem<DK_, DV_>), p.stream>>>(                        \
             q, k, v, dO, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, states, slots, dhT, dq, dk, dv, da, \
             dh0, p.st);                                                                             \
     } while (0)
