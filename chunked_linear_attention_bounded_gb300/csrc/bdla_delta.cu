@@ -393,36 +393,45 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
     for (int c = ntile - 1; c >= 0; --c) {
         const int64_t t0 = d.start + (int64_t)c * kT;
         const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
-        // ---- P0: inputs, the state before the tile, decay scalars
+        // ---- P0: inputs, the state before the tile (every global load issued
+        //      before the shared stores), decay scalars
         {
-            const int rows_k = DK / 8, rows_v = DV / 8;
-            for (int e = tid; e < kT * rows_k; e += kBT) {
-                const int t = e / rows_k, c8 = (e % rows_k) * 8;
-                uint4 qv = make_uint4(0, 0, 0, 0), kv = qv;
-                if (t < nv) {
-                    const size_t off = ((size_t)(t0 + t) * H + h) * DK + c8;
-                    qv = *reinterpret_cast<const uint4 *>(q + off);
-                    kv = *reinterpret_cast<const uint4 *>(k + off);
-                }
-                *reinterpret_cast<uint4 *>(sm.Q + t * LK + c8) = qv;
-                *reinterpret_cast<uint4 *>(sm.K + t * LK + c8) = kv;
-            }
-            for (int e = tid; e < kT * rows_v; e += kBT) {
-                const int t = e / rows_v, c8 = (e % rows_v) * 8;
-                uint4 vv = make_uint4(0, 0, 0, 0), gv = vv;
-                if (t < nv) {
-                    const size_t off = ((size_t)(t0 + t) * H + h) * DV + c8;
-                    vv = *reinterpret_cast<const uint4 *>(v + off);
-                    gv = *reinterpret_cast<const uint4 *>(dO + off);
-                }
-                *reinterpret_cast<uint4 *>(sm.V + t * LV + c8) = vv;
-                *reinterpret_cast<uint4 *>(sm.dO + t * LV + c8) = gv;
-            }
+            constexpr int rows_k = DK / 8, rows_v = DV / 8;
+            constexpr int NS = DK * rows_v / kBT;   // state chunks per thread
+            static_assert(NS >= 1 && DK * rows_v % kBT == 0 && kT * rows_k <= kBT && kT * rows_v <= kBT, "loads");
             const __nv_bfloat16 *src = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride;
-            for (int e = tid; e < DK * rows_v; e += kBT) {
-                const int row = e / rows_v, c8 = (e % rows_v) * 8;
-                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) =
-                    *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            uint4 sv[NS];
+#pragma unroll
+            for (int x = 0; x < NS; ++x) {
+                const int e = tid + x * kBT, row = e / rows_v, c8 = (e % rows_v) * 8;
+                sv[x] = *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            }
+            const uint4 z4 = make_uint4(0, 0, 0, 0);
+            uint4 qv = z4, kv = z4, vv = z4, gv = z4;
+            const int tk = tid / rows_k, ck = (tid % rows_k) * 8, tq = tid / rows_v, cv = (tid % rows_v) * 8;
+            const bool hk = tid < kT * rows_k, hv = tid < kT * rows_v;
+            if (hk && tk < nv) {
+                const size_t off = ((size_t)(t0 + tk) * H + h) * DK + ck;
+                qv = *reinterpret_cast<const uint4 *>(q + off);
+                kv = *reinterpret_cast<const uint4 *>(k + off);
+            }
+            if (hv && tq < nv) {
+                const size_t off = ((size_t)(t0 + tq) * H + h) * DV + cv;
+                vv = *reinterpret_cast<const uint4 *>(v + off);
+                gv = *reinterpret_cast<const uint4 *>(dO + off);
+            }
+#pragma unroll
+            for (int x = 0; x < NS; ++x) {
+                const int e = tid + x * kBT, row = e / rows_v, c8 = (e % rows_v) * 8;
+                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) = sv[x];
+            }
+            if (hk) {
+                *reinterpret_cast<uint4 *>(sm.Q + tk * LK + ck) = qv;
+                *reinterpret_cast<uint4 *>(sm.K + tk * LK + ck) = kv;
+            }
+            if (hv) {
+                *reinterpret_cast<uint4 *>(sm.V + tq * LV + cv) = vv;
+                *reinterpret_cast<uint4 *>(sm.dO + tq * LV + cv) = gv;
             }
             if (warp == 0) {
                 const bool in = lane < nv;

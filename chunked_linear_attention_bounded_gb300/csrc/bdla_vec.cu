@@ -68,26 +68,33 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv
     }
 }
 
-// Channel pass of a tile: thread i < DK walks the 16 tokens of channel i.
+// Channel pass of a tile: thread i < DK walks the 16 tokens of channel i
+// (the tile's 16 logits of the channel are loaded before any is used).
 // Writes Qt, Kt, Kh (bf16, in place over the raw q, k where given), the
-// tile-local Gamma (optional) and g = e^{gamma}.  Rows past nv have
-// lambda = 0 and zero q, k, so they change nothing.
+// tile-local Gamma and d lambda / d a (both optional) and g = e^{gamma}.
+// Rows past nv have lambda = 0 and zero q, k, so they change nothing.
 template <int DK>
 __device__ __forceinline__ void channel_pass(const float *__restrict__ a, int64_t t0, int nv, int H, int h, float b,
                                              int mode, __nv_bfloat16 *Qt, __nv_bfloat16 *Kt, __nv_bfloat16 *Kh,
-                                             float *gam_out, float *g)
+                                             float *gam_out, float *g, float *dlam_out = nullptr)
 {
     constexpr int LK = padb(DK);
     const int i = threadIdx.x;
     if (i >= DK)
         return;
+    float av[kT];
+#pragma unroll
+    for (int t = 0; t < kT; ++t)
+        av[t] = t < nv ? a[((t0 + t) * H + h) * (int64_t)DK + i] : 0.0f;
     float G[kT];
     float run = 0.0f;
 #pragma unroll
     for (int t = 0; t < kT; ++t) {
-        const float lam = t < nv ? log_decay(a[((t0 + t) * H + h) * (int64_t)DK + i], b, mode) : 0.0f;
+        const float lam = t < nv ? log_decay(av[t], b, mode) : 0.0f;
         run += lam;
         G[t] = run;
+        if (dlam_out != nullptr)
+            dlam_out[t * DK + i] = t < nv ? log_decay_deriv(av[t], b, mode) : 0.0f;
     }
     const float gam = run;
 #pragma unroll
@@ -275,6 +282,7 @@ struct VecBwdSmem {
     __nv_bfloat16 P[kT * kT], dP[kT * kT];
     float A[kT * kT], dA[kT * kT];
     float Gm[kT * DK];     // tile-local Gamma
+    float Dl[kT * DK];     // d lambda / d a
     float X1[kT * padf(DK)];   // dO S_in^T (inter dq, unscaled)
     float X2[kT * padf(DK)];   // dP^T Qt (intra dk, unscaled), then the pair terms X
     float X3[kT * padf(DK)];   // V D^T (inter dk, unscaled), then the terms Y
@@ -320,19 +328,47 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     for (int c = ntile - 1; c >= 0; --c) {
         const int64_t t0 = d.start + (int64_t)c * kT;
         const int nv = (int)(d.len - (int64_t)c * kT < kT ? d.len - (int64_t)c * kT : kT);
-        // ---- loads
+        // ---- loads: every global load of the tile is issued before the shared stores
         {
+            constexpr int NS = DK * DV / 8 / kVecBwdThreads;   // state chunks per thread
+            static_assert(NS >= 1 && DK * DV / 8 % kVecBwdThreads == 0, "state chunks");
+            static_assert(kT * DK / 8 <= kVecBwdThreads && kT * DV / 8 <= kVecBwdThreads, "row chunks");
             const __nv_bfloat16 *src = states + ((size_t)h * n_slots + (size_t)(d.start / kT + n + c)) * sstride;
-            for (int e = tid; e < DK * DV / 8; e += kVecBwdThreads) {
-                const int row = e / (DV / 8), c8 = (e % (DV / 8)) * 8;
-                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) =
-                    *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            uint4 sv[NS];
+#pragma unroll
+            for (int x = 0; x < NS; ++x) {
+                const int e = tid + x * kVecBwdThreads, row = e / (DV / 8), c8 = (e % (DV / 8)) * 8;
+                sv[x] = *reinterpret_cast<const uint4 *>(src + (size_t)row * DV + c8);
+            }
+            const uint4 z4 = make_uint4(0, 0, 0, 0);
+            uint4 qv = z4, kv = z4, vv = z4, gv = z4;
+            const int tk = tid / (DK / 8), ck = (tid % (DK / 8)) * 8;
+            const int tvv = tid / (DV / 8), cv = (tid % (DV / 8)) * 8;
+            const bool hk = tid < kT * DK / 8, hv = tid < kT * DV / 8;
+            if (hk && tk < nv) {
+                const size_t off = ((size_t)(t0 + tk) * H + h) * DK + ck;
+                qv = *reinterpret_cast<const uint4 *>(q + off);
+                kv = *reinterpret_cast<const uint4 *>(k + off);
+            }
+            if (hv && tvv < nv) {
+                const size_t off = ((size_t)(t0 + tvv) * H + h) * DV + cv;
+                vv = *reinterpret_cast<const uint4 *>(v + off);
+                gv = *reinterpret_cast<const uint4 *>(dO + off);
+            }
+#pragma unroll
+            for (int x = 0; x < NS; ++x) {
+                const int e = tid + x * kVecBwdThreads, row = e / (DV / 8), c8 = (e % (DV / 8)) * 8;
+                *reinterpret_cast<uint4 *>(sm.S16 + row * LV + c8) = sv[x];
+            }
+            if (hk) {
+                *reinterpret_cast<uint4 *>(sm.Qr + tk * LK + ck) = qv;
+                *reinterpret_cast<uint4 *>(sm.Kr + tk * LK + ck) = kv;
+            }
+            if (hv) {
+                *reinterpret_cast<uint4 *>(sm.V + tvv * LV + cv) = vv;
+                *reinterpret_cast<uint4 *>(sm.dO + tvv * LV + cv) = gv;
             }
         }
-        load_rows(sm.Qr, LK, q, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.Kr, LK, k, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.V, LV, v, t0, nv, H, h, DV, 0, DV);
-        load_rows(sm.dO, LV, dO, t0, nv, H, h, DV, 0, DV);
         __syncthreads();
         for (int e = tid; e < kT * DK; e += kVecBwdThreads) {
             const int x = (e / DK) * LK + e % DK;
@@ -340,7 +376,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             sm.Kt[x] = sm.Kr[x];
         }
         __syncthreads();
-        channel_pass<DK>(a, t0, nv, H, h, b, mode, sm.Qt, sm.Kt, sm.Kh, sm.Gm, sm.g);
+        channel_pass<DK>(a, t0, nv, H, h, b, mode, sm.Qt, sm.Kt, sm.Kh, sm.Gm, sm.g, sm.Dl);
         if (tid < DK)
             sm.gam[tid] = sm.Gm[(kT - 1) * DK + tid];
         __syncthreads();
@@ -473,31 +509,47 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             for (int t = 0; t < kT; ++t) {
                 if (t < nv) {
                     const size_t off = ((size_t)(t0 + t) * H + h) * DK + i;
-                    da[off] = (xb + (ytot - yb) + sm.cst[i]) * log_decay_deriv(a[off], b, mode);
+                    da[off] = (xb + (ytot - yb) + sm.cst[i]) * sm.Dl[t * DK + i];
                 }
                 xb += sm.X2[t * LX + i];
                 yb += sm.X3[t * LX + i];
             }
         }
         __syncthreads();
-        // ---- adjoint: D <- diag(g) D + Qt^T dO, tile by tile (each warp owns its tiles)
-        for (int tile = warp; tile < (DK / 16) * (DV / 16); tile += kVecBwdThreads / 32) {
-            const int mi = tile / (DV / 16), ni = tile % (DV / 16);
-            for (int e = lane; e < 256; e += 32)
-                sm.D32[(16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15)] *= sm.g[16 * mi + (e >> 4)];
+        // ---- adjoint: D <- diag(g) D + Qt^T dO; each warp owns NTW tiles and
+        //      takes every step for all of them before the next step
+        {
+            constexpr int NTW = (DK / 16) * (DV / 16) / (kVecBwdThreads / 32);
+            static_assert(NTW >= 1 && (DK / 16) * (DV / 16) % (kVecBwdThreads / 32) == 0, "adjoint tiles");
+#pragma unroll
+            for (int x = 0; x < NTW; ++x) {
+                const int tile = warp + x * (kVecBwdThreads / 32), mi = tile / (DV / 16), ni = tile % (DV / 16);
+#pragma unroll
+                for (int e = lane; e < 256; e += 32)
+                    sm.D32[(16 * mi + (e >> 4)) * LF + 16 * ni + (e & 15)] *= sm.g[16 * mi + (e >> 4)];
+            }
             __syncwarp();
-            wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
-            wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
-            wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
-            wmma::load_matrix_sync(acc, sm.D32 + 16 * mi * LF + 16 * ni, LF, wmma::mem_row_major);
-            wmma::load_matrix_sync(fa, sm.Qt + 16 * mi, LK);   // A[i][t] = Qt[t][16 mi + i]
-            wmma::load_matrix_sync(fb, sm.dO + 16 * ni, LV);
-            wmma::mma_sync(acc, fa, fb, acc);
-            wmma::store_matrix_sync(sm.D32 + 16 * mi * LF + 16 * ni, acc, LF, wmma::mem_row_major);
+#pragma unroll
+            for (int x = 0; x < NTW; ++x) {
+                const int tile = warp + x * (kVecBwdThreads / 32), mi = tile / (DV / 16), ni = tile % (DV / 16);
+                wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+                wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major> fa;
+                wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major> fb;
+                wmma::load_matrix_sync(acc, sm.D32 + 16 * mi * LF + 16 * ni, LF, wmma::mem_row_major);
+                wmma::load_matrix_sync(fa, sm.Qt + 16 * mi, LK);   // A[i][t] = Qt[t][16 mi + i]
+                wmma::load_matrix_sync(fb, sm.dO + 16 * ni, LV);
+                wmma::mma_sync(acc, fa, fb, acc);
+                wmma::store_matrix_sync(sm.D32 + 16 * mi * LF + 16 * ni, acc, LF, wmma::mem_row_major);
+            }
             __syncwarp();
-            for (int e = lane; e < 256; e += 32) {
-                const int r = 16 * mi + (e >> 4), c2 = 16 * ni + (e & 15);
-                sm.D16[r * LV + c2] = __float2bfloat16_rn(sm.D32[r * LF + c2]);
+#pragma unroll
+            for (int x = 0; x < NTW; ++x) {
+                const int tile = warp + x * (kVecBwdThreads / 32), mi = tile / (DV / 16), ni = tile % (DV / 16);
+#pragma unroll
+                for (int e = lane; e < 256; e += 32) {
+                    const int r = 16 * mi + (e >> 4), c2 = 16 * ni + (e & 15);
+                    sm.D16[r * LV + c2] = __float2bfloat16_rn(sm.D32[r * LF + c2]);
+                }
             }
         }
         __syncthreads();
