@@ -627,7 +627,9 @@ def variant_arm(args, w, inp):
            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                         "frac": achieved / hbm, "peak_source": hbm_src, "traffic": None,
                         "algorithmic_bytes_per_launch": ab[dom]},
-           "kernel_ms": kernel_ms, "gpu_launches": 2 * K, "clocks": clk.summary(),
+           "kernel_ms": kernel_ms,
+           # fwd and bwd kernels, each after the document-order kernel for packed documents
+           "gpu_launches": (2 + (2 if nd > 1 else 0)) * K, "clocks": clk.summary(),
            "states": "bf16 state before every 16-token tile, written by the forward, read by the backward"}
     print(json.dumps(out), flush=True)
 

@@ -474,9 +474,29 @@ bdla_status check_vec(const bdla_dims &d, const int32_t *cu, int n_docs)
     return BDLA_OK;
 }
 
-size_t vec_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off)
+// Workspace of the per-channel and delta-rule calls: status word, the
+// document order (packed calls with 2 .. kMaxOrderedDocs documents), and for
+// the backward the states of its own states pass.
+size_t variant_order_bytes(bool varlen, int n_docs)
 {
-    size_t off = round_up(kStatusBytes);
+    return (varlen && n_docs > 1 && n_docs <= kMaxOrderedDocs) ? round_up((size_t)n_docs * 4) : 0;
+}
+
+// The documents longest first in the workspace's order region (packed calls
+// with several documents), else nullptr: one small kernel on the stream.
+cudaError_t variant_order(const Problem &p, void *ws, bool varlen, const int32_t **order)
+{
+    *order = nullptr;
+    if (variant_order_bytes(varlen, p.n_docs) == 0)
+        return cudaSuccess;
+    auto *o = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + round_up(kStatusBytes));
+    *order = o;
+    return launch_doc_order(p, o);
+}
+
+size_t vec_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off, bool varlen = false)
+{
+    size_t off = round_up(kStatusBytes) + variant_order_bytes(varlen, n_docs);
     *states_off = off;
     if (op == BDLA_OP_BWD) {
         Problem p{};
@@ -506,7 +526,7 @@ size_t bdla_workspace_bytes_vec(int op, bdla_dims d, int n_docs)
     if (check_vec(d, varlen ? reinterpret_cast<const int32_t *>(1) : nullptr, n_docs) != BDLA_OK)
         return 0;
     size_t so;
-    return vec_layout(op, d, varlen ? n_docs : d.B, &so);
+    return vec_layout(op, d, varlen ? n_docs : d.B, &so, varlen);
 }
 
 bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const float *a, float b, int chunk,
@@ -524,12 +544,14 @@ bdla_status bdla_fwd_vec(const void *q, const void *k, const void *v, const floa
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
         return BDLA_ERR_DTYPE;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so, cu_seqlens != nullptr)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
     KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
+    const int32_t *order;
+    BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
     BDLA_CUDA(launch_vec_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
                              static_cast<const __nv_bfloat16 *>(v), a, h0, o, o_dtype == BDLA_F32, hT,
-                             static_cast<__nv_bfloat16 *>(states)));
+                             static_cast<__nv_bfloat16 *>(states), order));
     return BDLA_OK;
 }
 
@@ -547,22 +569,25 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
         !aligned16(dhT) || !aligned16(dh0) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, vec_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so, cu_seqlens != nullptr)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const __nv_bfloat16 *st = static_cast<const __nv_bfloat16 *>(states);
+    const int32_t *order;
     if (st == nullptr) {   // no states from the forward: a states pass into the workspace
         auto *wst = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
         KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_vec_fwd(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, wst));
+        BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
+        BDLA_CUDA(launch_vec_fwd(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, wst, order));
         st = wst;
     }
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
         BDLA_CUDA(launch_vec_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, st, dhT, dq,
-                                 dk, dv, da, dh0));
+                                 dk, dv, da, dh0, order));
     }
     return BDLA_OK;
 }
@@ -570,9 +595,9 @@ bdla_status bdla_bwd_vec(const void *q, const void *k, const void *v, const floa
 // ---------------------------------------------------------------- gated delta rule
 namespace {
 
-size_t delta_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off)
+size_t delta_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off, bool varlen = false)
 {
-    size_t off = round_up(kStatusBytes);
+    size_t off = round_up(kStatusBytes) + variant_order_bytes(varlen, n_docs);
     *states_off = off;
     if (op == BDLA_OP_BWD) {
         Problem p{};
@@ -591,7 +616,7 @@ size_t bdla_workspace_bytes_delta(int op, bdla_dims d, int n_docs)
     if (check_vec(d, varlen ? reinterpret_cast<const int32_t *>(1) : nullptr, n_docs) != BDLA_OK)
         return 0;
     size_t so;
-    return delta_layout(op, d, varlen ? n_docs : d.B, &so);
+    return delta_layout(op, d, varlen ? n_docs : d.B, &so, varlen);
 }
 
 bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const float *a, const float *beta,
@@ -609,12 +634,14 @@ bdla_status bdla_fwd_delta(const void *q, const void *k, const void *v, const fl
     if (o_dtype != BDLA_BF16 && o_dtype != BDLA_F32)
         return BDLA_ERR_DTYPE;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(BDLA_OP_FWD, d, cu_seqlens ? n_docs : d.B, &so, cu_seqlens != nullptr)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
     KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
+    const int32_t *order;
+    BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
     BDLA_CUDA(launch_delta_fwd(p, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
                                static_cast<const __nv_bfloat16 *>(v), a, beta, h0, o, o_dtype == BDLA_F32, hT,
-                               static_cast<__nv_bfloat16 *>(states)));
+                               static_cast<__nv_bfloat16 *>(states), order));
     return BDLA_OK;
 }
 
@@ -633,22 +660,25 @@ bdla_status bdla_bwd_delta(const void *q, const void *k, const void *v, const fl
         !aligned16(dbeta) || !aligned16(h0) || !aligned16(dhT) || !aligned16(dh0) || !aligned16(states))
         return BDLA_ERR_ALIGN;
     size_t so;
-    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so)));
+    BDLA_TRY(check_ws(ws, ws_bytes, delta_layout(states ? BDLA_OP_FWD : BDLA_OP_BWD, d, cu_seqlens ? n_docs : d.B, &so, cu_seqlens != nullptr)));
     Problem p = make_problem(d, cu_seqlens, n_docs, b, mode, ws, stream);
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
     const __nv_bfloat16 *st = static_cast<const __nv_bfloat16 *>(states);
+    const int32_t *order;
     if (st == nullptr) {   // no states from the forward: a states pass into the workspace
         auto *wst = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + so);
         KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
-        BDLA_CUDA(launch_delta_fwd(p, qb, kb, vb, a, beta, h0, nullptr, 0, nullptr, wst));
+        BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
+        BDLA_CUDA(launch_delta_fwd(p, qb, kb, vb, a, beta, h0, nullptr, 0, nullptr, wst, order));
         st = wst;
     }
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        BDLA_CUDA(variant_order(p, ws, cu_seqlens != nullptr, &order));
         BDLA_CUDA(launch_delta_bwd(p, qb, kb, vb, static_cast<const __nv_bfloat16 *>(dO), a, beta, st, dhT,
-                                   dq, dk, dv, da, dbeta, dh0));
+                                   dq, dk, dv, da, dbeta, dh0, order));
     }
     return BDLA_OK;
 }

@@ -55,21 +55,6 @@ struct DeltaFwdSmem {
     float G[kT], eG[kT], beta[kT];
 };
 
-// Rows [t0, t0 + nv) of a token-major bf16 tensor [tokens][H][d] (columns
-// [c0, c0 + w)) into a [16][ld] tile; rows past nv are zero.  w % 8 == 0.
-__device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv_bfloat16 *src, int64_t t0, int nv,
-                                          int H, int h, int d, int c0, int w)
-{
-    const int chunks = kT * w / 8;
-    for (int e = threadIdx.x; e < chunks; e += kDT) {
-        const int t = e / (w / 8), c = (e % (w / 8)) * 8;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (t < nv)
-            val = *reinterpret_cast<const uint4 *>(src + ((t0 + t) * H + h) * (int64_t)d + c0 + c);
-        *reinterpret_cast<uint4 *>(dst + t * ld + c) = val;
-    }
-}
-
 // C[16][16] (ld LS) = A B^T for two [16][DK] bf16 tiles (ld LK); one warp.
 template <int DK, int LK, int LS>
 __device__ __forceinline__ void gram16(float *C, const __nv_bfloat16 *A, const __nv_bfloat16 *B)
@@ -115,14 +100,15 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a,
                  const float *__restrict__ beta, float b, int mode, const int32_t *__restrict__ cu, int T,
                  int64_t tokens, int H, int dv, const float *__restrict__ h0, void *__restrict__ o, int o_f32,
-                 float *__restrict__ hT, __nv_bfloat16 *__restrict__ states, int64_t n_slots, DeviceStatus *st)
+                 float *__restrict__ hT, __nv_bfloat16 *__restrict__ states, int64_t n_slots, DeviceStatus *st,
+               const int32_t *__restrict__ order)
 {
     using Sm = DeltaFwdSmem<DK>;
     constexpr int LK = Sm::LK, LV = Sm::LV, LF = Sm::LF, LS = Sm::LS;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j0 = blockIdx.x * kDvs, h = blockIdx.y, n = blockIdx.z;
+    const int j0 = blockIdx.x * kDvs, h = blockIdx.y, n = order != nullptr ? order[blockIdx.z] : (int)blockIdx.z;
     const DocSpan d = doc_span(cu, n, T);
     if (!doc_valid(d, tokens)) {
         if (tid == 0)
@@ -151,10 +137,29 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                     *reinterpret_cast<const uint4 *>(sm.S16 + row * LV + col);
             }
         }
-        if (!STATES)
-            load_rows(sm.Q, LK, q, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.K, LK, k, t0, nv, H, h, DK, 0, DK);
-        load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, kDvs);
+        {   // q, k and the value slice: every global load before the shared stores
+            static_assert(kT * DK / 8 <= kDT && kT * kDvs / 8 <= kDT, "one chunk per thread");
+            const uint4 z4 = make_uint4(0, 0, 0, 0);
+            uint4 qv = z4, kv = z4, vv = z4;
+            const int tk = tid / (DK / 8), ck = (tid % (DK / 8)) * 8;
+            const int tq = tid / (kDvs / 8), cv = (tid % (kDvs / 8)) * 8;
+            const bool hk = tid < kT * DK / 8, hv = tid < kT * kDvs / 8;
+            if (hk && tk < nv) {
+                const size_t off = ((size_t)(t0 + tk) * H + h) * DK + ck;
+                if (!STATES)
+                    qv = *reinterpret_cast<const uint4 *>(q + off);
+                kv = *reinterpret_cast<const uint4 *>(k + off);
+            }
+            if (hv && tq < nv)
+                vv = *reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + tq) * H + h) * dv + j0 + cv);
+            if (hk) {
+                if (!STATES)
+                    *reinterpret_cast<uint4 *>(sm.Q + tk * LK + ck) = qv;
+                *reinterpret_cast<uint4 *>(sm.K + tk * LK + ck) = kv;
+            }
+            if (hv)
+                *reinterpret_cast<uint4 *>(sm.V + tq * LV + cv) = vv;
+        }
         if (warp == 0) {
             const bool in = lane < nv;
             float x = in ? log_decay(a[(t0 + lane) * H + h], b, mode) : 0.0f;
@@ -343,6 +348,7 @@ struct DeltaBwdSmem {
     float E[kT * LS], P[kT * LS], KE[kT * LS], Lm[kT * LS], Tm[kT * LS], dP[kT * LS], X[kT * LS], dL[kT * LS];
     float stage[kBT / 32][256];   // per-warp 16 x 16 fp32 staging
     float G[kT], eG[kT], w[kT], beta[kT], sq[kT], sm_[kT], wdw[kT], red[kBT / 32];
+    float dlda[kT], cross[kT], dbeta[kT];   // d lambda / d a; pair sums and dbeta (P11)
 };
 static_assert(sizeof(DeltaBwdSmem<128, 128>) <= 227 * 1024, "delta backward tile exceeds shared memory");
 
@@ -354,7 +360,8 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H,
                  const __nv_bfloat16 *__restrict__ states, int64_t n_slots, const float *__restrict__ dhT,
                  float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, float *__restrict__ da,
-                 float *__restrict__ dbeta, float *__restrict__ dh0, DeviceStatus *st)
+                 float *__restrict__ dbeta, float *__restrict__ dh0, DeviceStatus *st,
+               const int32_t *__restrict__ order)
 {
     using Sm = DeltaBwdSmem<DK, DV>;
     constexpr int LK = Sm::LK, LV = Sm::LV, LW = Sm::LW, LS = Sm::LS;
@@ -364,7 +371,7 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x, n = order != nullptr ? order[blockIdx.y] : (int)blockIdx.y;
     const DocSpan d = doc_span(cu, n, T);
     if (!doc_valid(d, tokens)) {
         if (tid == 0)
@@ -435,7 +442,8 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             }
             if (warp == 0) {
                 const bool in = lane < nv;
-                float x = in ? log_decay(a[(t0 + lane) * H + h], b, mode) : 0.0f;
+                const float av = in ? a[(t0 + lane) * H + h] : 0.0f;
+                float x = in ? log_decay(av, b, mode) : 0.0f;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -448,6 +456,7 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                     sm.eG[lane] = expf(x);
                     sm.w[lane] = expf(gam - x);
                     sm.beta[lane] = in ? beta[(t0 + lane) * H + h] : 0.0f;
+                    sm.dlda[lane] = in ? log_decay_deriv(av, b, mode) : 0.0f;
                 }
             }
         }
@@ -577,21 +586,28 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             wmma::store_matrix_sync(C + 16 * ni, acc, LW, wmma::mem_row_major);
         }
         __syncthreads();
-        // ---- P8: dP, dT, dv
-        for (int e = tid; e < kT * kT; e += kBT) {
-            const int t = e / kT, s = e % kT;
+        // ---- P8: dP, dT (two adjacent lanes per (t, s), each half of the sums), dv
+        static_assert(2 * kT * kT == kBT, "two lanes per pair, every thread");
+        if (tid < 2 * kT * kT) {
+            const int item = tid >> 1, part = tid & 1;
+            const int t = item / kT, s = item % kT;
             float acc = 0.0f;
             if (s <= t)
-                for (int j = 0; j < DV; ++j)
+                for (int j = part; j < DV; j += 2)
                     acc += __bfloat162float(sm.dO[t * LV + j]) * sm.B1[s * LW + j];
-            sm.dP[t * LS + s] = acc;
             float dt = 0.0f;
-            for (int j = 0; j < DV; ++j)
+            for (int j = part; j < DV; j += 2)
                 dt += sm.B4[t * LW + j] * __bfloat162float(sm.V[s * LV + j]);
             float dw = 0.0f;
-            for (int i = 0; i < DK; ++i)
+            for (int i = part; i < DK; i += 2)
                 dw += sm.B3[t * LW + i] * __bfloat162float(sm.K[s * LK + i]);
-            sm.X[t * LS + s] = dt + sm.eG[s] * dw;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            dt += __shfl_xor_sync(0xffffffffu, dt, 1);
+            dw += __shfl_xor_sync(0xffffffffu, dw, 1);
+            if (part == 0) {
+                sm.dP[t * LS + s] = acc;
+                sm.X[t * LS + s] = dt + sm.eG[s] * dw;
+            }
         }
         for (int e = tid; e < kT * DV; e += kBT) {
             const int t = e / DV, j = e % DV;
@@ -644,7 +660,21 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             sm.dL[t * LS + s] = acc;
         }
         __syncthreads();
-        // ---- P11: dq, dk; per-row sums for the decay gradient
+        // ---- P11: dq, dk; per-row sums for the decay gradient; the last warp
+        //      (no dq/dk items) takes the pair sums and dbeta
+        static_assert(kT * (DK / 8) <= kBT - 32, "the last warp is free in P11");
+        if (warp == NW - 1 && lane < kT) {
+            const int r = lane;
+            float cr = 0.0f;
+            for (int t = r; t < kT; ++t)
+                for (int s = 0; s < r; ++s)
+                    cr += sm.dP[t * LS + s] * sm.P[t * LS + s] + sm.dL[t * LS + s] * sm.Lm[t * LS + s];
+            sm.cross[r] = cr;
+            float db = sm.X[r * LS + r];
+            for (int s = 0; s < r; ++s)
+                db += sm.dL[r * LS + s] * sm.KE[r * LS + s];
+            sm.dbeta[r] = db;
+        }
         {
             constexpr int IPR = DK / 8;   // items per row, contiguous lanes
             for (int e = tid; e < kT * IPR; e += kBT) {
@@ -700,10 +730,7 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
         // ---- P12: decay and write-strength gradients; D <- e^gamma D + Q^T (e^Gamma o dO) - W^T dDelta
         if (warp == 0 && lane < kT) {
             const int r = lane;
-            float cross = 0.0f;
-            for (int t = r; t < kT; ++t)
-                for (int s = 0; s < r; ++s)
-                    cross += sm.dP[t * LS + s] * sm.P[t * LS + s] + sm.dL[t * LS + s] * sm.Lm[t * LS + s];
+            const float cross = sm.cross[r];
             float suffix = 0.0f, prefix = 0.0f;
             for (int t = r; t < kT; ++t)
                 suffix += sm.eG[t] * (sm.sq[t] + sm.sm_[t]);
@@ -713,14 +740,11 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 #pragma unroll
             for (int x = 0; x < NW; ++x)
                 state += sm.red[x];
-            float db = sm.X[r * LS + r];
-            for (int s = 0; s < r; ++s)
-                db += sm.dL[r * LS + s] * sm.KE[r * LS + s];
             if (r < nv) {
                 const size_t off = (size_t)(t0 + r) * H + h;
                 const float dl = cross + suffix + prefix + expf(gam) * state;
-                da[off] = dl * log_decay_deriv(a[off], b, mode);
-                dbeta[off] = db;
+                da[off] = dl * sm.dlda[r];
+                dbeta[off] = sm.dbeta[r];
             }
         }
         {
@@ -773,7 +797,7 @@ int64_t delta_state_slots(const Problem &p) { return p.tokens / kT + p.n_docs + 
 
 cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *a, const float *beta, const float *h0, void *o,
-                             int o_f32, float *hT, __nv_bfloat16 *states)
+                             int o_f32, float *hT, __nv_bfloat16 *states, const int32_t *order)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -787,7 +811,7 @@ cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __n
             return err;                                                                             \
         kern<<<grid, kDT, sizeof(DeltaFwdSmem<DK_>), p.stream>>>(q, k, v, a, beta, p.b, p.mode, p.cu, p.T,   \
                                                                  p.tokens, p.H, p.dv, h0, o, o_f32, hT,     \
-                                                                 states, slots, p.st);                      \
+                                                                 states, slots, p.st, order);               \
     } while (0)
     const bool st = o == nullptr;   // states pass only
     if (p.dk == 64) {
@@ -808,7 +832,7 @@ cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __n
 cudaError_t launch_delta_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a, const float *beta,
                              const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
-                             float *da, float *dbeta, float *dh0)
+                             float *da, float *dbeta, float *dh0, const int32_t *order)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -822,7 +846,7 @@ cudaError_t launch_delta_bwd(const Problem &p, const __nv_bfloat16 *q, const __n
             return err;                                                                             \
         kern<<<grid, kBT, sizeof(DeltaBwdSmem<DK_, DV_>), p.stream>>>(                              \
             q, k, v, dO, a, beta, p.b, p.mode, p.cu, p.T, p.tokens, p.H, states, slots, dhT, dq, dk, dv, da, \
-            dbeta, dh0, p.st);                                                                      \
+            dbeta, dh0, p.st, order);                                                               \
     } while (0)
     if (p.dk == 64 && p.dv == 64)
         BDLA_DELTA_BWD(64, 64);

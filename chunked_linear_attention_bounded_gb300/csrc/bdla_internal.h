@@ -170,17 +170,18 @@ cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
                              float *part, const SegPlan &seg);
 
 
-// Per-channel decay (a, da: [tokens][H][dk] fp32).  Forward: o, hT; with
+// Per-channel decay (a, da: [tokens][H][dk] fp32).  `order` (optional): the
+// documents in launch order (longest first).  Forward: o, hT; with
 // `states` non-null it runs the states pass instead (no q, no o): the bf16
 // state before every 16-token tile into states [H][vec_state_slots][dk][dv].
 int64_t vec_state_slots(const Problem &p);
 cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, const float *a, const float *h0, void *o, int o_f32,
-                           float *hT, __nv_bfloat16 *states);
+                           float *hT, __nv_bfloat16 *states, const int32_t *order);
 cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a,
                            const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
-                           float *da, float *dh0);
+                           float *da, float *dh0, const int32_t *order);
 
 // Gated delta rule (a, beta: [tokens][H] fp32).  Forward: o, hT; with
 // `states` non-null it runs the states pass instead (no q, no o): the bf16
@@ -188,10 +189,10 @@ cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
 int64_t delta_state_slots(const Problem &p);
 cudaError_t launch_delta_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const float *a, const float *beta, const float *h0, void *o,
-                             int o_f32, float *hT, __nv_bfloat16 *states);
+                             int o_f32, float *hT, __nv_bfloat16 *states, const int32_t *order);
 cudaError_t launch_delta_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a, const float *beta,
                              const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
-                             float *da, float *dbeta, float *dh0);
+                             float *da, float *dbeta, float *dh0, const int32_t *order);
 
 }  // namespace bdla

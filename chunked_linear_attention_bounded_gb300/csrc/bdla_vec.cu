@@ -162,13 +162,14 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ a, float b, int mode,
                const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dv,
                const float *__restrict__ h0, void *__restrict__ o, int o_f32, float *__restrict__ hT,
-               __nv_bfloat16 *__restrict__ states, int64_t n_slots, DeviceStatus *st)
+               __nv_bfloat16 *__restrict__ states, int64_t n_slots, DeviceStatus *st,
+               const int32_t *__restrict__ order)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     VecFwdSmem<DK, DV> &sm = *reinterpret_cast<VecFwdSmem<DK, DV> *>(smem_raw);
     constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int j0 = blockIdx.x * DV, h = blockIdx.y, n = blockIdx.z;
+    const int j0 = blockIdx.x * DV, h = blockIdx.y, n = order != nullptr ? order[blockIdx.z] : (int)blockIdx.z;
     const DocSpan d = doc_span(cu, n, T);
     if (!doc_valid(d, tokens)) {
         if (tid == 0)
@@ -303,13 +304,14 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                const float *__restrict__ a, float b, int mode, const int32_t *__restrict__ cu, int T,
                int64_t tokens, int H, const __nv_bfloat16 *__restrict__ states, int64_t n_slots,
                const float *__restrict__ dhT, float *__restrict__ dq, float *__restrict__ dk,
-               float *__restrict__ dv, float *__restrict__ da, float *__restrict__ dh0, DeviceStatus *st)
+               float *__restrict__ dv, float *__restrict__ da, float *__restrict__ dh0, DeviceStatus *st,
+               const int32_t *__restrict__ order)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     VecBwdSmem<DK, DV> &sm = *reinterpret_cast<VecBwdSmem<DK, DV> *>(smem_raw);
     constexpr int LK = padb(DK), LV = padb(DV), LF = padf(DV), LX = padf(DK);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x, n = order != nullptr ? order[blockIdx.y] : (int)blockIdx.y;
     const DocSpan d = doc_span(cu, n, T);
     if (!doc_valid(d, tokens)) {
         if (tid == 0)
@@ -571,7 +573,7 @@ int64_t vec_state_slots(const Problem &p) { return p.tokens / kT + p.n_docs + 1;
 
 cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, const float *a, const float *h0, void *o, int o_f32,
-                           float *hT, __nv_bfloat16 *states)
+                           float *hT, __nv_bfloat16 *states, const int32_t *order)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -586,7 +588,7 @@ cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
             return err;                                                                             \
         kern<<<grid, kVecFwdThreads, sizeof(VecFwdSmem<DK_, DVS>), p.stream>>>(                        \
             q, k, v, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, p.dv, h0, o, o_f32, hT, states, slots, \
-            p.st);                                                                                  \
+            p.st, order);                                                                           \
     } while (0)
     const bool st = o == nullptr;   // states pass only
     if (p.dk == 64) {
@@ -607,7 +609,7 @@ cudaError_t launch_vec_fwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
 cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *a,
                            const __nv_bfloat16 *states, const float *dhT, float *dq, float *dk, float *dv,
-                           float *da, float *dh0)
+                           float *da, float *dh0, const int32_t *order)
 {
     if (p.n_docs <= 0)
         return cudaSuccess;
@@ -621,7 +623,7 @@ cudaError_t launch_vec_bwd(const Problem &p, const __nv_bfloat16 *q, const __nv_
             return err;                                                                             \
         kern<<<grid, kVecBwdThreads, sizeof(VecBwdSmem<DK_, DV_>), p.stream>>>(                        \
             q, k, v, dO, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, states, slots, dhT, dq, dk, dv, da, \
-            dh0, p.st);                                                                             \
+            dh0, p.st, order);                                                                      \
     } while (0)
     if (p.dk == 64 && p.dv == 64)
         BDLA_VEC_BWD(64, 64);
