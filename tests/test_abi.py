@@ -152,3 +152,44 @@ def test_segment_plan_with_the_largest_document_count(L):
 def test_package_exports():
     for name in ("fwd", "bwd", "decay", "Workspace", "BdlaError"):
         assert hasattr(pkg, name)
+
+
+def test_variant_workspace_and_tile_states_sizes(L):
+    """Per-channel / delta-rule calls: the state before every 16-token tile
+    takes H x (tokens/16 + documents + 1) bf16 dk x dv matrices; packed calls
+    with several documents also keep the documents' launch order (one int32
+    each) in the workspace; the backward's workspace adds its own states."""
+    D = bdla.Dims(1, 65536, 32, 128, 128)
+    slots = 65536 // 16 + 8 + 1
+    assert L.bdla_tile_states_bytes(D, 8) == 32 * slots * 128 * 128 * 2
+    assert L.bdla_tile_states_bytes(bdla.Dims(2, 100, 3, 64, 64), 0) == 3 * (200 // 16 + 2 + 1) * 64 * 64 * 2
+    assert L.bdla_tile_states_bytes(bdla.Dims(1, 16, 2, 128, 256), 0) == 0       # dv 256 unsupported here
+    for ws_fn in (L.bdla_workspace_bytes_vec, L.bdla_workspace_bytes_delta):
+        f_packed = ws_fn(bdla.OP_FWD, D, 8)
+        f_one = ws_fn(bdla.OP_FWD, D, 1)
+        f_fixed = ws_fn(bdla.OP_FWD, bdla.Dims(8, 8192, 32, 128, 128), 0)
+        assert f_packed > f_one == f_fixed                 # the order region (8 documents)
+        b_packed = ws_fn(bdla.OP_BWD, D, 8)
+        assert b_packed - f_packed >= L.bdla_tile_states_bytes(D, 8)
+
+
+def test_variant_host_validation(L):
+    """The per-channel and delta-rule entry points refuse bad arguments on the
+    host (nothing below reaches a kernel)."""
+    E = bdla
+    Dm = bdla.Dims(1, 64, 2, 64, 64)
+    st = L.bdla_fwd_vec(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 0, None, FAKE, 0, None,
+                        ctypes.c_void_p((1 << 20) + 8), Dm, 0, FAKE, 1 << 40, None)
+    assert st == E.ERR_ALIGN                                   # misaligned states
+    st = L.bdla_fwd_delta(FAKE, FAKE, FAKE, FAKE, None, -5.0, 16, None, 0, None, FAKE, 0, None, None, Dm, 0,
+                          FAKE, 1 << 40, None)
+    assert st == E.ERR_NULL                                    # beta missing
+    st = L.bdla_bwd_delta(FAKE, FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 0, None, FAKE, None, None, FAKE, FAKE,
+                          FAKE, FAKE, None, None, Dm, 0, FAKE, 1 << 40, None)
+    assert st == E.ERR_NULL                                    # dbeta missing
+    st = L.bdla_fwd_delta(FAKE, FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 0, None, FAKE, 0, None, None,
+                          bdla.Dims(1, 64, 2, 64, 256), 0, FAKE, 1 << 40, None)
+    assert st == E.ERR_UNSUPPORTED                             # dv 256
+    st = L.bdla_fwd_vec(FAKE, FAKE, FAKE, FAKE, -5.0, 16, None, 0, None, FAKE, 0, None, None, Dm, 0, FAKE, 16,
+                        None)
+    assert st == E.ERR_WORKSPACE

@@ -47,3 +47,23 @@ def test_algorithmic_bytes_of_the_measured_workload():
     assert got["fwd"] == th * per_fwd + 2 * units * state
     assert got["bwd"] == th * per_bwd + units * state
     assert got["bwd"] == 5402263552
+
+
+def test_algorithmic_bytes_with_fp32_checkpoints():
+    """The 256K stage as its config asks (fp32 state every 16 tokens): the
+    forward also writes the 128-token block starts, the expansion kernel the
+    7 inner states of every block (reading k, v and the tile cumsums once),
+    and the backward reads one checkpoint per block."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunked_linear_attention_bounded_gb300.inputs import WORKLOADS
+    w = WORKLOADS["c256k"]
+    th = 262144 * 16
+    blocks = 262144 // 128 * 16
+    state = 128 * 256 * 4
+    got = bench.algorithmic_bytes(w, 1)
+    assert got["states"] == th * (2 * 128 + 2 * 256 + 4) + blocks * 7 * state
+    assert got["states"] == 33302773760
+    plain = bench.algorithmic_bytes(WORKLOADS["c8k"], 4)
+    assert "states" not in plain
+    assert got["fwd"] - blocks * state == th * (2 * 128 * 2 + 2 * 256 + 4 + 2 * 256) + 16 * state
