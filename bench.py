@@ -133,6 +133,18 @@ def measured_traffic(kernel: str, workload: str):
     return entry[0]
 
 
+def traffic_source(kernel: str, workload: str):
+    """Where `traffic` comes from: a stored ncu capture, valid only for the
+    kernel source it was taken on."""
+    entry = NCU_TRAFFIC.get((kernel, workload))
+    if entry is None:
+        return "no ncu capture for this kernel and workload"
+    if kernel_digest(kernel) != entry[1]:
+        return f"ncu capture of source digest {entry[1]}; the source has changed since (digest {kernel_digest(kernel)})"
+    return (f"ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of kernel source digest "
+            f"{entry[1]}, not measured in this run")
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -469,6 +481,7 @@ def ours_arm(args, w, inp):
                "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
                             "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
                             "traffic": measured_traffic(dom, w.name),
+                            "traffic_source": traffic_source(dom, w.name),
                             "algorithmic_bytes_per_launch": ab[dom]},
                "kernel_ms": kernel_ms,
                "kernel_roofline": per_kernel,
@@ -678,6 +691,7 @@ def decode_arm(args):
            "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
                         "unit": "GB/s", "frac": achieved / hbm, "peak_source": hbm_src,
                         "traffic": measured_traffic("decode", "decode"),
+                        "traffic_source": traffic_source("decode", "decode"),
                         "algorithmic_bytes_per_launch": step_bytes},
            "gpu_launches": K, "clocks": clk.summary()}
     print(json.dumps(out), flush=True)
