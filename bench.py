@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true",
                     help="skip the 1M-token bounded-vs-ablation comparison")
+    ap.add_argument("--variant", choices=["vec", "delta"], default=None,
+                    help="run the workload's shape with one decay per key channel or as the gated delta rule")
     ap.add_argument("--ckpt-stride", type=int, default=None,
                     help="fp32 state checkpoints every N tokens (overrides the workload's own)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -713,6 +715,9 @@ def main():
         w = dataclasses.replace(w, fwd_only=False)
     if args.ckpt_stride is not None:
         w = dataclasses.replace(w, ckpt_stride=args.ckpt_stride)
+    if args.variant is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_{args.variant}", vec=args.variant == "vec",
+                                delta=args.variant == "delta", ckpt_stride=0)
     if args.impl == "ours":
         from chunked_linear_attention_bounded_gb300.replicas import rank_workload
         w = rank_workload(w, rank)
