@@ -55,6 +55,32 @@ struct DeltaFwdSmem {
     float G[kT], eG[kT], beta[kT];
 };
 
+// 4 / 8 consecutive bf16 of a shared row as floats, by one 8- / 16-byte load
+// (a bf16 is the upper half of the fp32 with the same bits).
+__device__ __forceinline__ void ld_bf4(const __nv_bfloat16 *p, float (&x)[4])
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void ld_bf8(const __nv_bfloat16 *p, float (&x)[8])
+{
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
 // C[16][16] (ld LS) = A B^T for two [16][DK] bf16 tiles (ld LK); one warp.
 template <int DK, int LK, int LS>
 __device__ __forceinline__ void gram16(float *C, const __nv_bfloat16 *A, const __nv_bfloat16 *B)
@@ -211,22 +237,33 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             }
         }
         __syncthreads();
-        // ---- W = T diag(e^{Gamma}) K (bf16 operand), U = T V (fp32, into Dl)
-        for (int e = tid; e < kT * DK; e += kDT) {
-            const int t = e / DK, i = e % DK;
-            float acc = 0.0f;
+        // ---- W = T diag(e^{Gamma}) K (bf16 operand), U = T V (fp32, into Dl); 4
+        //      columns per item, T lower-triangular (s <= t)
+        for (int e = tid; e < kT * DK / 4; e += kDT) {
+            const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int s = 0; s <= t; ++s) {
+                const float c = sm.Tm[t * LS + s] * sm.eG[s];
+                float x[4];
+                ld_bf4(sm.K + s * LK + i4, x);
 #pragma unroll
-            for (int s = 0; s < kT; ++s)
-                acc += sm.Tm[t * LS + s] * sm.eG[s] * __bfloat162float(sm.K[s * LK + i]);
-            sm.Wb[t * LK + i] = __float2bfloat16_rn(acc);
+                for (int y = 0; y < 4; ++y)
+                    acc[y] += c * x[y];
+            }
+            *reinterpret_cast<uint2 *>(sm.Wb + t * LK + i4) = make_uint2(pack2_bf16(acc[0], acc[1]), pack2_bf16(acc[2], acc[3]));
         }
-        for (int e = tid; e < kT * kDvs; e += kDT) {
-            const int t = e / kDvs, j = e % kDvs;
-            float acc = 0.0f;
+        for (int e = tid; e < kT * kDvs / 4; e += kDT) {
+            const int t = e / (kDvs / 4), j4 = (e % (kDvs / 4)) * 4;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int s = 0; s <= t; ++s) {
+                const float c = sm.Tm[t * LS + s];
+                float x[4];
+                ld_bf4(sm.V + s * LV + j4, x);
 #pragma unroll
-            for (int s = 0; s < kT; ++s)
-                acc += sm.Tm[t * LS + s] * __bfloat162float(sm.V[s * LV + j]);
-            sm.Dl[t * LF + j] = acc;
+                for (int y = 0; y < 4; ++y)
+                    acc[y] += c * x[y];
+            }
+            *reinterpret_cast<float4 *>(sm.Dl + t * LF + j4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         __syncthreads();
         // ---- W S_0
@@ -258,9 +295,10 @@ delta_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                 out[x] = eg * sm.QS[t * LF + c8 + x];
             for (int s = 0; s <= t; ++s) {
                 const float p = sm.QK[t * LS + s];
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    out[x] += p * sm.Dl[s * LF + c8 + x];
+                const float4 d0 = *reinterpret_cast<const float4 *>(sm.Dl + s * LF + c8);
+                const float4 d1 = *reinterpret_cast<const float4 *>(sm.Dl + s * LF + c8 + 4);
+                out[0] += p * d0.x; out[1] += p * d0.y; out[2] += p * d0.z; out[3] += p * d0.w;
+                out[4] += p * d1.x; out[5] += p * d1.y; out[6] += p * d1.z; out[7] += p * d1.w;
             }
             if (t < nv) {
                 const size_t off = ((size_t)(t0 + t) * H + h) * dv + j0 + c8;
@@ -532,22 +570,33 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             sm.eGdO[t * LV + j] = __float2bfloat16_rn(sm.eG[t] * __bfloat162float(sm.dO[t * LV + j]));
         }
         __syncthreads();
-        // ---- P4: W = T diag(e^Gamma) K (bf16), U = T V (fp32)
-        for (int e = tid; e < kT * DK; e += kBT) {
-            const int t = e / DK, i = e % DK;
-            float acc = 0.0f;
+        // ---- P4: W = T diag(e^Gamma) K (bf16), U = T V (fp32); 4 columns per item,
+        //      T lower-triangular (s <= t)
+        for (int e = tid; e < kT * DK / 4; e += kBT) {
+            const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int s = 0; s <= t; ++s) {
+                const float c = sm.Tm[t * LS + s] * sm.eG[s];
+                float x[4];
+                ld_bf4(sm.K + s * LK + i4, x);
 #pragma unroll
-            for (int s = 0; s < kT; ++s)
-                acc += sm.Tm[t * LS + s] * sm.eG[s] * __bfloat162float(sm.K[s * LK + i]);
-            sm.Wb[t * LK + i] = __float2bfloat16_rn(acc);
+                for (int y = 0; y < 4; ++y)
+                    acc[y] += c * x[y];
+            }
+            *reinterpret_cast<uint2 *>(sm.Wb + t * LK + i4) = make_uint2(pack2_bf16(acc[0], acc[1]), pack2_bf16(acc[2], acc[3]));
         }
-        for (int e = tid; e < kT * DV; e += kBT) {
-            const int t = e / DV, j = e % DV;
-            float acc = 0.0f;
+        for (int e = tid; e < kT * DV / 4; e += kBT) {
+            const int t = e / (DV / 4), j4 = (e % (DV / 4)) * 4;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int s = 0; s <= t; ++s) {
+                const float c = sm.Tm[t * LS + s];
+                float x[4];
+                ld_bf4(sm.V + s * LV + j4, x);
 #pragma unroll
-            for (int s = 0; s < kT; ++s)
-                acc += sm.Tm[t * LS + s] * __bfloat162float(sm.V[s * LV + j]);
-            sm.B1[t * LW + j] = acc;
+                for (int y = 0; y < 4; ++y)
+                    acc[y] += c * x[y];
+            }
+            *reinterpret_cast<float4 *>(sm.B1 + t * LW + j4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         __syncthreads();
         // ---- P5: W S_0
@@ -586,26 +635,37 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
             wmma::store_matrix_sync(C + 16 * ni, acc, LW, wmma::mem_row_major);
         }
         __syncthreads();
-        // ---- P8: dP, dT (two adjacent lanes per (t, s), each half of the sums), dv
-        static_assert(2 * kT * kT == kBT, "two lanes per pair, every thread");
-        if (tid < 2 * kT * kT) {
-            const int item = tid >> 1, part = tid & 1;
-            const int t = item / kT, s = item % kT;
-            float acc = 0.0f;
-            if (s <= t)
-                for (int j = part; j < DV; j += 2)
-                    acc += __bfloat162float(sm.dO[t * LV + j]) * sm.B1[s * LW + j];
-            float dt = 0.0f;
-            for (int j = part; j < DV; j += 2)
-                dt += sm.B4[t * LW + j] * __bfloat162float(sm.V[s * LV + j]);
-            float dw = 0.0f;
-            for (int i = part; i < DK; i += 2)
-                dw += sm.B3[t * LW + i] * __bfloat162float(sm.K[s * LK + i]);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            dt += __shfl_xor_sync(0xffffffffu, dt, 1);
-            dw += __shfl_xor_sync(0xffffffffu, dw, 1);
+        // ---- P8: dP, dT: warp t, lane (s, part): the two lanes s and s + 16 take
+        //      alternate 4-column chunks of the sums (a quarter warp then reads 8
+        //      different rows in 8 different bank groups); dv below
+        static_assert(NW == kT, "one warp per row t");
+        {
+            const int t = warp, s = lane & 15, part = lane >> 4;
+            float acc = 0.0f, dt = 0.0f, dw = 0.0f;
+#pragma unroll 4
+            for (int m = 0; m < DV / 8; ++m) {
+                const int j = 8 * m + 4 * part;
+                float o4[4], v4[4];
+                ld_bf4(sm.dO + t * LV + j, o4);
+                ld_bf4(sm.V + s * LV + j, v4);
+                const float4 d4 = *reinterpret_cast<const float4 *>(sm.B1 + s * LW + j);
+                const float4 g4 = *reinterpret_cast<const float4 *>(sm.B4 + t * LW + j);
+                acc += o4[0] * d4.x + o4[1] * d4.y + o4[2] * d4.z + o4[3] * d4.w;
+                dt += g4.x * v4[0] + g4.y * v4[1] + g4.z * v4[2] + g4.w * v4[3];
+            }
+#pragma unroll 4
+            for (int m = 0; m < DK / 8; ++m) {
+                const int i = 8 * m + 4 * part;
+                float k4[4];
+                ld_bf4(sm.K + s * LK + i, k4);
+                const float4 w4 = *reinterpret_cast<const float4 *>(sm.B3 + t * LW + i);
+                dw += w4.x * k4[0] + w4.y * k4[1] + w4.z * k4[2] + w4.w * k4[3];
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+            dt += __shfl_xor_sync(0xffffffffu, dt, 16);
+            dw += __shfl_xor_sync(0xffffffffu, dw, 16);
             if (part == 0) {
-                sm.dP[t * LS + s] = acc;
+                sm.dP[t * LS + s] = s <= t ? acc : 0.0f;
                 sm.X[t * LS + s] = dt + sm.eG[s] * dw;
             }
         }
@@ -692,19 +752,24 @@ delta_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
                     const float da_ts = s < t ? sm.beta[t] * sm.dL[t * LS + s] * sm.E[t * LS + s] : 0.0f;
                     const float da_st = t < s ? sm.beta[s] * sm.dL[s * LS + t] * sm.E[s * LS + t] : 0.0f;
                     const float ck = da_ts + da_st;
+                    float ks[8], qs[8];
+                    ld_bf8(sm.K + s * LK + c8, ks);
+                    ld_bf8(sm.Q + s * LK + c8, qs);
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
-                        const float ks = __bfloat162float(sm.K[s * LK + c8 + x]);
-                        gq[x] += dpe_ts * ks;
-                        gk[x] += dpe_st * __bfloat162float(sm.Q[s * LK + c8 + x]) + ck * ks;
+                        gq[x] += dpe_ts * ks[x];
+                        gk[x] += dpe_st * qs[x] + ck * ks[x];
                     }
                 }
                 float pm = 0.0f, pw = 0.0f;
+                {
+                    float kt[8];
+                    ld_bf8(sm.K + t * LK + c8, kt);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float kt = __bfloat162float(sm.K[t * LK + c8 + x]);
-                    pm += sm.B3[t * LW + c8 + x] * kt;
-                    pw += sm.B5[t * LW + c8 + x] * kt;
+                    for (int x = 0; x < 8; ++x) {
+                        pm += sm.B3[t * LW + c8 + x] * kt[x];
+                        pw += sm.B5[t * LW + c8 + x] * kt[x];
+                    }
                 }
 #pragma unroll
                 for (int off = 1; off < IPR; off <<= 1) {
