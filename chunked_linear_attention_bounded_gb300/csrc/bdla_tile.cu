@@ -249,8 +249,8 @@ ckpt_expand_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__r
     if (__syncthreads_or(!ok)) {
         if (tid == 0)
             set_status(st, BDLA_ERR_TIMEOUT, (unsigned)blockIdx.x);
-        if (!ok)
-            sm100::mbar_wait(&sm.bar, 0, wait_ns);   // let the copies land before the CTA leaves
+        if (!ok)   // let the copies land before the CTA leaves (full limit, whatever the trigger's)
+            sm100::mbar_wait(&sm.bar, 0, kDefaultWaitNs);
         return;
     }
     // weight the keys in place: k_t o w_t
