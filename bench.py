@@ -109,7 +109,7 @@ def algorithmic_bytes(w, n_seq):
 NCU_TRAFFIC = {
     ("fwd", "varlen64k"): (1643861504 + 1054696704, "02db1295df326daf"),
     ("bwd", "varlen64k"): (2717015296 + 3181785600, "9d70b7adbb7c6ece"),
-    ("decode", "decode"): (543210000 + 478080000, "243a14f8e322bc2c"),
+    ("decode", "decode"): (543212800 + 478050816, "d1cbdc04a87dd7bc"),
 }
 KERNEL_SOURCES = {
     "fwd": ("bdla_fwd_sm100.cu", "bdla_sm100.cuh", "bdla_common.cuh"),
