@@ -68,46 +68,65 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16 *dst, int ld, const __nv
     }
 }
 
-// Channel pass of a tile: thread i < DK walks the 16 tokens of channel i
-// (the tile's 16 logits of the channel are loaded before any is used).
-// Writes Qt, Kt, Kh (bf16, in place over the raw q, k where given), the
-// tile-local Gamma and d lambda / d a (both optional) and g = e^{gamma}.
-// Rows past nv have lambda = 0 and zero q, k, so they change nothing.
-template <int DK>
+// Channel pass of a tile: NT / DK threads per channel (adjacent lanes), each
+// taking a run of the 16 tokens; their partial cumulative sums are joined by a
+// warp scan of width NT / DK.  Writes Qt, Kt, Kh (bf16, in place over the raw
+// q, k where given), the tile-local Gamma, d lambda / d a and gamma (all
+// optional) and g = e^{gamma}.  Rows past nv have lambda = 0 and zero q, k, so they
+// change nothing.  Every thread of the block takes part.
+template <int DK, int NT>
 __device__ __forceinline__ void channel_pass(const float *__restrict__ a, int64_t t0, int nv, int H, int h, float b,
                                              int mode, __nv_bfloat16 *Qt, __nv_bfloat16 *Kt, __nv_bfloat16 *Kh,
-                                             float *gam_out, float *g, float *dlam_out = nullptr)
+                                             float *gam_out, float *g, float *dlam_out = nullptr,
+                                             float *gam_total = nullptr)
 {
     constexpr int LK = padb(DK);
-    const int i = threadIdx.x;
-    if (i >= DK)
-        return;
-    float av[kT];
+    constexpr int PARTS = NT / DK;       // threads per channel
+    constexpr int TPP = kT / PARTS;      // tokens per thread
+    static_assert(NT % DK == 0 && kT % PARTS == 0 && 32 % PARTS == 0, "channel split");
+    const int i = threadIdx.x / PARTS, part = threadIdx.x % PARTS;
+    const int tb = part * TPP;           // first token of this thread's run
+    float av[TPP];
 #pragma unroll
-    for (int t = 0; t < kT; ++t)
-        av[t] = t < nv ? a[((t0 + t) * H + h) * (int64_t)DK + i] : 0.0f;
-    float G[kT];
+    for (int x = 0; x < TPP; ++x)
+        av[x] = tb + x < nv ? a[((t0 + tb + x) * H + h) * (int64_t)DK + i] : 0.0f;
+    float G[TPP];
     float run = 0.0f;
 #pragma unroll
-    for (int t = 0; t < kT; ++t) {
-        const float lam = t < nv ? log_decay(av[t], b, mode) : 0.0f;
-        run += lam;
-        G[t] = run;
+    for (int x = 0; x < TPP; ++x) {
+        const bool in = tb + x < nv;
+        run += in ? log_decay(av[x], b, mode) : 0.0f;
+        G[x] = run;
         if (dlam_out != nullptr)
-            dlam_out[t * DK + i] = t < nv ? log_decay_deriv(av[t], b, mode) : 0.0f;
+            dlam_out[(tb + x) * DK + i] = in ? log_decay_deriv(av[x], b, mode) : 0.0f;
     }
-    const float gam = run;
+    // exclusive prefix of the earlier runs of this channel, and the channel's total
+    float incl = run;
 #pragma unroll
-    for (int t = 0; t < kT; ++t) {
+    for (int off = 1; off < PARTS; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off, PARTS);
+        if (part >= off)
+            incl += y;
+    }
+    const float before = incl - run;
+    const float gam = __shfl_sync(0xffffffffu, incl, PARTS - 1, PARTS);
+#pragma unroll
+    for (int x = 0; x < TPP; ++x) {
+        const int t = tb + x;
+        const float Gt = before + G[x];
         const float kr = __bfloat162float(Kt[t * LK + i]);
         if (Qt != nullptr)
-            Qt[t * LK + i] = __float2bfloat16_rn(__bfloat162float(Qt[t * LK + i]) * expf(G[t]));
-        Kt[t * LK + i] = __float2bfloat16_rn(kr * expf(-G[t]));
-        Kh[t * LK + i] = __float2bfloat16_rn(kr * expf(gam - G[t]));
+            Qt[t * LK + i] = __float2bfloat16_rn(__bfloat162float(Qt[t * LK + i]) * expf(Gt));
+        Kt[t * LK + i] = __float2bfloat16_rn(kr * expf(-Gt));
+        Kh[t * LK + i] = __float2bfloat16_rn(kr * expf(gam - Gt));
         if (gam_out != nullptr)
-            gam_out[t * DK + i] = G[t];
+            gam_out[t * DK + i] = Gt;
     }
-    g[i] = expf(gam);
+    if (part == 0) {
+        g[i] = expf(gam);
+        if (gam_total != nullptr)
+            gam_total[i] = gam;
+    }
 }
 
 // S32 <- diag(g) S32 + Kh^T V (fp32 master), then S16 <- bf16(S32).
@@ -202,7 +221,7 @@ vec_fwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         load_rows(sm.Kt, LK, k, t0, nv, H, h, DK, 0, DK);
         load_rows(sm.V, LV, v, t0, nv, H, h, dv, j0, DV);
         __syncthreads();
-        channel_pass<DK>(a, t0, nv, H, h, b, mode, STATES ? nullptr : sm.Qt, sm.Kt, sm.Kh, nullptr, sm.g);
+        channel_pass<DK, kVecFwdThreads>(a, t0, nv, H, h, b, mode, STATES ? nullptr : sm.Qt, sm.Kt, sm.Kh, nullptr, sm.g);
         __syncthreads();
         if (!STATES) {
             if (warp == 0) {   // diagonal tile: A = Qt Kt^T
@@ -378,9 +397,7 @@ vec_bwd_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             sm.Kt[x] = sm.Kr[x];
         }
         __syncthreads();
-        channel_pass<DK>(a, t0, nv, H, h, b, mode, sm.Qt, sm.Kt, sm.Kh, sm.Gm, sm.g, sm.Dl);
-        if (tid < DK)
-            sm.gam[tid] = sm.Gm[(kT - 1) * DK + tid];
+        channel_pass<DK, kVecBwdThreads>(a, t0, nv, H, h, b, mode, sm.Qt, sm.Kt, sm.Kh, sm.Gm, sm.g, sm.Dl, sm.gam);
         __syncthreads();
         // ---- scores: A = Qt Kt^T (warp 0), dA = dO V^T (warp 1)
         if (warp < 2) {
