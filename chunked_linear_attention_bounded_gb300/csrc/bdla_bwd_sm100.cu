@@ -108,11 +108,11 @@ struct BwdSmem {
     float gq[BT];                  // Gamma per row (ablation diagonal path)
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
-    uint64_t full_in, free_in, z_ready, m1_done, ea_done, mb_done, eb_done, md_done, ee_done,
-        mf_done, acc_free, drain, full_z, z_free;
-    uint64_t never;
+    uint64_t full_in, free_in, z_ready, m1a_done, m1b_done, ea_done, mb_done, eb_done, md_done, ee_done,
+        mf_done, acc_free_c1, acc_free_c2, acc_free_c3, drain, full_z, z_free;
+    uint64_t never;       // nothing arrives here: the wait of the stall test hook
     uint64_t wait_ns;     // limit of the pipeline waits
-    int stall_at[3];      // test hook: block at which producer / MMA / epilogue stall (-1: never)   // nothing arrives here: the wait of the stall test hook
+    int stall_at[3];      // test hook: block at which producer / MMA / epilogue stall (-1: never)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -317,14 +317,17 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.full_in, 1);
         mbar_init(&sm.free_in, 1);
         mbar_init(&sm.z_ready, kEpiThreads);
-        mbar_init(&sm.m1_done, 1);
+        mbar_init(&sm.m1a_done, 1);
+        mbar_init(&sm.m1b_done, 1);
         mbar_init(&sm.ea_done, kEpiThreads);
         mbar_init(&sm.mb_done, 1);
         mbar_init(&sm.eb_done, kEpiThreads);
         mbar_init(&sm.md_done, 1);
         mbar_init(&sm.ee_done, kEpiThreads);
         mbar_init(&sm.mf_done, 1);
-        mbar_init(&sm.acc_free, kEpiThreads);
+        mbar_init(&sm.acc_free_c1, kEpiThreads);
+        mbar_init(&sm.acc_free_c2, kEpiThreads);
+        mbar_init(&sm.acc_free_c3, kEpiThreads);
         mbar_init(&sm.drain, 1);
         mbar_init(&sm.full_z, 1);
         mbar_init(&sm.z_free, 1);
@@ -432,21 +435,34 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const uint32_t par = jj & 1;
                 // (test hook: the stalling MMA warp waits on `never` instead of full_in)
                 const bool sm_ = jj == sm.stall_at[1];
+                // M1 accumulator by accumulator, each as soon as the previous
+                // block's outputs have been read out of it (dv, then dk, then dq)
                 if (*abort_flag || !mbar_wait_lim(sm_ ? &sm.never : &sm.full_in, sm_ ? 0u : par, &sm.wait_ns) ||
-                    // S_in: straight from its TMA load, or once the epilogue converted it
-                    !mbar_wait_lim(st_tma ? &sm.full_z : &sm.z_ready, par, &sm.wait_ns) ||
-                    (jj > 0 && !mbar_wait_lim(&sm.acc_free, (jj - 1) & 1, &sm.wait_ns))) {
+                    (jj > 0 && !mbar_wait_lim(&sm.acc_free_c2, (jj - 1) & 1, &sm.wait_ns))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < DV / 16; ++ks)
+                    umma_bf16(t_c2, kmaj(sdo, ks), kmaj(sv, ks), id_ss, ks > 0);
+                if (jj > 0 && !mbar_wait_lim(&sm.acc_free_c1, (jj - 1) & 1, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks)
                     umma_bf16(t_c1, kmaj(sq, ks), kmaj(sk, ks), id_ss, ks > 0);
-                for (int ks = 0; ks < DV / 16; ++ks) {
-                    umma_bf16(t_c2, kmaj(sdo, ks), kmaj(sv, ks), id_ss, ks > 0);
-                    umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
+                umma_commit(&sm.m1a_done);
+                // S_in: straight from its TMA load, or once the epilogue converted it
+                if (!mbar_wait_lim(st_tma ? &sm.full_z : &sm.z_ready, par, &sm.wait_ns) ||
+                    (jj > 0 && !mbar_wait_lim(&sm.acc_free_c3, (jj - 1) & 1, &sm.wait_ns))) {
+                    ok = false;
+                    break;
                 }
-                umma_commit(&sm.m1_done);
+                tc_fence_after();
+                for (int ks = 0; ks < DV / 16; ++ks)
+                    umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
+                umma_commit(&sm.m1b_done);
                 if (!mbar_wait_lim(&sm.ea_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
@@ -529,9 +545,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int64_t t_w = d.start + (int64_t)pend_j * BT + 32 * q4;
             const int n_valid = (int)(d.len - ((int64_t)pend_j * BT + 32 * q4));
             const bool full_blk = d.len - (int64_t)pend_j * BT >= BT;
+            // each accumulator is released to the next block's M1 once this
+            // thread has read its last panel of it (dv, dk, then dq)
+            bool c2_freed = false, c1_freed = false;
             if (DV == 128 && out_tma && full_blk && blockIdx.z == 0) {
-                // fp32 panels (32 columns) written by TMA stores.  Items: dq
-                // panels, then dk panels, then dv panels.  The first n_a items
+                // fp32 panels (32 columns) written by TMA stores.  Items: dv
+                // panels, then dk panels, then dq panels.  The first n_a items
                 // go two per round (one per column half) staged alternately in
                 // z and x; the last four one per round (each half staging 16
                 // of its columns) alternately in x's two panels, so that z is
@@ -543,20 +562,21 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const int rounds = n_a / 2 + 4;
                 const int t0s = (int)(d.start + (int64_t)pend_j * BT);
                 auto item_col = [&](int it, int &coord, const CUtensorMap *&map) -> uint32_t {
-                    if (it < dk / 32) {
-                        coord = it * 32;
-                        map = &tdq;
-                        return t_c3 + it * 32;
+                    if (it < DV / 32) {
+                        coord = j0 + it * 32;
+                        map = &tdv;
+                        return t_c2 + it * 32;
                     }
-                    if (it < 2 * (dk / 32)) {
-                        coord = (it - dk / 32) * 32;
+                    if (it < DV / 32 + dk / 32) {
+                        coord = (it - DV / 32) * 32;
                         map = &tdk;
-                        return t_c1 + (it - dk / 32) * 32;
+                        return t_c1 + (it - DV / 32) * 32;
                     }
-                    coord = j0 + (it - 2 * (dk / 32)) * 32;
-                    map = &tdv;
-                    return t_c2 + (it - 2 * (dk / 32)) * 32;
+                    coord = (it - DV / 32 - dk / 32) * 32;
+                    map = &tdq;
+                    return t_c3 + (it - DV / 32 - dk / 32) * 32;
                 };
+                const int c2_last = DV / 32 - 1, c1_last = DV / 32 + dk / 32 - 1;
                 const int ka = n_a / 2;                  // two-item rounds
                 for (int k = 0; k < rounds; ++k) {
                     const bool pair = k < ka;
@@ -591,6 +611,19 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         for (int k4 = 0; k4 < 4; ++k4)
                             *reinterpret_cast<uint4 *>(buf + sw128_offset(r, 4 * half + k4)) =
                                 make_uint4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                    }
+                    {   // every item up to `read` has been read out of tensor memory by its reader
+                        const int read = pair ? 2 * k + 1 : n_a + (k - ka);
+                        if (!c2_freed && read >= c2_last) {
+                            tc_fence_before();
+                            mbar_arrive(&sm.acc_free_c2);
+                            c2_freed = true;
+                        }
+                        if (!c1_freed && read >= c1_last) {
+                            tc_fence_before();
+                            mbar_arrive(&sm.acc_free_c1);
+                            c1_freed = true;
+                        }
                     }
                     fence_proxy_async_smem();
                     epi_sync();
@@ -677,7 +710,11 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     mbar_arrive(&sm.z_free);   // the producer may load the next state into z
             }
             tc_fence_before();
-            mbar_arrive(&sm.acc_free);
+            if (!c2_freed)
+                mbar_arrive(&sm.acc_free_c2);
+            if (!c1_freed)
+                mbar_arrive(&sm.acc_free_c1);
+            mbar_arrive(&sm.acc_free_c3);
             // its decay gradient is summed up later, off the path to the next EA
             da_pend = true;
             da_valid = valid;
@@ -800,9 +837,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (warp == 2 && lane == 0)
                 tma_store_wait_read();
             {
-                // (test hook: the stalling epilogue waits on `never` instead of m1_done)
+                // (test hook: the stalling epilogue waits on `never` instead of m1a_done)
                 const bool se = jj == sm.stall_at[2];
-                ok = epi_all(mbar_wait_lim(se ? &sm.never : &sm.m1_done, se ? 0u : par, &sm.wait_ns)) && !*abort_flag;
+                ok = epi_all(mbar_wait_lim(se ? &sm.never : &sm.m1a_done, se ? 0u : par, &sm.wait_ns)) && !*abort_flag;
             }
             if (!ok)
                 break;
@@ -908,6 +945,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
             }
             sm.rowpart[bp][half][r] = rowsum;
+            // the C3 GEMM of M1 (dO S_in^T) reads S_in from z: it has completed
+            // before E overwrites z (and before C3 is scaled below)
+            ok = epi_all(mbar_wait_lim(&sm.m1b_done, par, &sm.wait_ns)) && !*abort_flag;
+            if (!ok)
+                break;
+            tc_fence_after();
             // E in one pass: <S_in, E> with the S_in row in z (bf16 checkpoints),
             // then the bf16 copy of E over it (z) and E <- e^{Lam_end} E in
             // tensor memory (read only by Mf, after ea_done)
