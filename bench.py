@@ -108,7 +108,7 @@ def algorithmic_bytes(w, n_seq):
 # source is unchanged; null otherwise.
 NCU_TRAFFIC = {
     ("fwd", "varlen64k"): (1643861504 + 1054696704, "02db1295df326daf"),
-    ("bwd", "varlen64k"): (2717015296 + 3181785600, "9d70b7adbb7c6ece"),
+    ("bwd", "varlen64k"): (2716321536 + 3181181952, "310b8baff6035a1a"),
     ("decode", "decode"): (543212800 + 478050816, "d1cbdc04a87dd7bc"),
 }
 KERNEL_SOURCES = {
