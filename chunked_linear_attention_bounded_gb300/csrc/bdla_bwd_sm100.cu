@@ -108,7 +108,8 @@ struct BwdSmem {
     float gq[BT];                  // Gamma per row (ablation diagonal path)
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
-    uint64_t full_in, free_in, z_ready, m1a_done, m1b_done, ea_done, mb_done, eb_done, md_done, ee_done,
+    uint64_t full_in, free_in, z_ready, m1a_done, m1b_done, p_ready, ea_done, mb_done, dp_ready, eb_done, md_done,
+        ee_done,
         mf_done, acc_free_c1, acc_free_c2, acc_free_c3, drain, full_z, z_free;
     uint64_t never;       // nothing arrives here: the wait of the stall test hook
     uint64_t wait_ns;     // limit of the pipeline waits
@@ -319,8 +320,10 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.z_ready, kEpiThreads);
         mbar_init(&sm.m1a_done, 1);
         mbar_init(&sm.m1b_done, 1);
+        mbar_init(&sm.p_ready, kEpiThreads);
         mbar_init(&sm.ea_done, kEpiThreads);
         mbar_init(&sm.mb_done, 1);
+        mbar_init(&sm.dp_ready, kEpiThreads);
         mbar_init(&sm.eb_done, kEpiThreads);
         mbar_init(&sm.md_done, 1);
         mbar_init(&sm.ee_done, kEpiThreads);
@@ -463,25 +466,37 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int ks = 0; ks < DV / 16; ++ks)
                     umma_bf16(t_c3, kmaj(sdo, ks), kmaj(sz, ks), id_dqs, ks > 0);
                 umma_commit(&sm.m1b_done);
-                if (!mbar_wait_lim(&sm.ea_done, par, &sm.wait_ns)) {
+                // Mb: P^T dO as soon as P is in x (and C2 read), V E^T once EA is done
+                if (!mbar_wait_lim(&sm.p_ready, par, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int ks = 0; ks < BT / 16; ++ks)
                     umma_bf16(t_c2, mnmaj(sx, ks), mnmaj(sdo, ks), id_pdo, ks > 0);
+                if (!mbar_wait_lim(&sm.ea_done, par, &sm.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 for (int ks = 0; ks < DV / 16; ++ks)
                     umma_bf16(t_c1, kmaj(sv, ks), kmaj(sz, ks), id_ve, ks > 0);
                 umma_commit(&sm.mb_done);
+                // Md: dP K as soon as dP is in x, dP^T Q once C1 has been rescaled
+                if (!mbar_wait_lim(&sm.dp_ready, par, &sm.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_c3, kmaj(sx, ks), mnmaj(sk, ks), id_dpk, 1);
                 if (!mbar_wait_lim(&sm.eb_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int ks = 0; ks < BT / 16; ++ks) {
+                for (int ks = 0; ks < BT / 16; ++ks)
                     umma_bf16(t_c1, mnmaj(sx, ks), mnmaj(sq, ks), id_dpq, 1);
-                    umma_bf16(t_c3, kmaj(sx, ks), mnmaj(sk, ks), id_dpk, 1);
-                }
                 umma_commit(&sm.md_done);
                 if (!mbar_wait_lim(&sm.ee_done, par, &sm.wait_ns)) {
                     ok = false;
@@ -945,6 +960,10 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         make_uint4(u[4 * k4], u[4 * k4 + 1], u[4 * k4 + 2], u[4 * k4 + 3]);
             }
             sm.rowpart[bp][half][r] = rowsum;
+            // P is in x and C2 (dO V^T) has been read: Mb's P^T dO may start
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.p_ready);
             // the C3 GEMM of M1 (dO S_in^T) reads S_in from z: it has completed
             // before E overwrites z (and before C3 is scaled below)
             ok = epi_all(mbar_wait_lim(&sm.m1b_done, par, &sm.wait_ns)) && !*abort_flag;
@@ -1026,12 +1045,25 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             sm.ypart[bp][half][r] = yv;
             tmem_st_wait();   // visible to Md and Mf through the fence before eb_done
 
-            // ---- Eb: C1 <- w_s o C1 (the inter-block part of dk), k . dk_inter,
-            //      then dP -> smem
+            // ---- Eb: dP -> smem (then Md's dP K may start), C1 <- w_s o C1 (the
+            //      inter-block part of dk) and k . dk_inter
             ok = epi_all(mbar_wait_lim(&sm.mb_done, par, &sm.wait_ns)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
+                const int cc = c >> 1;
+                unsigned char *xp = sm.x + (c >> 1) * kPanel;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
+                        make_uint4(dpk[cc * 16 + 4 * k4], dpk[cc * 16 + 4 * k4 + 1],
+                                   dpk[cc * 16 + 4 * k4 + 2], dpk[cc * 16 + 4 * k4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.dp_ready);
             float kd = 0.0f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) if ((c & 1) == half && c * 32 < dk) {
@@ -1055,16 +1087,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tmem_st32(t_c1 + lane_off + c * 32, x);
             }
             sm.kdpart[bp][half][r] = kd * wsc;
-#pragma unroll
-            for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
-                const int cc = c >> 1;
-                unsigned char *xp = sm.x + (c >> 1) * kPanel;
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                    *reinterpret_cast<uint4 *>(xp + sw128_offset(r, (c & 1) * 4 + k4)) =
-                        make_uint4(dpk[cc * 16 + 4 * k4], dpk[cc * 16 + 4 * k4 + 1],
-                                   dpk[cc * 16 + 4 * k4 + 2], dpk[cc * 16 + 4 * k4 + 3]);
-            }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
