@@ -24,18 +24,21 @@
 // S_in (the state before the block) comes from forward checkpoints.
 //
 // Phases of one block (MMA warp <-> eight epilogue warps, two per TMEM lane
-// quarter splitting the columns):
-//   M1  C1 = Q K^T, C2 = dO V^T, C3 = dO S_in^T
+// quarter splitting the columns).  Each GEMM is issued as soon as its operands
+// and its accumulator are ready, in this order:
+//   M1  C2 = dO V^T, C1 = Q K^T, C3 = dO S_in^T (each once the previous
+//       block's output in that accumulator has been read out)
 //   EA  P (smem) and dP (registers), W row sums, E -> bf16 copy;
-//       then, while Mb runs, E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
-//   Mb  C2 = P^T dO, C1 = V E^T
-//   Eb  C1 <- w_s o C1, k . dk_inter, dP -> smem; then, while Md runs,
-//       dO -> e^{Lam} o dO, the W column sums v . (P^T dO) and K o w_s into
-//       V's tile (V is not read again in the block; when dv < dk it does
-//       not hold K, and K is scaled in place once Md has read it)
-//   Md  C1 += dP^T Q, C3 += dP K
-//   Mf  C2 += (K o w_s) E, E += Q^T (e^{Lam} o dO)
-//   Eg  dq = C3, dk = C1, dv = C2, da      (overlaps the next block's loads)
+//       E <- e^{Lam_end} E, C3 <- e^{Lam_t} C3 and Y
+//   Mb  C2 = P^T dO (once P is in smem), C1 = V E^T (after EA)
+//   Eb  dO -> e^{Lam} o dO, dP -> smem, C1 <- w_s o C1, k . dk_inter; then,
+//       while Md runs, the W column sums v . (P^T dO) and K o w_s into V's
+//       tile (V is not read again in the block; when dv < dk it does not
+//       hold K, and K is scaled in place once Md has read it)
+//   Mf1 E += Q^T (e^{Lam} o dO)        (once dO is rescaled)
+//   Md  C3 += dP K (once dP is in smem), C1 += dP^T Q (after Eb)
+//   Mf2 C2 += (K o w_s) E              (after the column sums)
+//   Eg  dv = C2, dk = C1, dq = C3, da  (overlaps the next block's loads)
 #include <cudaTypedefs.h>
 
 #include "bdla_internal.h"
@@ -109,8 +112,7 @@ struct BwdSmem {
     float dgp[BT][kChunk + 1];     // ablation: diagonal-tile P, computed pair by pair
     float dgd[BT][kChunk + 1];     // ablation: diagonal-tile dP
     uint64_t full_in, free_in, z_ready, m1a_done, m1b_done, p_ready, ea_done, mb_done, dp_ready, eb_done, md_done,
-        ee_done,
-        mf_done, acc_free_c1, acc_free_c2, acc_free_c3, drain, full_z, z_free;
+        do_ready, ee_done, mf_done, acc_free_c1, acc_free_c2, acc_free_c3, drain, full_z, z_free;
     uint64_t never;       // nothing arrives here: the wait of the stall test hook
     uint64_t wait_ns;     // limit of the pipeline waits
     int stall_at[3];      // test hook: block at which producer / MMA / epilogue stall (-1: never)
@@ -326,6 +328,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&sm.dp_ready, kEpiThreads);
         mbar_init(&sm.eb_done, kEpiThreads);
         mbar_init(&sm.md_done, 1);
+        mbar_init(&sm.do_ready, kEpiThreads);
         mbar_init(&sm.ee_done, kEpiThreads);
         mbar_init(&sm.mf_done, 1);
         mbar_init(&sm.acc_free_c1, kEpiThreads);
@@ -482,6 +485,14 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int ks = 0; ks < DV / 16; ++ks)
                     umma_bf16(t_c1, kmaj(sv, ks), kmaj(sz, ks), id_ve, ks > 0);
                 umma_commit(&sm.mb_done);
+                // Mf's first GEMM, Q^T (e^{Lam} o dO) into E, as soon as dO is rescaled
+                if (!mbar_wait_lim(&sm.do_ready, par, &sm.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    umma_bf16(t_e, mnmaj(sq, ks), mnmaj(sdo, ks), id_qdo, 1);
                 // Md: dP K as soon as dP is in x, dP^T Q once C1 has been rescaled
                 if (!mbar_wait_lim(&sm.dp_ready, par, &sm.wait_ns)) {
                     ok = false;
@@ -498,6 +509,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int ks = 0; ks < BT / 16; ++ks)
                     umma_bf16(t_c1, mnmaj(sx, ks), mnmaj(sq, ks), id_dpq, 1);
                 umma_commit(&sm.md_done);
+                // Mf: K o w_s E into C2 once K o w_s is written and the column
+                // sums are read
                 if (!mbar_wait_lim(&sm.ee_done, par, &sm.wait_ns)) {
                     ok = false;
                     break;
@@ -505,8 +518,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tc_fence_after();
                 for (int ks = 0; ks < dk / 16; ++ks)
                     umma_bf16(t_c2, kmaj(khat_v ? sv : sk, ks), mnmaj(sz, ks), id_ke, 1);
-                for (int ks = 0; ks < BT / 16; ++ks)
-                    umma_bf16(t_e, mnmaj(sq, ks), mnmaj(sdo, ks), id_qdo, 1);
                 umma_commit(&sm.mf_done);
                 umma_commit(&sm.free_in);
             }
@@ -1045,12 +1056,23 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             sm.ypart[bp][half][r] = yv;
             tmem_st_wait();   // visible to Md and Mf through the fence before eb_done
 
-            // ---- Eb: dP -> smem (then Md's dP K may start), C1 <- w_s o C1 (the
+            // ---- Eb: dO -> e^{Lam} o dO (then Mf's Q^T dO may start: Mb has read
+            //      dO), dP -> smem (then Md's dP K may start), C1 <- w_s o C1 (the
             //      inter-block part of dk) and k . dk_inter
             ok = epi_all(mbar_wait_lim(&sm.mb_done, par, &sm.wait_ns)) && !*abort_flag;
             if (!ok)
                 break;
             tc_fence_after();
+#pragma unroll
+            for (int p = 0; p < DV / 64; ++p)
+#pragma unroll
+                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
+                    uint4 *oa = reinterpret_cast<uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
+                    *oa = scale_bf16x8(*oa, qsc);
+                }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.do_ready);
 #pragma unroll
             for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
                 const int cc = c >> 1;
@@ -1091,15 +1113,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sm.eb_done);
-            // ---- while Md runs (it reads neither dO nor E): dO -> e^{Lam} o dO for Mf
-#pragma unroll
-            for (int p = 0; p < DV / 64; ++p)
-#pragma unroll
-                for (int c8 = 4 * half; c8 < 4 * half + 4; ++c8) {
-                    uint4 *oa = reinterpret_cast<uint4 *>(sm.dO + p * kPanel + sw128_offset(r, c8));
-                    *oa = scale_bf16x8(*oa, qsc);
-                }
-            // and the column sums of W: v_s . (P^T dO)_s (C2 and V stay untouched until Mf)
+            // ---- while Md runs: the column sums of W: v_s . (P^T dO)_s (C2 and V stay untouched until Mf)
             {
                 float vc = 0.0f;
 #pragma unroll
