@@ -54,7 +54,7 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-    size_t gamma = 0;    // Gamma [H, tokens] fp32
+    size_t gamma = 0;    // Gamma [H, tokens] fp32 (kernels that read it from memory)
     size_t dfac = 0;     // d lambda / d a [H, tokens] fp32 (backward)
     size_t states = 0;   // recomputed bf16 states for the backward, 0 if unused
     size_t part = 0;     // partial dq, dk, da of the second dv slice (dv = 256)
@@ -154,7 +154,7 @@ Problem make_problem(const bdla_dims &d, const int32_t *cu, int n_docs, float b,
     } while (0)
 
 // Segment plan of a call with its buffers carved from the workspace.
-// (The order array is filled by launch_doc_order for packed calls.)
+// (The order array is filled by launch_doc_check for packed calls.)
 SegPlan seg_of(const bdla_dims &d, int n_docs, bool varlen, const Layout &L, void *ws)
 {
     SegPlan sp = plan_of(d, n_docs);
@@ -209,10 +209,12 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
                             (int64_t)total_tokens(d) / kBlock + (varlen ? n_docs : d.B) <= INT32_MAX;
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     {
+        // the forward kernel takes Gamma from the logits itself; the segment
+        // summaries and the in-block checkpoint passes read it from memory
         KernelMark mark_(BDLA_KERNEL_DECAY, p.stream);
-        BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
-        if (seg.order)
-            BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
+        BDLA_CUDA(launch_doc_check(p, const_cast<int32_t *>(seg.order)));
+        if (seg.seg_blk > 0 || (ckpt && !fused_ckpt))
+            BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     }
     if (seg.seg_blk > 0) {
         // the state entering every segment
@@ -224,7 +226,7 @@ bdla_status fwd_impl(const void *q, const void *k, const void *v, const float *a
     }
     {
         KernelMark mark_(BDLA_KERNEL_FWD, p.stream);
-        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, o, o_dtype == BDLA_F32, hT,
+        BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, a, h0, o, o_dtype == BDLA_F32, hT,
                                    (fused_ckpt || split_ckpt) ? ckpt : nullptr, ckpt_dtype == BDLA_BF16,
                                    ckpt_stride, seg));
     }
@@ -279,10 +281,11 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     const auto *dob = static_cast<const __nv_bfloat16 *>(dO);
     const SegPlan seg = seg_of(d, p.n_docs, varlen, L, ws);
     {
+        // Gamma and d lambda / d a for the backward and the segment
+        // summaries (the forward of the states pass forms Gamma itself)
         KernelMark mark_(BDLA_KERNEL_DECAY, p.stream);
+        BDLA_CUDA(launch_doc_check(p, const_cast<int32_t *>(seg.order)));
         BDLA_CUDA(launch_decay(p, a, gamma, dfac));
-        if (seg.order)
-            BDLA_CUDA(launch_doc_order(p, const_cast<int32_t *>(seg.order)));
     }
     const void *states = ckpt;
     int st_bf16 = ck_bf16, st_stride = stride;
@@ -297,7 +300,7 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
         }
         {
         KernelMark mark_(BDLA_KERNEL_STATES, p.stream);
-            BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, gamma, h0, nullptr, 0, nullptr, stb, 1, kBlock, seg));
+            BDLA_CUDA(launch_fwd_sm100(p, qb, kb, vb, a, h0, nullptr, 0, nullptr, stb, 1, kBlock, seg));
         }
         states = stb;
         st_bf16 = 1;
@@ -348,6 +351,7 @@ bdla_status bdla_decay(const float *a, float b, int chunk, const int32_t *cu_seq
     dd.dk = 64;
     dd.dv = 64;
     Problem p = make_problem(dd, cu_seqlens, n_docs, b, mode, ws, stream);
+    BDLA_CUDA(launch_doc_check(p, nullptr));
     BDLA_CUDA(launch_decay(p, a, gamma, nullptr));
     return BDLA_OK;
 }
@@ -421,7 +425,7 @@ const char *bdla_status_string(bdla_status s)
     case BDLA_ERR_CUDA: return "a CUDA runtime call failed";
     case BDLA_ERR_TIMEOUT: return "device: a bounded wait expired";
     case BDLA_ERR_DEVICE: return "device: malformed cu_seqlens or another device-side check";
-    case BDLA_ERR_TOO_LARGE: return "problem larger than the fixed scratch of bdla_fwd_noalloc";
+    case BDLA_ERR_TOO_LARGE: return "more tokens than bdla_fwd_noalloc addresses (2^31 - 1)";
     }
     return "unknown status";
 }
@@ -482,16 +486,19 @@ size_t variant_order_bytes(bool varlen, int n_docs)
     return (varlen && n_docs > 1 && n_docs <= kMaxOrderedDocs) ? round_up((size_t)n_docs * 4) : 0;
 }
 
-// The documents longest first in the workspace's order region (packed calls
-// with several documents), else nullptr: one small kernel on the stream.
+// Packed calls: cu_seqlens checked on the device, and the documents longest
+// first in the workspace's order region (2 .. kMaxOrderedDocs documents),
+// else nullptr: one small kernel on the stream.
 cudaError_t variant_order(const Problem &p, void *ws, bool varlen, const int32_t **order)
 {
     *order = nullptr;
-    if (variant_order_bytes(varlen, p.n_docs) == 0)
+    if (!varlen)
         return cudaSuccess;
-    auto *o = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + round_up(kStatusBytes));
+    int32_t *o = nullptr;
+    if (variant_order_bytes(varlen, p.n_docs) != 0)
+        o = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + round_up(kStatusBytes));
     *order = o;
-    return launch_doc_order(p, o);
+    return launch_doc_check(p, o);
 }
 
 size_t vec_layout(int op, const bdla_dims &d, int n_docs, size_t *states_off, bool varlen = false)

@@ -49,6 +49,23 @@ __device__ __forceinline__ float log_decay_deriv(float a, float b, int mode)
     return -sigmoidf_(a);
 }
 
+// Gamma of one token: the inclusive sum of the log-decays up to it inside its
+// 16-token tile.  Lane l of a full warp holds position (l & 15) of a tile
+// (lanes 0-15 one tile, 16-31 the next) and passes its lambda (0 past the
+// end of the document: positions past the end never enter an earlier
+// position's sum).  Every kernel takes Gamma from this four-step shuffle
+// scan, so all of them see bitwise the same Gamma for the same logits.
+__device__ __forceinline__ float tile_gamma(float lam, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < kChunk; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, lam, off, kChunk);
+        if ((lane & (kChunk - 1)) >= off)
+            lam += y;
+    }
+    return lam;
+}
+
 // Document [start, end) of document n: packed offsets or fixed length T.
 struct DocSpan {
     int64_t start;

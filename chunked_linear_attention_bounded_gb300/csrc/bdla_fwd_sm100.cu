@@ -117,7 +117,7 @@ template <int DV, bool ABL, bool STATES>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tck,
-                 int ck_tma, const float *__restrict__ gamma,
+                 int ck_tma, const float *__restrict__ a, float b, int mode,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const float *__restrict__ h0, void *__restrict__ o, int o_f32,
                  float *__restrict__ hT, void *__restrict__ ckpt, int ck_bf16, int ckpt_stride,
@@ -392,18 +392,20 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         };
 
         bool ok = true;
-        // Gamma of the first block; later blocks are fetched one block ahead
-        float g_next = (nblk > 0 && r < d.len) ? gamma[(int64_t)h * tokens + d.start + r] : 0.0f;
+        // logits of the first block; later blocks are fetched one block ahead
+        float a_next = (nblk > 0 && r < d.len) ? a[(d.start + r) * H + h] : 0.0f;
         for (int j = 0; j < nblk; ++j) {
             const int s = j & 1;
             const int Lb = (int)(d.len - (int64_t)j * BT < BT ? d.len - (int64_t)j * BT : BT);
             const bool valid = r < Lb;
             const int tau = r >> 4;
-            // ---- decay scalars of this block
-            const float g = g_next;
+            // ---- decay scalars of this block: Gamma from the logits
+            // (the state-only pass serves both decay modes; the others are ABL-specific)
+            const int md = STATES ? mode : (ABL ? BDLA_DECAY_NEG_SOFTPLUS : BDLA_DECAY_BOUNDED_SIGMOID);
+            const float g = tile_gamma(valid ? log_decay(a_next, b, md) : 0.0f, lane);
             if (j + 1 < nblk) {
                 const int64_t tn = (int64_t)(j + 1) * BT + r;
-                g_next = tn < d.len ? gamma[(int64_t)h * tokens + d.start + tn] : 0.0f;
+                a_next = tn < d.len ? a[(d.start + tn) * H + h] : 0.0f;
             }
             const int last = min(16 * tau + 15, Lb - 1);
             const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
@@ -730,7 +732,7 @@ bool make_state_map(CUtensorMap *map, const void *ptr, int dk, int dv, int64_t n
 template <int DV, bool ABL, bool STATES>
 static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                       const CUtensorMap &mv, const CUtensorMap &mck, int ck_tma,
-                                      const float *gamma, const float *h0,
+                                      const float *a, const float *h0,
                                       void *o, int o_f32, float *hT, void *ckpt, int ck_bf16,
                                       int ckpt_stride, const SegPlan &seg)
 {
@@ -742,7 +744,7 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
     const int64_t n_slots = ckpt ? ckpt_slots(p, ckpt_stride) : 0;
     dim3 grid(p.dv / DV, p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs);
     const WaitCfg wc = wait_cfg(STATES ? BDLA_KERNEL_STATES : BDLA_KERNEL_FWD);
-    kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, gamma, p.cu, p.T, p.tokens, p.H, p.dk,
+    kern<<<grid, kFwdThreads, smem, p.stream>>>(mq, mk, mv, mck, ck_tma, a, p.b, p.mode, p.cu, p.T, p.tokens, p.H, p.dk,
                                                 p.dv, h0, o, o_f32, hT, ckpt, ck_bf16, ckpt_stride,
                                                 n_slots, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st,
                                                 wc.ns, wc.stall);
@@ -750,7 +752,7 @@ static cudaError_t launch_fwd_sm100_t(const Problem &p, const CUtensorMap &mq, c
 }
 
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
+                             const __nv_bfloat16 *v, const float *a, const float *h0, void *o,
                              int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride,
                              const SegPlan &seg)
 {
@@ -781,7 +783,7 @@ cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __n
         ck_tma = 1;
     }
 #define BDLA_FWD_GO(DV_, ABL_, ST_)                                                                 \
-    return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, mck, ck_tma, gamma, h0, o, o_f32, hT,  \
+    return launch_fwd_sm100_t<DV_, ABL_, ST_>(p, mq, mk, mv, mck, ck_tma, a, h0, o, o_f32, hT,      \
                                               ckpt, ck_bf16, ckpt_stride, seg)
     if (states_only) {
         if (p.dv == 64)

@@ -53,7 +53,10 @@ struct SegPlan {
 // Documents of packed calls with at most this many documents are taken
 // longest first.
 constexpr int kMaxOrderedDocs = 4096;
-cudaError_t launch_doc_order(const Problem &p, int32_t *order);
+// Packed calls: checks cu_seqlens on the device (a bad offset is reported as
+// BDLA_ERR_DEVICE) and, with `order` given and several documents, writes the
+// documents by decreasing length into it.  Nothing for fixed-length calls.
+cudaError_t launch_doc_check(const Problem &p, int32_t *order);
 
 // Chooses the segment length for a problem: a fixed length set through
 // bdla_set_seq_split, never (split < 0), or, by default, a cut into about
@@ -141,8 +144,9 @@ cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const _
 // checkpoints whose stride divides 128.
 // o == nullptr runs the state chain only (checkpoints for the backward).
 // With segments, seg.buf holds each segment's initial state (seg_scan).
+// Gamma comes from the logits `a` ([tokens][H]) inside the kernel.
 cudaError_t launch_fwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                             const __nv_bfloat16 *v, const float *gamma, const float *h0, void *o,
+                             const __nv_bfloat16 *v, const float *a, const float *h0, void *o,
                              int o_f32, float *hT, void *ckpt, int ck_bf16, int ckpt_stride,
                              const SegPlan &seg);
 
@@ -162,6 +166,7 @@ cudaError_t launch_seg_scan(const Problem &p, const float *init, bool backward, 
 // block: checkpoints whose stride divides 128, fp32 or bf16.  For dv = 256
 // the value columns are split in two slices; `part` (bwd_partial_floats
 // floats of workspace) receives the second slice's partial dq, dk, da.
+// Gamma and d lambda / d a ([H][tokens]) come from the decay kernel.
 size_t bwd_partial_floats(const Problem &p);
 cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,

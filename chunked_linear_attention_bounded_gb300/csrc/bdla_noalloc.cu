@@ -4,15 +4,15 @@
 // runs where cudaMalloc is forbidden or unavailable (inside a custom
 // allocator's own callbacks, a runtime that hands out only fixed, pre-planned
 // buffers for inputs and outputs, or a framework layer that must not touch
-// the allocator on this path).  bdla_fwd_noalloc serves them: the per-token
-// decay scratch (Gamma) and the device status word live in file-scope
-// __device__ arrays of this library, so the caller passes only inputs and
-// outputs.  The price is a fixed maximum problem size and a shared scratch.
+// the allocator on this path).  bdla_fwd_noalloc serves them: the forward
+// kernel forms the decay cumsum from the logits itself, and the device status
+// word lives in a file-scope __device__ variable of this library, so the
+// caller passes only inputs and outputs.
 //
-// The arrays are part of the library's device image: every GPU that loads
-// the library holds them (8 MiB + 256 B) until the process exits.  The
-// status word keeps the first device-side error of any call (it starts at
-// zero with the image) until bdla_noalloc_read_status reads and clears it.
+// The status word is part of the library's device image: every GPU that
+// loads the library holds it (256 B) until the process exits.  It keeps the
+// first device-side error of any call (it starts at zero with the image)
+// until bdla_noalloc_read_status reads and clears it.
 #include <mutex>
 
 #include "bdla_internal.h"
@@ -21,22 +21,17 @@ namespace bdla {
 
 namespace {
 
-// Gamma for at most this many (token, head) pairs: 8 MiB of fp32.
-constexpr size_t kNoAllocMaxTokenHeads = (size_t)1 << 21;
-
-__device__ __align__(256) float g_noalloc_gamma[kNoAllocMaxTokenHeads];
 __device__ __align__(256) DeviceStatus g_noalloc_status;
 
 constexpr int kMaxDevices = 64;
 struct NoAllocPtrs {
-    float *gamma = nullptr;
     DeviceStatus *status = nullptr;
 };
 NoAllocPtrs g_noalloc_ptrs[kMaxDevices];
 std::mutex g_noalloc_mu;
 
-// Device addresses of the two arrays on the current device, looked up once
-// per device (the host-side names are stand-ins, not device addresses).
+// Device address of the status word on the current device, looked up once
+// per device (the host-side name is a stand-in, not a device address).
 bdla_status noalloc_setup(NoAllocPtrs &out)
 {
     int dev = 0;
@@ -44,13 +39,10 @@ bdla_status noalloc_setup(NoAllocPtrs &out)
         return BDLA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     NoAllocPtrs &p = g_noalloc_ptrs[dev];
-    if (p.gamma == nullptr) {
-        void *g = nullptr, *s = nullptr;
-        if (cudaGetSymbolAddress(&g, g_noalloc_gamma) != cudaSuccess)
-            return BDLA_ERR_CUDA;
+    if (p.status == nullptr) {
+        void *s = nullptr;
         if (cudaGetSymbolAddress(&s, g_noalloc_status) != cudaSuccess)
             return BDLA_ERR_CUDA;
-        p.gamma = static_cast<float *>(g);
         p.status = static_cast<DeviceStatus *>(s);
     }
     out = p;
@@ -73,9 +65,9 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
         return s;
     if ((s = check_decay(b, chunk, mode)) != BDLA_OK)
         return s;
-    // B * T * H (token, head) pairs, compared without forming the product
+    // token coordinates of the kernels' tensor copies are 32-bit
     const int64_t tokens = (int64_t)d.B * d.T;
-    if (tokens > (int64_t)(kNoAllocMaxTokenHeads / (size_t)d.H))
+    if (tokens > (int64_t)INT32_MAX)
         return BDLA_ERR_TOO_LARGE;
     if (tokens > 0 && (!q || !k || !v || !a || !o))
         return BDLA_ERR_NULL;
@@ -103,11 +95,9 @@ extern "C" bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void
     // bdla_noalloc_read_status reads and clears it
     p.st = ptrs.status;
     p.stream = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_decay(p, a, ptrs.gamma, nullptr) != cudaSuccess)
-        return BDLA_ERR_CUDA;
     if (launch_fwd_sm100(p, static_cast<const __nv_bfloat16 *>(q),
                          static_cast<const __nv_bfloat16 *>(k),
-                         static_cast<const __nv_bfloat16 *>(v), ptrs.gamma, h0, o,
+                         static_cast<const __nv_bfloat16 *>(v), a, h0, o,
                          o_dtype == BDLA_F32, hT, nullptr, 0, 0, SegPlan{}) != cudaSuccess)
         return BDLA_ERR_CUDA;
     return BDLA_OK;

@@ -75,7 +75,7 @@ typedef enum {
     BDLA_ERR_CUDA = 8,         /* a CUDA runtime call (launch, attribute) failed */
     BDLA_ERR_TIMEOUT = 9,      /* device: a bounded wait gave up */
     BDLA_ERR_DEVICE = 10,      /* device: malformed cu_seqlens or another device check */
-    BDLA_ERR_TOO_LARGE = 11    /* bdla_fwd_noalloc: problem larger than its fixed scratch */
+    BDLA_ERR_TOO_LARGE = 11    /* bdla_fwd_noalloc: more than 2^31 - 1 tokens (B * T) */
 } bdla_status;
 
 typedef enum {
@@ -191,18 +191,17 @@ bdla_status bdla_decode(const void *q, const void *k, const void *v, const float
  * callers, such as code running inside an allocator's callbacks or a runtime
  * that only hands out fixed buffers for inputs and outputs, which must not
  * call cudaMalloc.  Same operation and argument meaning as bdla_fwd for
- * fixed-length batches, without checkpoints.  Its scratch (the per-token
- * decay cumsum for at most 2^21 (token, head) pairs, i.e. B*T*H <= 2097152,
- * and a device status word) is a fixed array inside the library that every
- * GPU loading the library holds (about 8 MiB) until exit; larger problems
- * return BDLA_ERR_TOO_LARGE before any launch.  It calls no cudaMalloc or
- * cudaFree.  The first call on each device looks up the array's device
- * address; make that first call before any stream capture.  Every call
- * shares the one array: calls that overlap on the GPU (different streams
- * without ordering) race and give wrong results; order them.  Device-side
- * errors (a bounded wait that expired) are recorded in the library's own
- * status word, which keeps the first error until bdla_noalloc_read_status
- * reads and clears it.  Sizes are checked as for bdla_fwd (B <= 65535).
+ * fixed-length batches, without checkpoints.  The kernel forms the decay
+ * cumsum from the logits itself, so the only scratch is a device status word,
+ * a fixed variable inside the library that every GPU loading the library
+ * holds (256 B) until exit.  It calls no cudaMalloc or cudaFree.  The first
+ * call on each device looks up the word's device address; make that first
+ * call before any stream capture.  Device-side errors (a bounded wait that
+ * expired) are recorded in that word, which keeps the first error of any
+ * call until bdla_noalloc_read_status reads and clears it.  Sizes are
+ * checked as for bdla_fwd (B <= 65535), and B * T above 2^31 - 1 (the
+ * kernels' 32-bit token coordinates) returns BDLA_ERR_TOO_LARGE before any
+ * launch.
  */
 bdla_status bdla_fwd_noalloc(const void *q, const void *k, const void *v, const float *a,
                              float b, int chunk, const float *h0, void *o, bdla_dtype o_dtype,

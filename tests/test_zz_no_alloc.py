@@ -1,12 +1,12 @@
 """bdla_fwd_noalloc: the forward entry point for callers that cannot allocate
 device memory (for example code running inside an allocator's callbacks, or
 a runtime that only provides fixed buffers for inputs and outputs).  Its
-scratch is a fixed array inside the library, so these tests check that two
-calls in a row, on different inputs, each match the ordinary bdla_fwd (which
-takes a caller workspace) and the fp64 oracle within the parity tolerance,
-that each call leaves no device-side error in the library's status word
-(read through bdla_noalloc_read_status), and that problems beyond the fixed
-scratch or the grid limits are refused before any launch.
+only scratch is a status word inside the library, so these tests check that
+two calls in a row, on different inputs, each match the ordinary bdla_fwd
+(which takes a caller workspace) and the fp64 oracle within the parity
+tolerance, that each call leaves no device-side error in the library's status
+word (read through bdla_noalloc_read_status), and that problems beyond the
+token coordinates or the grid limits are refused before any launch.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it passes alone and after the other tests."""
@@ -65,7 +65,7 @@ def test_noalloc_forward_matches_bdla_fwd_and_oracle_on_two_calls_in_a_row():
         assert_close(f"hT[call {i}] vs oracle", gpu_to_ref_layout("hT", hT), ref["hT"])
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch_or_the_grid():
+def test_noalloc_refuses_problems_beyond_its_token_coordinates_or_the_grid():
     # Every pointer below is fake and never dereferenced: each call is
     # rejected by a host-side check before any launch (no GPU needed).
     fake = ctypes.c_void_p(1 << 20)
@@ -74,13 +74,13 @@ def test_noalloc_refuses_problems_beyond_its_scratch_or_the_grid():
     def call(dims):
         return L.bdla_fwd_noalloc(fake, fake, fake, fake, -5.0, 16, None, fake, 0, None, dims, 0, None)
 
-    # 2^21 (token, head) pairs is the limit
-    st = call(bdla.Dims(1, (1 << 21) // 4 + 16, 4, 128, 128))
+    # B * T = 2^31 tokens is one more than the 32-bit token coordinates address
+    st = call(bdla.Dims(2, 1 << 30, 1, 128, 128))
     assert st == bdla.ERR_TOO_LARGE
-    assert "fixed scratch" in bdla.status_string(st)
+    assert "2^31 - 1" in bdla.status_string(st)
     # B * T * H = 2^15 * 2^30 * 2^19 wraps to 0 in 64-bit arithmetic; refused all the same
     assert call(bdla.Dims(1 << 15, 1 << 30, 1 << 19, 128, 128)) == bdla.ERR_TOO_LARGE
     assert call(bdla.Dims(1 << 15, (1 << 31) - 1, 1 << 19, 128, 128)) == bdla.ERR_TOO_LARGE
-    # more documents than a grid extent holds, although small enough for the scratch
+    # more documents than a grid extent holds
     assert call(bdla.Dims(65536, 1, 1, 64, 64)) == bdla.ERR_UNSUPPORTED
     assert call(bdla.Dims(1, 64, 2, 256, 64)) == bdla.ERR_UNSUPPORTED
