@@ -96,7 +96,9 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
     if (op == BDLA_OP_BWD) {
         L.dfac = off;
         off += per_head * d.H;
-        if (!bwd_ckpt_usable(ckpt_stride)) {
+        // bf16 block states: recomputed, or converted from fp32 checkpoints
+        // inside the blocks (strides below 128 are fp32 only)
+        if (!bwd_ckpt_usable(ckpt_stride) || ckpt_stride < kBlock) {
             L.states = off;
             const int64_t slots = (tokens + kBlock - 1) / kBlock + n_docs;
             off += round_up((size_t)d.H * slots * d.dk * d.dv * 2);
@@ -306,6 +308,14 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
         st_bf16 = 1;
         st_stride = kBlock;
     }
+    // fp32 checkpoints inside the blocks: the backward reads bf16 copies of
+    // the block-start states, converted below, by TMA
+    const bool convert = bwd_ckpt_usable(stride) && !ck_bf16 && stride < kBlock;
+    if (convert) {
+        states = wsb + L.states;
+        st_bf16 = 1;
+        st_stride = kBlock;
+    }
     if (seg.seg_blk > 0) {
         // the adjoint entering every segment from its end
         {
@@ -317,6 +327,9 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
     float *part = L.part ? reinterpret_cast<float *>(wsb + L.part) : nullptr;
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
+        if (convert)
+            BDLA_CUDA(launch_states_bf16(p, static_cast<const float *>(ckpt), stride,
+                                         reinterpret_cast<__nv_bfloat16 *>(wsb + L.states)));
         BDLA_CUDA(launch_bwd_sm100(p, qb, kb, vb, dob, gamma, dfac, states, st_bf16, st_stride, dhT, dq,
                                    dk, dv, da, dh0, part, seg));
     }

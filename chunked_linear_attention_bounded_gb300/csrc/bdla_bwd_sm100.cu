@@ -266,7 +266,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const __grid_constant__ CUtensorMap tst, int st_tma,
                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
-                 const __grid_constant__ CUtensorMap tdv, int out_tma,
+                 const __grid_constant__ CUtensorMap tdv, const __grid_constant__ CUtensorMap tdq1,
+                 const __grid_constant__ CUtensorMap tdk1, int out_tma,
                  const float *__restrict__ gamma, const float *__restrict__ dfac,
                  const int32_t *__restrict__ cu, int T, int64_t tokens, int H, int dk, int dv,
                  const void *__restrict__ states, int st_bf16, int st_stride, int64_t n_slots,
@@ -285,6 +286,10 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     float *dq = blockIdx.z == 0 ? dq_base : part + (size_t)(blockIdx.z - 1) * (2 * part_qk + part_a);
     float *dkk = blockIdx.z == 0 ? dk_base : dq + part_qk;
     float *da = blockIdx.z == 0 ? da_base : dq + 2 * part_qk;
+    // TMA maps of this slice's dq and dk (slice 1: its partial sums), formed
+    // where a store needs them
+#define BDLA_MAP_DQ (blockIdx.z == 0 ? &tdq : &tdq1)
+#define BDLA_MAP_DK (blockIdx.z == 0 ? &tdk : &tdk1)
     // one document, or one segment of it (then the adjoint after its last
     // token comes from seg_init)
     const SegSpan span = seg_span(cu, T, tokens, n_docs,
@@ -574,7 +579,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // each accumulator is released to the next block's M1 once this
             // thread has read its last panel of it (dv, dk, then dq)
             bool c2_freed = false, c1_freed = false;
-            if (DV == 128 && out_tma && full_blk && blockIdx.z == 0) {
+            if (DV == 128 && out_tma && full_blk && blockIdx.z <= 1) {
                 // fp32 panels (32 columns) written by TMA stores.  Items: dv
                 // panels, then dk panels, then dq panels.  The first n_a items
                 // go two per round (one per column half) staged alternately in
@@ -595,11 +600,11 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                     if (it < DV / 32 + dk / 32) {
                         coord = (it - DV / 32) * 32;
-                        map = &tdk;
+                        map = BDLA_MAP_DK;
                         return t_c1 + (it - DV / 32) * 32;
                     }
                     coord = (it - DV / 32 - dk / 32) * 32;
-                    map = &tdq;
+                    map = BDLA_MAP_DQ;
                     return t_c3 + (it - DV / 32 - dk / 32) * 32;
                 };
                 const int c2_last = DV / 32 - 1, c1_last = DV / 32 + dk / 32 - 1;
@@ -668,7 +673,7 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                     epi_sync();   // that round's buffers may be staged again
                 }
-            } else if (out_tma && full_blk && blockIdx.z == 0) {
+            } else if (out_tma && full_blk && blockIdx.z <= 1) {
                 // fp32 panels (32 columns) staged in z + x and written by TMA stores:
                 // item i < dk/32: dq panel i; next dk/32: dk panels; then dv panels
                 constexpr int kStagePanels = DV / 64 + 2;
@@ -698,9 +703,9 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         for (int pi = 0; pi < kStagePanels && base + pi < n_items; ++pi) {
                             const int it = base + pi;
                             if (it < dk / 32)
-                                tma_store_3d(&tdq, sm.z + pi * kPanel, it * 32, h, t0s);
+                                tma_store_3d(BDLA_MAP_DQ, sm.z + pi * kPanel, it * 32, h, t0s);
                             else if (it < 2 * (dk / 32))
-                                tma_store_3d(&tdk, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
+                                tma_store_3d(BDLA_MAP_DK, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
                             else
                                 tma_store_3d(&tdv, sm.z + pi * kPanel, j0 + (it - 2 * (dk / 32)) * 32, h, t0s);
                         }
@@ -1203,6 +1208,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     if (warp == 1)
         tmem_dealloc(tmem, 512);
 }
+#undef BDLA_MAP_DQ
+#undef BDLA_MAP_DK
 
 // dq += partial dq of the other dv slices (and dk, da).
 __global__ void add_partials_kernel(float *__restrict__ dq, float *__restrict__ dk,
@@ -1245,8 +1252,14 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
     const int slices = p.dv / DV;
     const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
     dim3 grid(p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs, slices);
+    // the second slice's partial dq and dk leave by TMA stores as well
+    CUtensorMap mdq1 = mdq, mdk1 = mdk;
+    int otma = out_tma;
+    if (slices > 1 && otma &&
+        (!make_grad_map(&mdq1, part, p.dk, p.H, p.tokens) || !make_grad_map(&mdk1, part + n_qk, p.dk, p.H, p.tokens)))
+        otma = 0;
     const WaitCfg wc = wait_cfg(BDLA_KERNEL_BWD);
-    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, out_tma,
+    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, mdq1, mdk1, otma,
                                                 gamma, dfac, p.cu, p.T,
                                                 p.tokens, p.H,
                                                 p.dk, p.dv, states, st_bf16, st_stride,

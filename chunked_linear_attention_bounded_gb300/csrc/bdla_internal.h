@@ -139,6 +139,10 @@ cudaError_t launch_fwd_tile(const Problem &p, const __nv_bfloat16 *q, const __nv
 cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                const float *gamma, float *ckpt, int ckpt_stride);
 
+// bf16 copies of the block-start states ([H][slots of stride 128][dk][dv])
+// from fp32 checkpoints whose stride divides 128.
+cudaError_t launch_states_bf16(const Problem &p, const float *ckpt, int ckpt_stride, __nv_bfloat16 *out);
+
 // Tensor-core forward (tcgen05 / TMEM / TMA): o, hT and checkpoints whose
 // stride is a multiple of 128 tokens, or the block-start ones of fp32
 // checkpoints whose stride divides 128.

@@ -381,4 +381,40 @@ cudaError_t launch_ckpt_expand(const Problem &p, const __nv_bfloat16 *k, const _
     return cudaGetLastError();
 }
 
+// bf16 copies of the states at the 128-token block starts, taken from fp32
+// checkpoints whose stride divides 128, in the layout of the forward's bf16
+// block checkpoints ([H][slots of stride 128][dk][dv]): the backward then
+// loads each block's S_in by one TMA copy.  One CTA per (block slot, head);
+// block slot b is the 128-token span of seg_span(..., b, 1), gaps return.
+__global__ void __launch_bounds__(256)
+states_bf16_kernel(const float *__restrict__ ck, int stride, int64_t ck_slots, __nv_bfloat16 *__restrict__ out,
+                   int64_t out_slots, const int32_t *__restrict__ cu, int T, int64_t tokens, int n_docs, int dk,
+                   int dv)
+{
+    const SegSpan sl = seg_span(cu, T, tokens, n_docs, (int)blockIdx.x, 1);
+    if (!sl.valid || sl.len <= 0)
+        return;
+    const int h = blockIdx.y;
+    const int64_t src = ckpt_slot(sl.doc_start, sl.n, (int64_t)sl.s * 128 / stride, stride);
+    const int64_t dst = ckpt_slot(sl.doc_start, sl.n, sl.s, 128);
+    const float4 *s4 = reinterpret_cast<const float4 *>(ck + ((size_t)h * ck_slots + src) * dk * dv);
+    uint2 *d2 = reinterpret_cast<uint2 *>(out + ((size_t)h * out_slots + dst) * dk * dv);
+    const int n4 = dk * dv / 4;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 x = s4[i];
+        d2[i] = make_uint2(sm100::pack_bf16(x.x, x.y), sm100::pack_bf16(x.z, x.w));
+    }
+}
+
+cudaError_t launch_states_bf16(const Problem &p, const float *ckpt, int ckpt_stride, __nv_bfloat16 *out)
+{
+    if (p.n_docs <= 0 || p.tokens <= 0)
+        return cudaSuccess;
+    const int64_t blocks = (p.tokens + 127) / 128 + p.n_docs;
+    states_bf16_kernel<<<dim3((unsigned)blocks, (unsigned)p.H), 256, 0, p.stream>>>(
+        ckpt, ckpt_stride, ckpt_slots(p, ckpt_stride), out, ckpt_slots(p, 128), p.cu, p.T, p.tokens, p.n_docs,
+        p.dk, p.dv);
+    return cudaGetLastError();
+}
+
 }  // namespace bdla
