@@ -101,7 +101,9 @@ enum { BDLA_OP_FWD = 0, BDLA_OP_BWD = 1, BDLA_OP_DECAY = 2 };
  * the stride of the checkpoints the backward will be handed (0 if none).
  * The stride matters because a backward handed no usable checkpoints
  * (stride 0, or a stride that does not divide 128) recomputes the states
- * before every 128-token block into the workspace.  `mode` does not change
+ * before every 128-token block into the workspace, and one handed fp32
+ * checkpoints inside the blocks (a stride below 128 that divides it) writes
+ * bf16 copies of the block-start states there.  `mode` does not change
  * the size.  Returns 0 on invalid dims.  The first 256 bytes of every
  * workspace are the device status word: zero them once after allocating the
  * workspace (bdla_read_device_status clears them again).
@@ -142,7 +144,8 @@ bdla_status bdla_fwd_varlen(const void *q, const void *k, const void *v, const f
  * dhT = dL/dhT (NULL = 0).  Writes dq, dk, dv, da (dL/da through the decay
  * parameterisation) and, when non-NULL, dh0.  ckpt (with its ckpt_stride) may
  * hold the forward's state checkpoints; NULL makes the backward recompute the
- * states it needs into the workspace.
+ * states it needs into the workspace (fp32 checkpoints with a stride below
+ * 128 are converted there to bf16 block-start states first).
  */
 bdla_status bdla_bwd(const void *q, const void *k, const void *v, const float *a,
                      float b, int chunk, const float *h0, const void *dO, const float *dhT,
