@@ -146,6 +146,32 @@ def test_bf16_block_checkpoints_feed_the_backward(dv):
     compare_all(gpu, run_oracle(inp, w.b, w.mode))
 
 
+@pytest.mark.parametrize("stride,dv", [(16, 256), (32, 128), (64, 256)])
+def test_fp32_inner_checkpoints_give_the_bf16_block_state_gradients(stride, dv):
+    """fp32 checkpoints whose stride divides 128 reach the backward as bf16
+    copies of their block-start states: the gradients are bitwise those of
+    the forward's own bf16 block checkpoints (the same fp32 states rounded the
+    same way), on packed documents of ragged lengths, and meet the oracle's
+    bar.  dv = 256 runs the backward's second value slice."""
+    w = _small("varlen64k", 900, H=2, n_docs=3, dv=dv, h0_std=0.2)
+    inp = make_inputs(w, with_grad=True)
+    g = to_device(inp)
+    grads = {}
+    for s, dt in ((stride, torch.float32), (128, torch.bfloat16)):
+        ws = bdla.Workspace(256, "cuda")
+        o, hT, ck = bdla.fwd(g["q"], g["k"], g["v"], g["a"], w.b, h0=g["h0"], cu_seqlens=g["cu_seqlens"],
+                             ckpt_stride=s, ckpt_dtype=dt, ws=ws)
+        grads[s] = bdla.bwd(g["q"], g["k"], g["v"], g["a"], g["dO"], w.b, h0=g["h0"],
+                            cu_seqlens=g["cu_seqlens"], ckpt=ck, ckpt_stride=s, want_dh0=True, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.read_device_status() == 0
+    for x, y in zip(grads[stride], grads[128]):
+        assert torch.equal(x, y)
+    dq, dk, dv_, da, dh0 = grads[stride]
+    compare_all(dict(dq=dq, dk=dk, dv=dv_, da=da, dh0=dh0), run_oracle(inp, w.b, w.mode),
+                names=("dq", "dk", "dv", "da", "dh0"))
+
+
 @pytest.mark.parametrize("cu", [[0, 100, 50, 300], [0, 100, 200], [0, 500]])
 def test_bad_cu_seqlens_set_device_status(cu):
     w = _small("varlen64k", 300, H=2, n_docs=2)
