@@ -61,6 +61,7 @@ struct FwdSmem {
     float coff[BT];      // e^{gamma_sig - Gamma_s}
     float gq[BT];        // Gamma per row (ablation diagonal path)
     float gam[BT / kChunk];
+    float eg[BT / kChunk];   // e^{gamma_tau}
     uint32_t abl_pair[BT][4];   // ablation: one half's 8 position-pair values of a row (bf16 pairs)
     uint64_t full_qk[2], empty_qk[2], score_full[2];
     uint64_t full_v, empty_v, p_ready, o_full, p_free, drain;
@@ -411,8 +412,10 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float g_last = __shfl_sync(0xffffffffu, g, last & 31);
             const float gam_tau = (16 * tau < Lb) ? g_last : 0.0f;
             epi_sync();   // both halves are done with the previous block's column factors
-            if (half == 0 && (r & 15) == 0)
+            if (half == 0 && (r & 15) == 0) {
                 sm.gam[tau] = gam_tau;
+                sm.eg[tau] = expf(gam_tau);
+            }
             if (half == 0) {
                 if (ABL)
                     sm.gq[r] = g;
@@ -505,10 +508,18 @@ fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             //      c), where the P V GEMM reads them
             if (!STATES) {
                 uint32_t uu[2][16];
-                float f[BT / kChunk];   // per source tile: e^{G_tau - G_sig+1} e^{Gamma_t}
+                // per source tile sg < tau: e^{G_tau - G_sg+1} e^{Gamma_t}, the
+                // product of the tile decays e^{gamma} between sg and tau
+                float f[BT / kChunk];
+                {
+                    float run = rt;
 #pragma unroll
-                for (int sg = 0; sg < BT / kChunk; ++sg)
-                    f[sg] = sg < tau ? rt * expf(Gt - G[sg + 1]) : (sg == tau ? rt : 0.0f);
+                    for (int sg = BT / kChunk - 1; sg >= 0; --sg) {
+                        const bool below = sg < tau;
+                        f[sg] = below ? run : (sg == tau ? rt : 0.0f);
+                        run = below ? run * sm.eg[sg] : run;
+                    }
+                }
 #pragma unroll
                 for (int c = 0; c < BT / 32; ++c) if ((c & 1) == half) {
                     uint32_t (&u)[16] = uu[c >> 1];
