@@ -141,3 +141,19 @@ def test_delta_states_from_the_forward_equal_the_backwards_own():
         assert torch.equal(x, y)
     for x, y in zip(own, handed):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("cu", [[0, 100, 50, 300], [0, 100, 200], [0, 500]])
+def test_delta_bad_cu_seqlens_set_device_status(cu):
+    """Malformed packed offsets: BDLA_ERR_DEVICE from the device-side document
+    check, spans outside the tensors skipped, the context still usable."""
+    w = _delta_case("varlen64k", 300, H=2, n_docs=2)
+    g = to_device(make_inputs(w, with_grad=False))
+    bad = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ws = bdla.Workspace(256, "cuda")
+    bdla.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, cu_seqlens=bad, ws=ws)
+    assert ws.read_device_status() == bdla.ERR_DEVICE
+    assert ws.read_device_status() == 0          # cleared after reading
+    bdla.fwd_delta(g["q"], g["k"], g["v"], g["a"], g["beta"], w.b, cu_seqlens=bad.new_tensor([0, 300]), ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_device_status() == 0

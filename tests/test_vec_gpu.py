@@ -142,3 +142,21 @@ def test_vec_states_from_the_forward_equal_the_backwards_own():
         assert torch.equal(x, y)
     for x, y in zip(own, handed):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("cu", [[0, 100, 50, 300], [0, 100, 200], [0, 500]])
+def test_vec_bad_cu_seqlens_set_device_status(cu):
+    """Malformed packed offsets (a negative length, offsets that stop short of
+    the tensors, a document past their end): the call reports BDLA_ERR_DEVICE
+    from the device-side document check, the kernels skip spans outside the
+    tensors, and the context stays usable."""
+    w = _vec_case("varlen64k", 300, H=2, n_docs=2)
+    g = to_device(make_inputs(w, with_grad=False))
+    bad = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ws = bdla.Workspace(256, "cuda")
+    bdla.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=bad, ws=ws)
+    assert ws.read_device_status() == bdla.ERR_DEVICE
+    assert ws.read_device_status() == 0          # cleared after reading
+    bdla.fwd_vec(g["q"], g["k"], g["v"], g["a"], w.b, cu_seqlens=bad.new_tensor([0, 300]), ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_device_status() == 0
