@@ -240,13 +240,22 @@ seg_summary_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
             if (nblk < 0)
                 continue;
             float run = 0.0f;   // summed log-decay of the blocks already taken
+            // Gamma of the row in block j (0 past the segment end); each block's
+            // value is loaded while the block before it is scaled
+            auto gamma_of = [&](int j) -> float {
+                const bool in = (int64_t)j * BT + r < g.len;
+                return in ? gamma[(int64_t)h * tokens + g.start + (int64_t)j * BT + r] : 0.0f;
+            };
+            float gv_next = nblk > 0 ? gamma_of(BWD ? 0 : nblk - 1) : 0.0f;
             for (int b = 0; b < nblk; ++b, ++gb) {
                 const int j = BWD ? b : nblk - 1 - b;
                 const int s = (int)(gb % kStages);
                 const int Lb = (int)(g.len - (int64_t)j * BT < BT ? g.len - (int64_t)j * BT : BT);
                 const bool valid = r < Lb;
                 const int tau = r >> 4;
-                const float gv = valid ? gamma[(int64_t)h * tokens + g.start + (int64_t)j * BT + r] : 0.0f;
+                const float gv = gv_next;
+                if (b + 1 < nblk)
+                    gv_next = gamma_of(BWD ? b + 1 : nblk - 2 - b);
                 const int lastr = min(16 * tau + 15, Lb - 1);
                 const float g_last = __shfl_sync(0xffffffffu, gv, lastr & 31);
                 row_sync();   // every row has read the previous block's tile totals
