@@ -57,7 +57,6 @@ struct Layout {
     size_t gamma = 0;    // Gamma [H, tokens] fp32 (kernels that read it from memory)
     size_t dfac = 0;     // d lambda / d a [H, tokens] fp32 (backward)
     size_t states = 0;   // recomputed bf16 states for the backward, 0 if unused
-    size_t part = 0;     // partial dq, dk, da of the second dv slice (dv = 256)
     size_t seg = 0;      // segment summaries / initial states [slots, H, dk, dv] fp32
     size_t lsum = 0;     // segment log-decay sums [slots, H] fp32
     size_t order = 0;    // documents by decreasing length, int32 [n_docs]
@@ -102,11 +101,6 @@ Layout layout(int op, const bdla_dims &d, int n_docs, int ckpt_stride)
             L.states = off;
             const int64_t slots = (tokens + kBlock - 1) / kBlock + n_docs;
             off += round_up((size_t)d.H * slots * d.dk * d.dv * 2);
-        }
-        if (d.dv > 128) {
-            L.part = off;
-            off += round_up((size_t)(d.dv / 128 - 1) * (2 * tokens * d.H * d.dk + tokens * d.H) *
-                            sizeof(float));
         }
     }
     const SegPlan sp = plan_of(d, n_docs);
@@ -324,7 +318,7 @@ bdla_status bwd_impl(const void *q, const void *k, const void *v, const float *a
             BDLA_CUDA(launch_seg_scan(p, dhT, true, seg));
         }
     }
-    float *part = L.part ? reinterpret_cast<float *>(wsb + L.part) : nullptr;
+    float *part = nullptr;   // the second dv slice adds into dq, dk, da directly
     {
         KernelMark mark_(BDLA_KERNEL_BWD, p.stream);
         if (convert)

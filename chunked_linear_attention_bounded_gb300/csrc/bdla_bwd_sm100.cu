@@ -202,7 +202,9 @@ __device__ __forceinline__ float block_exclusive_scan(float x, float *warp_tot, 
 // Coalesced store of a warp's 32 rows x 32 fp32 values (lane = row):
 // transposed through a 4 KB shared staging tile (16-byte chunks XOR-swizzled
 // by row, conflict-free) so that each group of 8 lanes writes one row's 128
-// contiguous bytes.  Rows >= n_valid are not written.
+// contiguous bytes (ADD: adds them to what memory holds).  Rows >= n_valid
+// are not written.
+template <bool ADD = false>
 __device__ __forceinline__ void warp_store_rows_f32(unsigned char *stage, const uint32_t (&x)[32],
                                                     float *gbase, size_t row_stride, int n_valid,
                                                     int lane)
@@ -216,8 +218,17 @@ __device__ __forceinline__ void warp_store_rows_f32(unsigned char *stage, const 
     for (int it = 0; it < 8; ++it) {
         const int row = 4 * it + (lane >> 3), c4 = lane & 7;
         const uint4 v = st4[row * 8 + (c4 ^ (row & 7))];
-        if (row < n_valid)
+        if (ADD) {
+            if (row < n_valid) {
+                float *dst = gbase + (size_t)row * row_stride + 4 * c4;
+                atomicAdd(dst, __uint_as_float(v.x));
+                atomicAdd(dst + 1, __uint_as_float(v.y));
+                atomicAdd(dst + 2, __uint_as_float(v.z));
+                atomicAdd(dst + 3, __uint_as_float(v.w));
+            }
+        } else if (row < n_valid) {
             *reinterpret_cast<uint4 *>(gbase + (size_t)row * row_stride + 4 * c4) = v;
+        }
     }
     __syncwarp();
 }
@@ -256,11 +267,14 @@ __device__ __forceinline__ void load_state_row(const void *states, int st_bf16, 
 
 // ABL: unbounded -softplus decay; the diagonal 16-token tiles of P and dP
 // are computed pair by pair on CUDA cores (explicit position-pair path).
-// With dv split over gridDim.z slices, slice z handles value columns
-// [z*DV, (z+1)*DV): dv is exact per slice, while dq, dk and da are partial
-// sums that slice z > 0 writes at offset z*part_qk / z*part_a (added to
-// slice 0 by a separate kernel).
-template <int DV, bool ABL>
+// dv = 256 runs as two value slices of 128 columns, one launch each in stream
+// order: dv is exact per slice, while dq, dk and da are partial sums; the
+// first launch (ADD = false) stores them and the second (ADD = true, columns
+// 128..255) adds its own to them, by TMA reduce-add for full blocks and by
+// atomics for da and a document's last partial block.  (The kernel can still
+// split slices over gridDim.z with partial sums written to `part`; the
+// launcher does not use that.)
+template <int DV, bool ABL, bool ADD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -281,15 +295,15 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     BwdSmem<DV> &sm = *reinterpret_cast<BwdSmem<DV> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x;
-    const int j0 = blockIdx.z * DV;
+    const int j0 = (ADD ? 1 : blockIdx.z) * DV;
     // slice 0 writes dq, dk, da; later slices write partial sums into `part`
-    float *dq = blockIdx.z == 0 ? dq_base : part + (size_t)(blockIdx.z - 1) * (2 * part_qk + part_a);
-    float *dkk = blockIdx.z == 0 ? dk_base : dq + part_qk;
-    float *da = blockIdx.z == 0 ? da_base : dq + 2 * part_qk;
+    float *dq = (ADD || blockIdx.z == 0) ? dq_base : part + (size_t)(blockIdx.z - 1) * (2 * part_qk + part_a);
+    float *dkk = (ADD || blockIdx.z == 0) ? dk_base : dq + part_qk;
+    float *da = (ADD || blockIdx.z == 0) ? da_base : dq + 2 * part_qk;
     // TMA maps of this slice's dq and dk (slice 1: its partial sums), formed
     // where a store needs them
-#define BDLA_MAP_DQ (blockIdx.z == 0 ? &tdq : &tdq1)
-#define BDLA_MAP_DK (blockIdx.z == 0 ? &tdk : &tdk1)
+#define BDLA_MAP_DQ ((ADD || blockIdx.z == 0) ? &tdq : &tdq1)
+#define BDLA_MAP_DK ((ADD || blockIdx.z == 0) ? &tdk : &tdk1)
     // one document, or one segment of it (then the adjoint after its last
     // token comes from seg_init)
     const SegSpan span = seg_span(cu, T, tokens, n_docs,
@@ -664,7 +678,10 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                             int coord;
                             const CUtensorMap *map;
                             item_col(pair ? 2 * k + hh : n_a + (k - ka), coord, map);
-                            tma_store_3d(map, buf + hh * kPanel, coord, h, t0s);
+                            if (ADD && map != &tdv)
+                                tma_reduce_add_3d(map, buf + hh * kPanel, coord, h, t0s);
+                            else
+                                tma_store_3d(map, buf + hh * kPanel, coord, h, t0s);
                         }
                         tma_store_commit();
                         tma_store_wait_read1();   // the round before this one is read
@@ -702,10 +719,17 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     if (warp == 2 && lane == 0) {
                         for (int pi = 0; pi < kStagePanels && base + pi < n_items; ++pi) {
                             const int it = base + pi;
-                            if (it < dk / 32)
-                                tma_store_3d(BDLA_MAP_DQ, sm.z + pi * kPanel, it * 32, h, t0s);
-                            else if (it < 2 * (dk / 32))
-                                tma_store_3d(BDLA_MAP_DK, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
+                            if (it < dk / 32) {
+                                if (ADD)
+                                    tma_reduce_add_3d(BDLA_MAP_DQ, sm.z + pi * kPanel, it * 32, h, t0s);
+                                else
+                                    tma_store_3d(BDLA_MAP_DQ, sm.z + pi * kPanel, it * 32, h, t0s);
+                            } else if (it < 2 * (dk / 32)) {
+                                if (ADD)
+                                    tma_reduce_add_3d(BDLA_MAP_DK, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
+                                else
+                                    tma_store_3d(BDLA_MAP_DK, sm.z + pi * kPanel, (it - dk / 32) * 32, h, t0s);
+                            }
                             else
                                 tma_store_3d(&tdv, sm.z + pi * kPanel, j0 + (it - 2 * (dk / 32)) * 32, h, t0s);
                         }
@@ -727,8 +751,8 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tmem_ld32(t_c3 + lane_off + c * 32, x);
                     tmem_ld32(t_c1 + lane_off + c * 32, y);
                     tmem_ld_wait();
-                    warp_store_rows_f32(stage, x, dq + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
-                    warp_store_rows_f32(stage, y, dkk + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
+                    warp_store_rows_f32<ADD>(stage, x, dq + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
+                    warp_store_rows_f32<ADD>(stage, y, dkk + ((size_t)t_w * H + h) * dk + c * 32, (size_t)H * dk, n_valid, lane);
                 }
 #pragma unroll
                 for (int c = 0; c < DV / 32; ++c) if ((c & 1) == half) {
@@ -771,8 +795,12 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int w = 0; w < 8; ++w)
                 se += sm.se[bp][w];
             const float C = expf(da_lend) * se;
-            if (da_valid && half == 0)
-                da[(size_t)da_t * H + h] = (px + (ty - py) + C) * da_fac;
+            if (da_valid && half == 0) {
+                if (ADD)
+                    atomicAdd(&da[(size_t)da_t * H + h], (px + (ty - py) + C) * da_fac);
+                else
+                    da[(size_t)da_t * H + h] = (px + (ty - py) + C) * da_fac;
+            }
             epi_sync();   // the scan scratch is reused by the next block
             da_pend = false;
         };
@@ -1211,30 +1239,6 @@ bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #undef BDLA_MAP_DQ
 #undef BDLA_MAP_DK
 
-// dq += partial dq of the other dv slices (and dk, da).
-__global__ void add_partials_kernel(float *__restrict__ dq, float *__restrict__ dk,
-                                    float *__restrict__ da, const float *__restrict__ part,
-                                    int64_t n_qk, int64_t n_a, int n_extra)
-{
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_qk; i += stride) {
-        float aq = dq[i], ak = dk[i];
-        for (int z = 0; z < n_extra; ++z) {
-            const float *p = part + (size_t)z * (2 * n_qk + n_a);
-            aq += p[i];
-            ak += p[n_qk + i];
-        }
-        dq[i] = aq;
-        dk[i] = ak;
-    }
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_a; i += stride) {
-        float acc = da[i];
-        for (int z = 0; z < n_extra; ++z)
-            acc += part[(size_t)z * (2 * n_qk + n_a) + 2 * n_qk + i];
-        da[i] = acc;
-    }
-}
-
 template <int DV, bool ABL>
 cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                const CUtensorMap &mv, const CUtensorMap &mdo, const CUtensorMap &mst,
@@ -1244,41 +1248,31 @@ cudaError_t launch_bwd_sm100_t(const Problem &p, const CUtensorMap &mq, const CU
                                const float *dhT, float *dq, float *dk, float *dv, float *da, float *dh0,
                                float *part, const SegPlan &seg)
 {
-    auto kern = bwd_sm100_kernel<DV, ABL>;
+    auto kern0 = bwd_sm100_kernel<DV, ABL, false>;
+    auto kern1 = bwd_sm100_kernel<DV, ABL, true>;
     const size_t smem = sizeof(BwdSmem<DV>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int slices = p.dv / DV;
+    cudaError_t err = cudaFuncSetAttribute(kern0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess && slices > 1)
+        err = cudaFuncSetAttribute(kern1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
-    const int slices = p.dv / DV;
-    const int64_t n_qk = p.tokens * p.H * p.dk, n_a = p.tokens * p.H;
-    dim3 grid(p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs, slices);
-    // the second slice's partial dq and dk leave by TMA stores as well
-    CUtensorMap mdq1 = mdq, mdk1 = mdk;
-    int otma = out_tma;
-    if (slices > 1 && otma &&
-        (!make_grad_map(&mdq1, part, p.dk, p.H, p.tokens) || !make_grad_map(&mdk1, part + n_qk, p.dk, p.H, p.tokens)))
-        otma = 0;
+    dim3 grid(p.H, seg.seg_blk > 0 ? (unsigned)seg.n_slots : (unsigned)p.n_docs, 1);
     const WaitCfg wc = wait_cfg(BDLA_KERNEL_BWD);
-    kern<<<grid, kBwdThreads, smem, p.stream>>>(mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, mdq1, mdk1, otma,
-                                                gamma, dfac, p.cu, p.T,
-                                                p.tokens, p.H,
-                                                p.dk, p.dv, states, st_bf16, st_stride,
-                                                ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0,
-                                                part, n_qk, n_a, p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st,
-                                                wc.ns, wc.stall);
-    if ((err = cudaGetLastError()) != cudaSuccess || slices == 1)
-        return err;
-    add_partials_kernel<<<1184, 256, 0, p.stream>>>(dq, dk, da, part, n_qk, n_a, slices - 1);
-    return cudaGetLastError();
+    // one launch per value slice, in stream order: the first stores dq, dk, da,
+    // the second (ADD) adds its partial sums to them
+    for (int slice = 0; slice < slices; ++slice) {
+        (slice == 0 ? kern0 : kern1)<<<grid, kBwdThreads, smem, p.stream>>>(
+            mq, mk, mv, mdo, mst, st_tma, mdq, mdk, mdvv, mdq, mdk, out_tma, gamma, dfac, p.cu, p.T, p.tokens, p.H,
+            p.dk, p.dv, states, st_bf16, st_stride, ckpt_slots(p, st_stride), dhT, dq, dk, dv, da, dh0, part, 0, 0,
+            p.n_docs, seg.seg_blk, seg.buf, seg.order, p.st, wc.ns, wc.stall);
+        if ((err = cudaGetLastError()) != cudaSuccess)
+            return err;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
-
-size_t bwd_partial_floats(const Problem &p)
-{
-    const int slices = p.dv > 128 ? p.dv / 128 : 1;
-    return (size_t)(slices - 1) * (size_t)(2 * p.tokens * p.H * p.dk + p.tokens * p.H);
-}
 
 cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,

@@ -168,10 +168,10 @@ cudaError_t launch_seg_scan(const Problem &p, const float *init, bool backward, 
 
 // Tensor-core backward.  `states` holds the state before every 128-token
 // block: checkpoints whose stride divides 128, fp32 or bf16.  For dv = 256
-// the value columns are split in two slices; `part` (bwd_partial_floats
-// floats of workspace) receives the second slice's partial dq, dk, da.
-// Gamma and d lambda / d a ([H][tokens]) come from the decay kernel.
-size_t bwd_partial_floats(const Problem &p);
+// the value columns are split in two slices, launched one after the other:
+// the first stores dq, dk, da and the second adds its partial sums to them
+// (`part` is not used).  Gamma and d lambda / d a ([H][tokens]) come from the
+// decay kernel.
 cudaError_t launch_bwd_sm100(const Problem &p, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                              const __nv_bfloat16 *v, const __nv_bfloat16 *dO, const float *gamma,
                              const float *dfac, const void *states, int st_bf16, int st_stride,
